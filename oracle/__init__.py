@@ -1,0 +1,18 @@
+"""Plain, slow CPU oracle for the paged-KV attention path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product package imports this
+module; only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm may call it.  It shares no code with the CUDA path.
+
+Everything is numpy float64 computed straight from the definition of
+attention over a paged cache: gather K/V in logical order through the block
+table, then softmax(q k^T * scale + mask) v.  See ``paged_attention.py``.
+"""
+from .paged_attention import (  # noqa: F401
+    bf16_bits_to_f64,
+    kv_append,
+    gather_sequence,
+    attend_rows,
+    paged_decode,
+    paged_varlen,
+)
