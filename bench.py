@@ -1,0 +1,464 @@
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step of the default workload (Qwen3-4B-shaped decode step, one layer:
+64 sequences with 256..2048 cached tokens, 32 query / 8 kv heads, head_dim
+128, 16-token pages in a shuffled 16384-page pool) is:
+    paged_kv_append (64 new K/V rows)  ->  paged_attn_decode (split + merge)
+The headline value is achieved HBM GB/s: algorithmic bytes of the step
+(every attended K/V byte once, q, out, the appended rows) divided by the
+device time of the step.  L2 is flushed (256 MB write) before every step,
+outside the timed events.  A second object reports the continuous-batching
+mixed step (8 prefill chunks + 120 decode rows) in tokens/s.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of 8 TB/s); mixed-step tokens/sec"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+            tf = d.get("bf16_tflops") or d.get("bf16")
+            tfs = d.get("bf16_tflops_sustained") or tf
+            if hbm:
+                return float(hbm), float(tf or FALLBACK_BF16_TFLOPS), float(
+                    tfs or FALLBACK_BF16_TFLOPS), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str):
+        self.bus = bus_id.lower()[-12:] if bus_id else ""
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=5).stdout
+                for line in out.strip().splitlines():
+                    f = [x.strip() for x in line.split(",")]
+                    if len(f) >= 9 and (not self.bus or f[0].lower().endswith(self.bus)):
+                        self.rows.append(f)
+                        break
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# -------------------------------------------------------------- byte models
+def decode_bytes(step: wl.Step) -> int:
+    """Algorithmic HBM bytes of one decode call: each attended K and V row
+    once (window-limited), q in, out, block-table entries and lengths."""
+    L = step.dec_seq_lens.astype(np.int64)
+    if step.window > 0:
+        L = np.minimum(L, step.window)
+    kv = int(L.sum()) * step.H_kv * step.D * 2 * 2
+    qo = step.Bd * step.H_q * step.D * 2 * 2
+    bt = int(np.sum(-(-L // step.P))) * 4 + step.Bd * 4
+    return kv + qo + bt
+
+
+def append_bytes(step: wl.Step, n_rows: int) -> int:
+    return n_rows * step.H_kv * step.D * 2 * 2 * 2 + n_rows * 8
+
+
+def varlen_flops(step: wl.Step) -> float:
+    """4*D*H_q flops per unmasked (query, key) pair (QK^T and PV)."""
+    pairs = 0
+    for c in range(step.Bp):
+        q, p = int(step.pre_qlen[c]), int(step.pre_prefix[c])
+        pos = p + np.arange(q)
+        n = pos + 1
+        if step.window > 0:
+            n = np.minimum(n, step.window)
+        pairs += int(n.sum())
+    return 4.0 * step.D * step.H_q * pairs
+
+
+# --------------------------------------------------------- device workload
+class DeviceStep:
+    """A step's inputs resident on the GPU (values drawn on the device)."""
+
+    def __init__(self, step: wl.Step, seed: int, device):
+        import torch
+        self.step = step
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        shape = (step.num_pages, step.H_kv, step.P, step.D)
+        bf = torch.bfloat16
+        self.k_cache = torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(bf)
+        if step.k_head_scale is not None:
+            s = torch.from_numpy(step.k_head_scale).to(device).view(1, -1, 1, 1)
+            self.k_cache = (self.k_cache.float() * s).to(bf)
+        self.v_cache = torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(bf)
+        n_new = step.n_new_tokens
+        self.k_new = torch.randn((n_new, step.H_kv, step.D), generator=g, device=device).to(bf)
+        self.v_new = torch.randn((n_new, step.H_kv, step.D), generator=g, device=device).to(bf)
+        self.slots = torch.from_numpy(step.all_slots).to(device)
+        self.q_dec = torch.randn((step.Bd, step.H_q, step.D), generator=g, device=device).to(bf) \
+            if step.Bd else None
+        self.out_dec = torch.empty_like(self.q_dec) if step.Bd else None
+        self.q_pre = torch.randn((step.total_q, step.H_q, step.D), generator=g,
+                                 device=device).to(bf) if step.Bp else None
+        self.out_pre = torch.empty_like(self.q_pre) if step.Bp else None
+        if step.Bd:
+            self.dec_bt = torch.from_numpy(step.dec_block_table).to(device)
+            self.dec_lens = torch.from_numpy(step.dec_seq_lens).to(device)
+        if step.Bp:
+            self.pre_bt = torch.from_numpy(step.pre_block_table).to(device)
+            self.cu_q = torch.from_numpy(step.cu_seq_lens_q).to(device)
+            self.cu_k = torch.from_numpy(step.cu_seq_lens_k).to(device)
+        import paged_kv_attention_11_gb300 as pkv
+        self.pkv = pkv
+        need = pkv.decode_workspace_size(max(step.Bd, 1), step.H_q, step.H_kv, step.D)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def append(self, stream):
+        self.pkv.paged_kv_append(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
+                                 err_flag=self.err, stream=stream)
+
+    def varlen(self, stream):
+        s = self.step
+        self.pkv.paged_attn_varlen(self.out_pre, self.q_pre, self.k_cache, self.v_cache,
+                                   self.cu_q, self.cu_k, self.pre_bt, s.max_seqlen_q(),
+                                   s.max_seqlen_k(), s.scale, True, s.window,
+                                   err_flag=self.err, stream=stream)
+
+    def decode(self, stream):
+        s = self.step
+        self.pkv.paged_attn_decode(self.out_dec, self.q_dec, self.k_cache, self.v_cache,
+                                   self.dec_bt, self.dec_lens, s.max_seq_len_dec(), s.scale,
+                                   s.window, workspace=self.ws, err_flag=self.err,
+                                   stream=stream)
+
+
+def time_steps(fn_phases, steps, warmup, stream, flush):
+    """Run warmup + steps; returns per-step per-phase device ms (events)."""
+    import torch
+    for _ in range(warmup):
+        for f in fn_phases:
+            f(stream)
+    torch.cuda.synchronize()
+    recs = []
+    for _ in range(steps):
+        flush()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(fn_phases) + 1)]
+        evs[0].record(stream)
+        for i, f in enumerate(fn_phases):
+            f(stream)
+            evs[i + 1].record(stream)
+        recs.append(evs)
+    torch.cuda.synchronize()
+    return [[recs[k][i].elapsed_time(recs[k][i + 1]) for i in range(len(fn_phases))]
+            for k in range(steps)]
+
+
+# --------------------------------------------------------------- ours arm
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_attention_11_gb300 import build
+    build.build()
+
+    hbm_peak, tf_peak, tf_sus, peak_src = peaks()
+    stream = torch.cuda.Stream(device)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush():
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(1)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- headline: Qwen3-shaped decode step -------------------------------
+    step = wl.qwen3_decode()
+    ds = DeviceStep(step, wl.BASE_SEED + 2 + 1000 * rank, device)
+    torch.cuda.synchronize()
+    bus = ""
+    try:
+        bus = torch.cuda.get_device_properties(device).pci_bus_id
+    except Exception:
+        pass
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clocks:
+        per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush)
+    torch.cuda.synchronize()
+    barrier()
+    assert int(ds.err.item()) == 0, f"device error flag {int(ds.err.item())}"
+    step_ms = float(np.mean([sum(p) for p in per]))
+    dec_ms = float(np.mean([p[1] for p in per]))
+    app_ms = float(np.mean([p[0] for p in per]))
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms, dec_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, dec_ms = float(t[0]), float(t[1])
+    dbytes = decode_bytes(step)
+    abytes = append_bytes(step, step.n_new_tokens)
+    value = ws * (dbytes + abytes) / (step_ms * 1e-3) / 1e9
+    dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers ---------------
+    e2e = run_e2e(ds, step, stream, flush, args, dbytes + abytes)
+
+    # ---- secondary: mixed continuous-batching step (tokens/s) -------------
+    mixed = run_mixed(args, device, stream, flush, rank)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, bf16 ~N(0,1), K scaled per kv head by U(0.5,2))",
+        "config": {"workload": "qwen3_decode: one layer, batch 64, cached ~U[256,2048], "
+                               "H_q 32 / H_kv 8, head_dim 128, page 16, 16384-page shuffled "
+                               "pool; step = append 64 rows + decode",
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "pct_of_8TBs": round(100.0 * value / ws / NOMINAL_HBM_GBS, 2),
+        "decode_only": {"gb_s": round(dec_gbs, 2), "us": round(dec_ms * 1e3, 2),
+                        "pct_of_8TBs": round(100 * dec_gbs / NOMINAL_HBM_GBS, 2)},
+        "append_us": round(app_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "kernel": "paged_attn_decode (split-KV pass + merge pass)",
+                     "achieved": round(dec_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / hbm_peak, 4), "peak_source": peak_src,
+                     "algorithmic_bytes": dbytes, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "mixed_step": mixed,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(step, ds, rank)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes):
+    """Same step through the public API, inputs from pinned host memory."""
+    import torch
+    host = {
+        "q": ds.q_dec.cpu().pin_memory(), "k_new": ds.k_new.cpu().pin_memory(),
+        "v_new": ds.v_new.cpu().pin_memory(), "slots": ds.slots.cpu().pin_memory(),
+        "bt": ds.dec_bt.cpu().pin_memory(), "lens": ds.dec_lens.cpu().pin_memory(),
+    }
+    out_h = torch.empty(ds.out_dec.shape, dtype=ds.out_dec.dtype).pin_memory()
+    dev = {k: torch.empty_like(v, device=ds.q_dec.device) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    pkv = ds.pkv
+
+    def full(s):
+        with torch.cuda.stream(s):
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            pkv.paged_kv_append(dev["k_new"], dev["v_new"], ds.k_cache, ds.v_cache,
+                                dev["slots"], err_flag=ds.err, stream=s)
+            pkv.paged_attn_decode(ds.out_dec, dev["q"], ds.k_cache, ds.v_cache, dev["bt"],
+                                  dev["lens"], step.max_seq_len_dec(), step.scale, step.window,
+                                  workspace=ds.ws, err_flag=ds.err, stream=s)
+            out_h.copy_(ds.out_dec, non_blocking=True)
+
+    per = time_steps([full], args.steps, args.warmup, stream, flush)
+    ms = float(np.mean([p[0] for p in per]))
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+def run_mixed(args, device, stream, flush, rank):
+    """Continuous-batching mixed step: append all new rows, varlen prefill of
+    8 chunks, decode of 120 sequences.  Tokens/s = new tokens / step time."""
+    import torch
+    try:
+        step = wl.mixed_step()
+        ds = DeviceStep(step, wl.BASE_SEED + 3 + 1000 * rank, device)
+        per = time_steps([ds.append, ds.varlen, ds.decode], args.steps, args.warmup, stream,
+                         flush)
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            return {"unavailable": f"device error flag {int(ds.err.item())}"}
+    except Exception as e:  # varlen not available yet, etc.
+        return {"unavailable": f"{type(e).__name__}: {e}"}
+    ms = float(np.mean([sum(p) for p in per]))
+    ph = np.mean(np.array(per), axis=0)
+    tokens = step.n_new_tokens
+    fl = varlen_flops(step)
+    _, tf_peak, _, src = peaks()
+    return {"metric": "mixed-step tokens/sec", "value": round(tokens / (ms * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(ms, 5), "tokens_per_step": int(tokens),
+            "workload": "mixed_step: 8 prefill chunks (len ~U[128,1024] on prefix ~U[0,512]) + "
+                        "120 decode rows (cached ~U[64,4096]); H 32/8/128, page 16",
+            "phase_us": {"append": round(ph[0] * 1e3, 2), "varlen": round(ph[1] * 1e3, 2),
+                         "decode": round(ph[2] * 1e3, 2)},
+            "varlen_roofline": {"bound": "tensor", "achieved": round(fl / (ph[1] * 1e-3) / 1e12, 2),
+                                "peak": tf_peak, "unit": "TFLOP/s",
+                                "frac": round(fl / (ph[1] * 1e-3) / 1e12 / tf_peak, 4),
+                                "peak_source": src, "algorithmic_flops": fl},
+            "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2)}
+
+
+# ---------------------------------------------------------- CPU baselines
+def oracle_decode_sample(step: wl.Step, vals: wl.StepValues, seqs):
+    """Time the oracle (append + decode) on the given sequences."""
+    import oracle
+    t0 = time.perf_counter()
+    slots = step.dec_slots[seqs]
+    hk, hv = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new[seqs], vals.v_new[seqs],
+                              slots)
+    oracle.paged_decode(vals.q_dec[0][seqs], hk, hv, step.dec_block_table[seqs],
+                        step.dec_seq_lens[seqs], step.scale, step.window)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(step: wl.Step, seqs) -> int:
+    L = step.dec_seq_lens[seqs].astype(np.int64)
+    return int(L.sum()) * step.H_kv * step.D * 4 + len(seqs) * step.H_q * step.D * 4 + \
+        len(seqs) * step.H_kv * step.D * 8
+
+
+def host_values(step: wl.Step) -> wl.StepValues:
+    return wl.fill_values(step, wl.BASE_SEED + 2)
+
+
+def cpu_baseline(step: wl.Step, ds, rank, budget_s: float = 12.0):
+    vals = host_values(step)
+    seqs_all = np.arange(step.Bd)
+    t = 0.0
+    nbytes = 0
+    k = 0
+    while t < budget_s and k < 50:
+        seqs = seqs_all[(k * 8) % step.Bd:(k * 8) % step.Bd + 8]
+        t += oracle_decode_sample(step, vals, seqs)
+        nbytes += sample_bytes(step, seqs)
+        k += 1
+    return {"value": round(nbytes / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{k} x (append + decode of 8 of the 64 sequences), {t:.1f} s of "
+                      f"single-threaded numpy fp64 on host ({os.cpu_count()} cores present)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    step = wl.qwen3_decode()
+    vals = host_values(step)
+    for k in range(args.warmup):
+        oracle_decode_sample(step, vals, np.arange(k % 8 * 8, k % 8 * 8 + 8))
+    times, nbytes = [], 0
+    for k in range(args.steps):
+        seqs = np.arange((k * 8) % step.Bd, (k * 8) % step.Bd + 8)
+        times.append(oracle_decode_sample(step, vals, seqs))
+        nbytes += sample_bytes(step, seqs)
+    t = sum(times)
+    v = nbytes / t / 1e9
+    line = {"metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "qwen3_decode (one step = append + decode of 8 of the 64 "
+                                   "sequences, fp64 CPU oracle)"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "8 sequences per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

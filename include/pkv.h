@@ -1,0 +1,173 @@
+/*
+ * pkv.h - C ABI of the paged-KV attention library (GB300, sm_103a).
+ *
+ * The operations follow the paged-KV rollout engine described in the
+ * scripts/benchmarks commit log ("Why this works": one contiguous page pool
+ * plus a page table mapping (sequence, logical block) -> physical page;
+ * "Files": new K/V rows are written in-kernel to their physical slot before
+ * attention reads them) and the varlen interface of the cb_sync_driver.py
+ * commit message (phase-2 fixes: cu_seq_lens_q on every paged forward) and
+ * the README "Integration notes" (max_seqlen_q / max_seqlen_k).  The sliding
+ * window rule (causal AND q_pos - kv_pos < window, strict) is the Gemma-4
+ * sliding-window commit of the same log.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller; the
+ *   library never allocates, frees, synchronises the host, or keeps a
+ *   pointer after returning.  Work is enqueued on `stream` (a cudaStream_t
+ *   passed as void*; NULL = legacy default stream) and runs asynchronously.
+ * - bf16 means IEEE bfloat16 (2 bytes).  Every tensor is dense and
+ *   row-major (C order) with the shape given below.
+ * - Page pools: k_cache and v_cache are separate tensors of shape
+ *   [num_pages, num_kv_heads, page_size, head_dim] bf16.  Token position p
+ *   of a sequence with block-table row T lives in page T[p / page_size],
+ *   row p % page_size.  A slot is page * page_size + row.
+ * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * - Supported shapes: head_dim in {64, 128, 256}; page_size a multiple of
+ *   16 (16 and 64 are the tested sizes); num_q_heads a multiple of
+ *   num_kv_heads with a group of at most 8 for decode and dividing 128 for
+ *   varlen.  Anything else returns PKV_ERR_UNSUPPORTED.
+ * - Host-detectable argument errors return PKV_ERR_INVALID before anything
+ *   is enqueued.  CUDA launch errors return PKV_ERR_CUDA (message from
+ *   pkv_last_cuda_error()).
+ * - Data-dependent errors never fault and never trap: the offending row or
+ *   page is skipped (masked out) and, if `err_flag` is non-NULL, the bits
+ *   below are OR-ed into that device int32.  The caller clears it.
+ * - Base pointers must be 16-byte aligned (k_cache/v_cache/q/out/k_new/
+ *   v_new); otherwise PKV_ERR_INVALID.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = 1,     /* bad argument detected on the host; nothing enqueued */
+  PKV_ERR_UNSUPPORTED = 2, /* well-formed but outside the supported shapes */
+  PKV_ERR_CUDA = 3         /* a CUDA runtime/driver call failed */
+} pkv_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PKV_DEVERR_SLOT    1  /* slot >= num_pages*page_size: that row was not written */
+#define PKV_DEVERR_PAGE    2  /* block-table entry outside [0, num_pages): its keys masked */
+#define PKV_DEVERR_LEN     4  /* a length exceeded max_blocks_per_seq*page_size or the
+                                 declared maximum: clamped */
+#define PKV_DEVERR_TIMEOUT 8  /* an internal pipeline wait gave up (never expected) */
+
+/*
+ * paged_kv_append - scatter this step's new K/V rows into the page pools.
+ *
+ * Source: scripts/benchmarks commit log, "Files" paragraph of the flex
+ * paged-KV engine commit (in-kernel k_cache[addr] = k_val write of each new
+ * row to its physical address; one reserved no-op slot for padded rows).
+ *
+ *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] bf16 (read)
+ *   k_cache,v_cache[num_pages, num_kv_heads, page_size, head_dim] bf16 (written)
+ *   slot_mapping   [num_tokens] int64: destination slot of row t; a negative
+ *                  slot means "skip this row" (padding)
+ *
+ * Rows are copied bit-exactly.  Slots must be distinct within one call
+ * (duplicates race; the winner is unspecified).  num_tokens == 0 is a no-op.
+ */
+pkv_status paged_kv_append(const void* k_new, const void* v_new,
+                           void* k_cache, void* v_cache,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           int32_t page_size, int64_t num_pages,
+                           int32_t* err_flag, void* stream);
+
+/*
+ * paged_attn_decode_workspace_size - bytes of device scratch that
+ * paged_attn_decode needs for this batch shape (on the current device).
+ */
+size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * paged_attn_decode - one query token per sequence attends its whole paged
+ * prefix (the decode step of the rollout engine: scripts/benchmarks commit
+ * log, "Why this works", page-table routing of every decode query).
+ *
+ *   out          [batch, num_q_heads, head_dim] bf16 (written)
+ *   q            [batch, num_q_heads, head_dim] bf16
+ *   block_table  [batch, max_blocks_per_seq] int32 physical page ids;
+ *                entries past ceil(seq_len/page_size) are never read
+ *   seq_lens     [batch] int32: keys of sequence b (its new token included,
+ *                i.e. append first); the query sits at position seq_len-1.
+ *                seq_len 0 gives a zero output row.
+ *   scale        multiplier of q.k (typically 1/sqrt(head_dim))
+ *   window       > 0: only keys with (seq_len-1) - pos < window are read;
+ *                <= 0: no window
+ *   max_seq_len  an upper bound on seq_lens (sizes the launch; larger
+ *                lengths are clamped to max_blocks_per_seq*page_size and
+ *                flagged)
+ *   workspace    device scratch of paged_attn_decode_workspace_size() bytes,
+ *                256-byte aligned; its contents need not be initialised
+ *
+ * Computed as a balanced split-KV pass (every CTA streams the same number
+ * of 16-key tiles across sequence boundaries) followed by a merge pass of
+ * the per-split partial outputs and log-sum-exps.
+ */
+pkv_status paged_attn_decode(void* out, const void* q,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch,
+                             int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t page_size, int64_t num_pages,
+                             int32_t max_seq_len, float scale, int32_t window,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t* err_flag, void* stream);
+
+/*
+ * paged_attn_varlen - packed variable-length attention over the paged cache
+ * (prefill chunks of the continuous-batching step).  Source: the
+ * cb_sync_driver.py commit message (cu_seq_lens_q on every paged forward),
+ * README "Integration notes" (max_seqlen_q / max_seqlen_k), and the
+ * document-causal / sliding-window masks of the scripts/benchmarks log.
+ *
+ *   out            [total_q, num_q_heads, head_dim] bf16 (written)
+ *   q              [total_q, num_q_heads, head_dim] bf16
+ *   cu_seq_lens_q  [batch+1] int32, non-decreasing, cu_seq_lens_q[0] = 0,
+ *                  cu_seq_lens_q[batch] = total_q
+ *   cu_seq_lens_k  [batch+1] int32: k_len of chunk b is
+ *                  cu_seq_lens_k[b+1]-cu_seq_lens_k[b] (cached prefix plus
+ *                  the chunk, already appended) and must be >= its q_len
+ *   block_table    [batch, max_blocks_per_seq] int32
+ *   max_seqlen_q, max_seqlen_k  upper bounds of q_len / k_len (size the
+ *                  launch; longer chunks are clamped and flagged)
+ *   causal         1: query i of a chunk sits at position k_len - q_len + i
+ *                  (bottom-right) and sees keys <= its position;
+ *                  0: every key of the chunk (window must then be <= 0)
+ *   window         > 0 (causal only): also require q_pos - k_pos < window
+ *
+ * Runs QK^T and PV on the tcgen05 tensor cores with TMEM accumulators.
+ */
+pkv_status paged_attn_varlen(void* out, const void* q,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* cu_seq_lens_q, const int32_t* cu_seq_lens_k,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             int32_t batch, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                             int32_t total_q,
+                             int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t page_size, int64_t num_pages,
+                             float scale, int32_t causal, int32_t window,
+                             int32_t* err_flag, void* stream);
+
+/* Human-readable name of a pkv_status value (static string). */
+const char* pkv_status_string(int32_t status);
+
+/* Message of the last CUDA error seen by this library on the calling host
+ * thread ("" if none). */
+const char* pkv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

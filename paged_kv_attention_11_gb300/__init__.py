@@ -1,0 +1,26 @@
+"""Paged-KV attention for GB300 (sm_103a): Python binding of libpkv.so.
+
+Three calls, same names as the C ABI (include/pkv.h):
+
+* ``paged_kv_append``   scatter new K/V rows into the page pools
+* ``paged_attn_decode`` one query per sequence over its paged prefix
+* ``paged_attn_varlen`` packed variable-length (prefill) attention
+
+This module only marshals arguments (device pointers, sizes, the current
+CUDA stream) into the library; every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if libpkv.so is missing the
+calls raise.
+"""
+from ._binding import (  # noqa: F401
+    PKVError,
+    DEVERR_LEN,
+    DEVERR_PAGE,
+    DEVERR_SLOT,
+    DEVERR_TIMEOUT,
+    decode_workspace_size,
+    lib,
+    lib_path,
+    paged_attn_decode,
+    paged_attn_varlen,
+    paged_kv_append,
+)

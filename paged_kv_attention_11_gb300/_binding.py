@@ -1,0 +1,152 @@
+"""ctypes marshalling for libpkv.so (argument packing only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libpkv.so")
+_lib: Optional[ctypes.CDLL] = None
+
+DEVERR_SLOT = 1
+DEVERR_PAGE = 2
+DEVERR_LEN = 4
+DEVERR_TIMEOUT = 8
+
+_c_i32, _c_i64, _c_p, _c_f = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+_SIGS = {
+    "paged_kv_append": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64,
+                        _c_p, _c_p],
+    "paged_attn_decode_workspace_size": [_c_i32, _c_i32, _c_i32, _c_i32],
+    "paged_attn_decode": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_i32,
+                          _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_p, ctypes.c_size_t,
+                          _c_p, _c_p],
+    "paged_attn_varlen": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32,
+                          _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f, _c_i32,
+                          _c_i32, _c_p, _c_p],
+    "pkv_status_string": [_c_i32],
+    "pkv_last_cuda_error": [],
+}
+_RES = {"paged_attn_decode_workspace_size": ctypes.c_size_t,
+        "pkv_status_string": ctypes.c_char_p, "pkv_last_cuda_error": ctypes.c_char_p}
+
+
+class PKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        L = lib()
+        msg = L.pkv_status_string(status).decode()
+        if status == 3:
+            msg += ": " + L.pkv_last_cuda_error().decode()
+        super().__init__(f"{fn} -> {msg}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpkv.so (built by paged_kv_attention_11_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m paged_kv_attention_11_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = _RES.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise PKVError(fn, status)
+
+
+def _bf16(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+
+
+def paged_kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                    err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k_new/v_new [T, H_kv, D]; caches [num_pages, H_kv, P, D]; slots [T] int64."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    num_pages, H_kv, P, D = k_cache.shape
+    _check("paged_kv_append", lib().paged_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+        k_new.shape[0], H_kv, D, P, num_pages, _ptr(err_flag), _stream(stream)))
+
+
+def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().paged_attn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim))
+
+
+def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                      max_seq_len: int, scale: float, window: int = 0,
+                      workspace: Optional[torch.Tensor] = None,
+                      err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out/q [B, H_q, D]; block_table [B, max_blocks] int32; seq_lens [B] int32."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    B, H_q, D = q.shape
+    num_pages, H_kv, P, _ = k_cache.shape
+    need = decode_workspace_size(B, H_q, H_kv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("paged_attn_decode", lib().paged_attn_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
+        float(scale), int(window), _ptr(workspace), workspace.numel(), _ptr(err_flag),
+        _stream(stream)))
+    return out
+
+
+def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, cu_seq_lens_q: torch.Tensor,
+                      cu_seq_lens_k: torch.Tensor, block_table: torch.Tensor,
+                      max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool = True,
+                      window: int = 0, err_flag: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """out/q [total_q, H_q, D]; cu_seq_lens_* [B+1] int32; block_table [B, max_blocks]."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    for n, t in (("cu_seq_lens_q", cu_seq_lens_q), ("cu_seq_lens_k", cu_seq_lens_k),
+                 ("block_table", block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    total_q, H_q, D = q.shape
+    num_pages, H_kv, P, _ = k_cache.shape
+    _check("paged_attn_varlen", lib().paged_attn_varlen(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seq_lens_q),
+        _ptr(cu_seq_lens_k), _ptr(block_table), block_table.shape[1],
+        cu_seq_lens_q.shape[0] - 1, int(max_seqlen_q), int(max_seqlen_k), total_q, H_q, H_kv,
+        D, P, num_pages, float(scale), 1 if causal else 0, int(window), _ptr(err_flag),
+        _stream(stream)))
+    return out

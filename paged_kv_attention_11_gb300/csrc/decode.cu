@@ -1,0 +1,563 @@
+// paged_attn_decode: one query per sequence over its paged K/V prefix.
+//
+// Semantics: scripts/benchmarks commit log, "Why this works" (decode reads
+// the pool through the page table; the new token is written first, so the
+// query at position len-1 sees keys 0..len-1) and the Gemma-4 sliding-window
+// commit (key allowed iff q_pos - k_pos < window).
+//
+// Design (GB300):
+//  * Work unit = one 16-key tile of one (sequence, kv head).  All units of
+//    the batch are laid end to end (sequence-major, then kv head) and the
+//    grid of N CTAs cuts that line into N equal ranges, so every CTA streams
+//    the same number of bytes whatever the length mix ("balanced split-KV").
+//    A CTA range that covers a whole (sequence, kv head) writes the bf16
+//    output directly; ranges that cut one produce partial (o, lse) pieces
+//    that the merge kernel combines.
+//  * A producer warp walks the range, looks the pages up in the block table
+//    (32 entries per coalesced load) and issues 2-D TMA box loads
+//    (64 x 16 bf16, 128-byte swizzle) of the K and V tile into an NSTAGE
+//    ring guarded by mbarriers.
+//  * NW consumer warps take the tiles round-robin.  Per tile a warp computes
+//    S^T = K Q^T (16 keys x 8 heads, GQA group padded to 8) with mma.sync,
+//    does the online softmax (exp2, warp shuffles), transposes P in
+//    registers with movmatrix and accumulates O^T = V^T P^T with mma.sync.
+//    K/V bytes are read from HBM exactly once; Q (<= 8 heads) lives in
+//    registers.
+//  * Each piece ends with a cross-warp LSE combine in shared memory.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+constexpr int kTile = 16;  // keys per pipeline stage
+constexpr int kGP = 8;     // GQA group padded to the mma N dimension
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t max_blocks;
+  int32_t batch;
+  int32_t H_q, H_kv, G, P;
+  int64_t num_pages;
+  int32_t window;
+  float scale_log2;
+  int32_t* cum;      // [batch+1] written by CTA 0 for the merge kernel
+  float* part_lse;   // [(S + N) * G]
+  float* part_o;     // [(S + N) * G * D]
+  int32_t* err;
+};
+
+// Keys [lo, L) of sequence b are attended; returns the tile range.
+__device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, int& lo,
+                                           int& t_lo, int& t_hi, bool flag) {
+  int len = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks * a.P;
+  if (len < 0 || len > cap) {
+    if (flag) raise_err(a.err, PKV_DEVERR_LEN);
+    len = len < 0 ? 0 : cap;
+  }
+  L = len;
+  lo = (a.window > 0 && len > a.window) ? len - a.window : 0;
+  t_lo = lo / kTile;
+  t_hi = (len + kTile - 1) / kTile;
+}
+
+// CTA c of N owns units [c*W/N, (c+1)*W/N).  The CTA that owns unit x:
+__device__ __forceinline__ int owner_cta(int64_t x, int64_t W, int64_t N) {
+  return (int)(((x + 1) * N + W - 1) / W - 1);
+}
+
+__device__ __forceinline__ bool cta_range_empty(int64_t c, int64_t W, int64_t N) {
+  return c * W / N == (c + 1) * W / N;
+}
+
+template <int D, int NW, int NSTAGE>
+struct DecodeSmem {
+  static constexpr int kTileBytes = kTile * D * 2;           // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
+  static constexpr int kCombStride = D + 4;                  // padded row (floats)
+  static constexpr int kStagesOff = 0;
+  static constexpr int kCombOff = NSTAGE * kStageBytes;      // [NW][8][D+4] fp32
+  static constexpr int kMLOff = kCombOff + NW * kGP * kCombStride * 4;  // [NW][8][2]
+  static constexpr int kBarOff = kMLOff + NW * kGP * 2 * 4;
+  static constexpr int kOkOff = kBarOff + 2 * NSTAGE * 8;
+  static constexpr int kScanOff = kOkOff + NSTAGE * 4;       // [NW+1] warp sums
+  static constexpr int kCumOff = ((kScanOff + (NW + 1) * 4) + 15) & ~15;
+  static size_t bytes(int batch) { return 1024 + kCumOff + (size_t)(batch + 1) * 4; }
+};
+
+template <int D, int NW, int NSTAGE>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
+  static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+  using L_ = DecodeSmem<D, NW, NSTAGE>;
+  constexpr int NT = (NW + 1) * 32;
+  constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
+  constexpr int kBoxBytes = kTile * 128;  // one 64-column box of a tile
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* comb_o = reinterpret_cast<float*>(smem + L_::kCombOff);
+  float* comb_ml = reinterpret_cast<float*>(smem + L_::kMLOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::kBarOff);
+  uint64_t* empty = full + NSTAGE;
+  int* stage_ok = reinterpret_cast<int*>(smem + L_::kOkOff);
+  int* scan_tmp = reinterpret_cast<int*>(smem + L_::kScanOff);
+  int* s_cum = reinterpret_cast<int*>(smem + L_::kCumOff);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int B = a.batch;
+
+  // ---- prefix sum of work units over sequences (every CTA, in smem) ----
+  {
+    const int per = (B + NT - 1) / NT;
+    const int b0 = tid * per;
+    int local = 0;
+    for (int b = b0; b < b0 + per && b < B; ++b) {
+      int L, lo, tl, th;
+      seq_extent(a, b, L, lo, tl, th, blockIdx.x == 0);
+      local += (th - tl) * a.H_kv;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan_tmp[warp] = incl;
+    if (tid == 0) {
+      for (int i = 0; i < 2 * NSTAGE; ++i) mbar_init(full + i, 1);  // full[] and empty[]
+      fence_mbar_init();
+    }
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += scan_tmp[w];
+    int run = base + incl - local;
+    for (int b = b0; b < b0 + per && b < B; ++b) {
+      s_cum[b] = run;
+      int L, lo, tl, th;
+      seq_extent(a, b, L, lo, tl, th, false);
+      run += (th - tl) * a.H_kv;
+    }
+    if (tid == NT - 1) s_cum[B] = run;
+    __syncthreads();
+  }
+  const int64_t W = s_cum[B];
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= B; i += NT) a.cum[i] = s_cum[i];
+  }
+  const int64_t N = gridDim.x;
+  const int64_t x0 = (int64_t)blockIdx.x * W / N;
+  const int64_t x1 = ((int64_t)blockIdx.x + 1) * W / N;
+  if (x0 >= x1) return;
+
+  // first sequence of the range: last b with s_cum[b] <= x0
+  int b_first;
+  {
+    int lo = 0, hi = B;  // s_cum[lo] <= x0 < s_cum[hi]
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (s_cum[mid] <= x0) lo = mid; else hi = mid;
+    }
+    b_first = lo;
+  }
+
+  if (warp == NW) {
+    // ============================ producer warp ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    bool dead = false;
+    int64_t x = x0;
+    int b = b_first;
+    int it = 0;  // CTA-wide tile counter
+    while (x < x1) {
+      int L, lo, t_lo, t_hi;
+      seq_extent(a, b, L, lo, t_lo, t_hi, false);
+      const int tiles_b = t_hi - t_lo;
+      const int64_t bstart = s_cum[b];
+      if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) { ++b; continue; }
+      const int g = (int)((x - bstart) / tiles_b);
+      const int64_t seg_start = bstart + (int64_t)g * tiles_b;
+      const int64_t seg_end = seg_start + tiles_b;
+      const int64_t p_end = seg_end < x1 ? seg_end : x1;
+      const int n = (int)(p_end - x);
+      const int first_tile = t_lo + (int)(x - seg_start);
+      const int* bt = a.block_table + (int64_t)b * a.max_blocks;
+      for (int k0 = 0; k0 < n; k0 += 32) {
+        int page = -1;
+        if (k0 + lane < n) {
+          const int key0 = (first_tile + k0 + lane) * kTile;
+          page = __ldg(bt + key0 / a.P);
+        }
+        const int cnt = min(32, n - k0);
+        for (int j = 0; j < cnt; ++j) {
+          const int pg = __shfl_sync(0xffffffffu, page, j);
+          if (lane == 0) {
+            const int s = it % NSTAGE;
+            const int r = it / NSTAGE;
+            if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
+            const int key0 = (first_tile + k0 + j) * kTile;
+            const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
+            stage_ok[s] = ok ? 1 : 0;
+            if (ok) {
+              uint8_t* st = smem + s * L_::kStageBytes;
+              mbar_arrive_expect_tx(full + s, L_::kStageBytes);
+              const int row = key0 % a.P;
+              const int z = pg * a.H_kv + g;
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c) {
+                tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
+                tma_load_3d(st + L_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row, z);
+              }
+            } else {
+              raise_err(a.err, PKV_DEVERR_PAGE);
+              mbar_arrive(full + s);
+            }
+          }
+          ++it;
+        }
+      }
+      x = p_end;
+      if (x >= seg_end && g == a.H_kv - 1) ++b;
+    }
+    // drain: every issued load must land before the CTA may exit
+    if (lane == 0) {
+      const int first = it > NSTAGE ? it - NSTAGE : 0;
+      for (int i = first; i < it; ++i)
+        mbar_wait(full + (i % NSTAGE), (i / NSTAGE) & 1, a.err, dead);
+    }
+    return;
+  }
+
+  // ============================== consumer warps ============================
+  const int quad = lane >> 2;  // 0..7: key row (QK) / head (Q frag)
+  const int qlan = lane & 3;   // 0..3: head pair (2*qlan, 2*qlan+1)
+  bool dead = false;
+  int64_t x = x0;
+  int b = b_first;
+  int it_base = 0;
+  while (x < x1) {
+    int L, lo, t_lo, t_hi;
+    seq_extent(a, b, L, lo, t_lo, t_hi, false);
+    const int tiles_b = t_hi - t_lo;
+    const int64_t bstart = s_cum[b];
+    if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) { ++b; continue; }
+    const int g = (int)((x - bstart) / tiles_b);
+    const int64_t seg_start = bstart + (int64_t)g * tiles_b;
+    const int64_t seg_end = seg_start + tiles_b;
+    const int64_t p_end = seg_end < x1 ? seg_end : x1;
+    const int n = (int)(p_end - x);
+    const int first_tile = t_lo + (int)(x - seg_start);
+
+    // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan.
+    uint32_t qb[KS][2];
+    {
+      const bool hv = quad < a.G;
+      const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.H_q + g * a.G + (hv ? quad : 0)) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t v0 = 0, v1 = 0;
+        if (hv) {
+          v0 = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * qlan));
+          v1 = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * qlan));
+        }
+        qb[ks][0] = v0;
+        qb[ks][1] = v1;
+      }
+    }
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+
+    // tiles k of this piece with (it_base + k) % NW == warp
+    int k = ((warp - it_base) % NW + NW) % NW;
+    for (; k < n; k += NW) {
+      const int it = it_base + k;
+      const int s = it % NSTAGE;
+      const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
+      const bool ok = landed && stage_ok[s] != 0;
+      const uint32_t stK = smem_u32(smem + s * L_::kStageBytes);
+      const uint32_t stV = stK + L_::kTileBytes;
+      const int key0 = (first_tile + k) * kTile;
+
+      // ---- S^T = K Q^T: 16 keys x 8 heads, two accumulation chains ----
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t rowaddr = stK + key * 128;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int chunk = 2 * ks + (lane >> 4);
+          const uint32_t addr =
+              rowaddr + (chunk >> 3) * kBoxBytes + (((chunk & 7) ^ (lane & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(addr, a0, a1, a2, a3);
+          if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+      }
+      // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
+      const int kA = key0 + quad, kB = kA + 8;
+      const bool vA = ok && kA >= lo && kA < L;
+      const bool vB = ok && kB >= lo && kB < L;
+      float x0A = vA ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;  // key kA, head A
+      float x0B = vA ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;  // key kA, head B
+      float x1A = vB ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;  // key kB, head A
+      float x1B = vB ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;  // key kB, head B
+      float tA = fmaxf(x0A, x1A), tB = fmaxf(x0B, x1B);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, off));
+        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, off));
+      }
+      const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+      const float uA = nA == -INFINITY ? 0.f : nA;
+      const float uB = nB == -INFINITY ? 0.f : nB;
+      const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
+      const float p0A = exp2f(x0A - uA), p0B = exp2f(x0B - uB);
+      const float p1A = exp2f(x1A - uA), p1B = exp2f(x1B - uB);
+      lA = lA * alA + p0A + p1A;
+      lB = lB * alB + p0B + p1B;
+      mA = nA;
+      mB = nB;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        o[i][0] *= alA;
+        o[i][1] *= alB;
+        o[i][2] *= alA;
+        o[i][3] *= alB;
+      }
+      // P^T as the B operand: transpose the 8x8 (key x head) blocks in registers
+      const uint32_t pb0 = movmatrix_t(pack_bf16(p0A, p0B));
+      const uint32_t pb1 = movmatrix_t(pack_bf16(p1A, p1B));
+
+      // ---- O^T += V^T P^T: D/16 m-tiles of 16 dims x 8 heads ----
+      {
+        const int j = lane >> 3;
+        const int key = (lane & 7) + (j >> 1) * 8;
+        const uint32_t rowaddr = stV + key * 128;
+#pragma unroll
+        for (int md = 0; md < KS; ++md) {
+          const int chunk = 2 * md + (j & 1);
+          const uint32_t addr =
+              rowaddr + (chunk >> 3) * kBoxBytes + (((chunk & 7) ^ (lane & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(addr, a0, a1, a2, a3);
+          mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+
+    // ---- combine the NW warps' partial softmax states for this piece ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lA += __shfl_xor_sync(0xffffffffu, lA, off);
+      lB += __shfl_xor_sync(0xffffffffu, lB, off);
+    }
+    {
+      float* co = comb_o + warp * kGP * L_::kCombStride;
+      const int hA = 2 * qlan, hB = hA + 1;
+#pragma unroll
+      for (int md = 0; md < KS; ++md) {
+        const int d = md * 16 + quad;
+        co[hA * L_::kCombStride + d] = o[md][0];
+        co[hB * L_::kCombStride + d] = o[md][1];
+        co[hA * L_::kCombStride + d + 8] = o[md][2];
+        co[hB * L_::kCombStride + d + 8] = o[md][3];
+      }
+      if (quad == 0) {
+        comb_ml[(warp * kGP + hA) * 2 + 0] = mA;
+        comb_ml[(warp * kGP + hA) * 2 + 1] = lA;
+        comb_ml[(warp * kGP + hB) * 2 + 0] = mB;
+        comb_ml[(warp * kGP + hB) * 2 + 1] = lB;
+      }
+    }
+    named_bar_sync(1, NW * 32);
+    const bool whole = seg_start >= x0 && seg_end <= x1;
+    const int64_t piece = (int64_t)b * a.H_kv + g + blockIdx.x;
+    for (int e = tid; e < a.G * D; e += NW * 32) {
+      const int h = e / D, d = e - (e / D) * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_ml[(w * kGP + h) * 2]);
+      float acc = 0.f, lsum = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float sc = exp2f(comb_ml[(w * kGP + h) * 2] - M);
+          acc += sc * comb_o[(w * kGP + h) * L_::kCombStride + d];
+          lsum += sc * comb_ml[(w * kGP + h) * 2 + 1];
+        }
+      }
+      const float val = lsum > 0.f ? acc / lsum : 0.f;
+      if (whole) {
+        a.out[((int64_t)b * a.H_q + g * a.G + h) * D + d] = __float2bfloat16_rn(val);
+      } else {
+        a.part_o[(piece * a.G + h) * D + d] = val;
+        if (d == 0) a.part_lse[piece * a.G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+      }
+    }
+    named_bar_sync(1, NW * 32);
+
+    it_base += n;
+    x = p_end;
+    if (x >= seg_end && g == a.H_kv - 1) ++b;
+  }
+}
+
+// Merge pass: one warp per (sequence, query head).  Zero-length sequences
+// get a zero row here; single-piece sequences were finished by the split
+// pass.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t nctas) {
+  constexpr int PER = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
+  if (pair >= (int64_t)a.batch * a.H_q) return;
+  const int b = (int)(pair / a.H_q);
+  const int h = (int)(pair - (int64_t)b * a.H_q);
+  const int g = h / a.G, hh = h - g * a.G;
+  const int64_t W = a.cum[a.batch];
+  const int64_t c0b = a.cum[b], c1b = a.cum[b + 1];
+  const int64_t tiles = (c1b - c0b) / a.H_kv;
+  __nv_bfloat16* orow = a.out + pair * D;
+  if (tiles == 0) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) orow[lane * PER + i] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int64_t seg_start = c0b + g * tiles, seg_end = seg_start + tiles;
+  const int cf = owner_cta(seg_start, W, nctas);
+  const int cl = owner_cta(seg_end - 1, W, nctas);
+  if (cf == cl) return;
+  const int64_t seg = (int64_t)b * a.H_kv + g;
+  // CTAs whose range is empty (possible when the grid has more CTAs than
+  // units) wrote no piece.
+  float M = -INFINITY;
+  for (int c = cf + lane; c <= cl; c += 32)
+    if (!cta_range_empty(c, W, nctas)) M = fmaxf(M, a.part_lse[(seg + c) * a.G + hh]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int c = cf; c <= cl; ++c) {
+      if (cta_range_empty(c, W, nctas)) continue;
+      const int64_t pc = (seg + c) * a.G + hh;
+      const float w = exp2f(a.part_lse[pc] - M);
+      wsum += w;
+      const float* src = a.part_o + pc * D + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += w * src[i];
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) orow[lane * PER + i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+// --------------------------------------------------------------- host side
+template <int D>
+struct DecodeCfg;
+template <> struct DecodeCfg<64> { static constexpr int NW = 4, NSTAGE = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<128> { static constexpr int NW = 4, NSTAGE = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<256> { static constexpr int NW = 4, NSTAGE = 4, CTAS_PER_SM = 2; };
+
+static int decode_ctas_per_sm(int D) {
+  switch (D) {
+    case 64: return DecodeCfg<64>::CTAS_PER_SM;
+    case 128: return DecodeCfg<128>::CTAS_PER_SM;
+    default: return DecodeCfg<256>::CTAS_PER_SM;
+  }
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
+  const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
+  const int64_t pieces = (int64_t)batch * H_kv + nmax;
+  const int64_t G = H_q / H_kv;
+  return align256((size_t)(batch + 1) * 4) + align256((size_t)pieces * G * 4) +
+         align256((size_t)pieces * G * D * 4);
+}
+
+template <int D>
+static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                   int max_seq_len, cudaStream_t stream, int num_sms) {
+  using C = DecodeCfg<D>;
+  using L_ = DecodeSmem<D, C::NW, C::NSTAGE>;
+  auto kern = decode_split_kernel<D, C::NW, C::NSTAGE>;
+  const size_t smem = L_::bytes(a.batch);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  // grid: enough CTAs to fill the GPU, but >= ~4 tiles each on the longest
+  // possible batch
+  int64_t max_keys = max_seq_len;
+  if (a.window > 0 && max_keys > a.window) max_keys = a.window;
+  const int64_t max_units = (int64_t)a.batch * a.H_kv * ((max_keys + kTile - 1) / kTile + 1);
+  int64_t n = (int64_t)num_sms * C::CTAS_PER_SM;
+  if (n > (max_units + 3) / 4) n = (max_units + 3) / 4;
+  if (n < 1) n = 1;
+  kern<<<(unsigned)n, (C::NW + 1) * 32, smem, stream>>>(a, tmK, tmV);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t pairs = (int64_t)a.batch * a.H_q;
+  decode_merge_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(a, (int32_t)n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
+                          int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
+                          float scale, int32_t window, void* workspace, int32_t* err,
+                          cudaStream_t stream, int num_sms) {
+  DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.max_blocks = max_blocks;
+  a.batch = batch;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.G = H_q / H_kv;
+  a.P = P;
+  a.num_pages = num_pages;
+  a.window = window;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
+  const int64_t pieces = (int64_t)batch * H_kv + nmax;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.cum = reinterpret_cast<int32_t*>(ws);
+  ws += align256((size_t)(batch + 1) * 4);
+  a.part_lse = reinterpret_cast<float*>(ws);
+  ws += align256((size_t)pieces * a.G * 4);
+  a.part_o = reinterpret_cast<float*>(ws);
+  a.err = err;
+  switch (D) {
+    case 64: return launch_decode_t<64>(a, tmK, tmV, max_seq_len, stream, num_sms);
+    case 128: return launch_decode_t<128>(a, tmK, tmV, max_seq_len, stream, num_sms);
+    case 256: return launch_decode_t<256>(a, tmK, tmV, max_seq_len, stream, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,39 @@
+// Internal launch interface between the C ABI layer (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int32_t num_tokens, int32_t H_kv,
+                             int32_t D, int32_t P, int64_t num_pages, int32_t* err,
+                             cudaStream_t stream, int num_sms);
+
+size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms);
+
+cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, const int32_t* block_table, int32_t max_blocks,
+                          const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
+                          int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
+                          float scale, int32_t window, void* workspace, int32_t* err,
+                          cudaStream_t stream, int num_sms);
+
+struct VarlenMaps {
+  CUtensorMap q;  // 4-D view of q: {D, G, H_kv, total_q}
+  CUtensorMap k;  // 3-D view of the K pool: {D, P, num_pages*H_kv}
+  CUtensorMap v;  // same for V
+};
+
+cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,
+                          const int32_t* cu_k, const int32_t* block_table, int32_t max_blocks,
+                          int32_t batch, int32_t max_seqlen_q, int32_t total_q, int32_t H_q,
+                          int32_t H_kv, int32_t D, int32_t P, int64_t num_pages, float scale,
+                          int32_t causal, int32_t window, int32_t* err, cudaStream_t stream,
+                          int num_sms);
+
+}  // namespace pkv

@@ -1,0 +1,116 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+symbol that include/pkv.h declares, and rejects bad arguments on the host
+(before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_11_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                            src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("paged_kv_append", "paged_attn_decode", "paged_attn_varlen",
+              "paged_attn_decode_workspace_size", "pkv_status_string", "pkv_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libpkv.so does not export {n}"
+
+
+def test_status_strings(lib):
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(1) == b"PKV_ERR_INVALID"
+    assert lib.pkv_status_string(2) == b"PKV_ERR_UNSUPPORTED"
+    assert lib.pkv_status_string(3) == b"PKV_ERR_CUDA"
+
+
+def _bind(lib):
+    import paged_kv_attention_11_gb300._binding as b
+    for name, args in b._SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = b._RES.get(name, ctypes.c_int)
+    return lib
+
+
+def test_host_validation_rejects_before_cuda(lib):
+    L = _bind(lib)
+    P = 0x1000  # fake, never dereferenced: validation fails first
+    # append: negative token count, zero heads
+    assert L.paged_kv_append(P, P, P, P, P, -1, 8, 128, 16, 64, None, None) == 1
+    assert L.paged_kv_append(P, P, P, P, P, 4, 0, 128, 16, 64, None, None) == 1
+    # append: head_dim not a multiple of 8 -> unsupported
+    assert L.paged_kv_append(P, P, P, P, P, 4, 8, 100, 16, 64, None, None) == 2
+    # append of zero rows is a no-op
+    assert L.paged_kv_append(None, None, None, None, None, 0, 8, 128, 16, 64, None, None) == 0
+    # decode: H_q not a multiple of H_kv
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 6, 4, 128, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 1
+    # decode: head_dim 96 / page size 8 / group of 16 unsupported
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 8, 2, 96, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 2
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 8, 2, 128, 8, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 2
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 32, 2, 128, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 2
+    # decode: NaN scale, missing pointers
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 8, 2, 128, 16, 64, 64, float("nan"), 0,
+                               P, 1 << 20, None, None) == 1
+    assert L.paged_attn_decode(None, P, P, P, P, 4, P, 2, 8, 2, 128, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 1
+    # decode: misaligned q
+    assert L.paged_attn_decode(P, P + 2, P, P, P, 4, P, 2, 8, 2, 128, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 1
+    # varlen: window without causal, causal not 0/1
+    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 8, 2, 128, 16, 64,
+                               0.1, 0, 16, None, None) == 1
+    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 8, 2, 128, 16, 64,
+                               0.1, 2, 0, None, None) == 1
+    # varlen: group that does not divide 128
+    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 6, 2, 128, 16, 64,
+                               0.1, 1, 0, None, None) == 2
+    # zero-size batches are no-ops
+    assert L.paged_attn_decode(None, None, None, None, None, 4, None, 0, 8, 2, 128, 16, 64, 0,
+                               0.1, 0, None, 0, None, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import paged_kv_attention_11_gb300._binding as b
+    monkeypatch.setattr(b, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(b, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        b.lib()
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_attention_11_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.replace("oracles", ""), f
