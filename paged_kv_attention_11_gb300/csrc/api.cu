@@ -214,6 +214,9 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   pkv::VarlenMaps maps;
   const int kv_rows = head_dim == 256 ? 64 : 128;  // keys per KV tile
   const int box_rows = page_size < kv_rows ? page_size : kv_rows;
+  // a KV tile must be whole page slices: page_size divides it or is a
+  // multiple of it
+  if (kv_rows % page_size != 0 && page_size % kv_rows != 0) return PKV_ERR_UNSUPPORTED;
   if (!encode_q_map(&maps.q, q, head_dim, G, num_kv_heads, total_q) ||
       !encode_pool_map_rows(&maps.k, k_cache, head_dim, page_size, num_pages, num_kv_heads,
                             box_rows) ||

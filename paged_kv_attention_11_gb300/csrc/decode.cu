@@ -473,10 +473,24 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
 }
 
 // --------------------------------------------------------------- host side
+// Launch shape per head_dim: consumer warps, pipeline stages (16-key K+V
+// tiles) per CTA, resident CTAs per SM.  Overridable at build time for
+// tuning sweeps.
+#ifndef PKV_DEC_NW
+#define PKV_DEC_NW 4
+#endif
+#ifndef PKV_DEC_NSTAGE
+#define PKV_DEC_NSTAGE 8
+#endif
+#ifndef PKV_DEC_CTAS
+#define PKV_DEC_CTAS 2
+#endif
 template <int D>
 struct DecodeCfg;
 template <> struct DecodeCfg<64> { static constexpr int NW = 4, NSTAGE = 8, CTAS_PER_SM = 2; };
-template <> struct DecodeCfg<128> { static constexpr int NW = 4, NSTAGE = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<128> {
+  static constexpr int NW = PKV_DEC_NW, NSTAGE = PKV_DEC_NSTAGE, CTAS_PER_SM = PKV_DEC_CTAS;
+};
 template <> struct DecodeCfg<256> { static constexpr int NW = 4, NSTAGE = 4, CTAS_PER_SM = 2; };
 
 static int decode_ctas_per_sm(int D) {
@@ -504,9 +518,18 @@ static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const C
   using L_ = DecodeSmem<D, C::NW, C::NSTAGE>;
   auto kern = decode_split_kernel<D, C::NW, C::NSTAGE>;
   const size_t smem = L_::bytes(a.batch);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // Raise the dynamic shared-memory limit once per device (and again only
+  // if a larger batch needs more).
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < (int)smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = (int)smem;
+  }
   // grid: enough CTAs to fill the GPU, but >= ~4 tiles each on the longest
   // possible batch
   int64_t max_keys = max_seq_len;
