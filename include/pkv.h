@@ -109,11 +109,17 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *                lengths are clamped to max_blocks_per_seq*page_size and
  *                flagged)
  *   workspace    device scratch of paged_attn_decode_workspace_size() bytes,
- *                256-byte aligned; its contents need not be initialised
+ *                256-byte aligned.  Zero-fill it once before its first use
+ *                (e.g. cudaMemsetAsync); every call leaves it zero-filled
+ *                again, so it can be reused by later calls in stream order.
+ *                Calls that overlap on the GPU need separate workspaces.
+ *                After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
  *
- * Computed as a balanced split-KV pass (every CTA streams the same number
- * of 16-key tiles across sequence boundaries) followed by a merge pass of
- * the per-split partial outputs and log-sum-exps.
+ * One kernel launch: a balanced split-KV pass (every CTA streams the same
+ * number of 16-key tiles, cutting across sequence boundaries); partial
+ * outputs of a sequence cut between CTAs are merged (log-sum-exp weights)
+ * by whichever CTA finishes its piece last, found with an arrival counter
+ * kept in the workspace.
  */
 pkv_status paged_attn_decode(void* out, const void* q,
                              const void* k_cache, const void* v_cache,

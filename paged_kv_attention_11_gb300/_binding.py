@@ -119,7 +119,7 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     num_pages, H_kv, P, _ = k_cache.shape
     need = decode_workspace_size(B, H_q, H_kv, D)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
     _check("paged_attn_decode", lib().paged_attn_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),

@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, int64_t total_vecs,
     int32_t vecs_per_tok, int32_t vecs_per_row, int32_t H_kv, int32_t P, int64_t num_slots,
     int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total_vecs; i += stride) {
     const int64_t t = i / vecs_per_tok;
@@ -50,11 +52,19 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, total,
-      vecs_per_tok, vecs_per_row, H_kv, P, num_pages * P, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<const uint4*>(k_new),
+                            static_cast<const uint4*>(v_new), static_cast<uint4*>(k_cache),
+                            static_cast<uint4*>(v_cache), slot_mapping, total, vecs_per_tok,
+                            vecs_per_row, H_kv, P, num_pages * P, err);
 }
 
 }  // namespace pkv

@@ -11,8 +11,11 @@
 //    grid of N CTAs cuts that line into N equal ranges, so every CTA streams
 //    the same number of bytes whatever the length mix ("balanced split-KV").
 //    A CTA range that covers a whole (sequence, kv head) writes the bf16
-//    output directly; ranges that cut one produce partial (o, lse) pieces
-//    that the merge kernel combines.
+//    output directly; ranges that cut one produce partial (o, lse) pieces.
+//    The last CTA to finish a piece of a (sequence, kv head) -- found with
+//    a per-segment arrival counter in the workspace -- merges all its
+//    pieces (log-sum-exp weighting) and writes the output, then resets the
+//    counter to zero.  No CTA ever waits for another.
 //  * A producer warp walks the range, looks the pages up in the block table
 //    (32 entries per coalesced load) and issues 2-D TMA box loads
 //    (64 x 16 bf16, 128-byte swizzle) of the K and V tile into an NSTAGE
@@ -24,6 +27,9 @@
 //    K/V bytes are read from HBM exactly once; Q (<= 8 heads) lives in
 //    registers.
 //  * Each piece ends with a cross-warp LSE combine in shared memory.
+//  * Launched with programmatic dependent launch: the prologue overlaps the
+//    previous kernel in the stream (e.g. the append that wrote the new
+//    token); griddepcontrol.wait precedes every read of the inputs.
 #include <math.h>
 
 #include "common.cuh"
@@ -45,7 +51,7 @@ struct DecodeArgs {
   int64_t num_pages;
   int32_t window;
   float scale_log2;
-  int32_t* cum;      // [batch+1] written by CTA 0 for the merge kernel
+  int32_t* seg_count;  // [batch * H_kv] arrival counters, zero between calls
   float* part_lse;   // [(S + N) * G]
   float* part_o;     // [(S + N) * G * D]
   int32_t* err;
@@ -85,7 +91,7 @@ struct DecodeSmem {
   static constexpr int kMLOff = kCombOff + NW * kGP * kCombStride * 4;  // [NW][8][2]
   static constexpr int kBarOff = kMLOff + NW * kGP * 2 * 4;
   static constexpr int kOkOff = kBarOff + 2 * NSTAGE * 8;
-  static constexpr int kScanOff = kOkOff + NSTAGE * 4;       // [NW+1] warp sums
+  static constexpr int kScanOff = kOkOff + NSTAGE * 4 + 16;  // [NW+1] warp sums
   static constexpr int kCumOff = ((kScanOff + (NW + 1) * 4) + 15) & ~15;
   static size_t bytes(int batch) { return 1024 + kCumOff + (size_t)(batch + 1) * 4; }
 };
@@ -111,11 +117,20 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   int* stage_ok = reinterpret_cast<int*>(smem + L_::kOkOff);
   int* scan_tmp = reinterpret_cast<int*>(smem + L_::kScanOff);
   int* s_cum = reinterpret_cast<int*>(smem + L_::kCumOff);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + L_::kOkOff + NSTAGE * 4);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int B = a.batch;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2 * NSTAGE; ++i) mbar_init(full + i, 1);  // full[] and empty[]
+    fence_mbar_init();
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  pdl_wait();  // inputs may come from the previous kernel in the stream
 
   // ---- prefix sum of work units over sequences (every CTA, in smem) ----
   {
@@ -126,6 +141,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       int L, lo, tl, th;
       seq_extent(a, b, L, lo, tl, th, blockIdx.x == 0);
       local += (th - tl) * a.H_kv;
+      // zero-length sequences have no work unit: their zero rows are written here
+      if (L == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
+        for (int i = 0; i < a.H_q * D; ++i)
+          a.out[(int64_t)b * a.H_q * D + i] = __float2bfloat16_rn(0.f);
+      }
     }
     int incl = local;
 #pragma unroll
@@ -134,10 +154,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       if (lane >= o) incl += v;
     }
     if (lane == 31) scan_tmp[warp] = incl;
-    if (tid == 0) {
-      for (int i = 0; i < 2 * NSTAGE; ++i) mbar_init(full + i, 1);  // full[] and empty[]
-      fence_mbar_init();
-    }
     __syncthreads();
     int base = 0;
     for (int w = 0; w < warp; ++w) base += scan_tmp[w];
@@ -151,10 +167,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     if (tid == NT - 1) s_cum[B] = run;
     __syncthreads();
   }
+  pdl_launch_dependents();
   const int64_t W = s_cum[B];
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= B; i += NT) a.cum[i] = s_cum[i];
-  }
   const int64_t N = gridDim.x;
   const int64_t x0 = (int64_t)blockIdx.x * W / N;
   const int64_t x1 = ((int64_t)blockIdx.x + 1) * W / N;
@@ -173,10 +187,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   if (warp == NW) {
     // ============================ producer warp ============================
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
     bool dead = false;
     int64_t x = x0;
     int b = b_first;
@@ -388,7 +398,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     }
     named_bar_sync(1, NW * 32);
     const bool whole = seg_start >= x0 && seg_end <= x1;
-    const int64_t piece = (int64_t)b * a.H_kv + g + blockIdx.x;
+    const int64_t seg = (int64_t)b * a.H_kv + g;
+    const int64_t piece = seg + blockIdx.x;
     for (int e = tid; e < a.G * D; e += NW * 32) {
       const int h = e / D, d = e - (e / D) * D;
       float M = -INFINITY;
@@ -411,6 +422,43 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         if (d == 0) a.part_lse[piece * a.G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
       }
     }
+    if (!whole) {
+      // arrival counter: the last CTA to deliver a piece of this segment
+      // merges all of them (nobody waits; the counter is reset afterwards)
+      __threadfence();
+      named_bar_sync(1, NW * 32);
+      const int cf = owner_cta(seg_start, W, N);
+      const int cl = owner_cta(seg_end - 1, W, N);
+      if (tid == 0) {
+        int npieces = 0;
+        for (int c = cf; c <= cl; ++c) npieces += cta_range_empty(c, W, N) ? 0 : 1;
+        const int old = atomicAdd(a.seg_count + seg, 1);
+        *merge_flag = (old == npieces - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, NW * 32);
+      if (*merge_flag) {
+        __threadfence();
+        for (int e = tid; e < a.G * D; e += NW * 32) {
+          const int h = e / D, d = e - (e / D) * D;
+          float M = -INFINITY;
+          for (int c = cf; c <= cl; ++c)
+            if (!cta_range_empty(c, W, N)) M = fmaxf(M, __ldcg(a.part_lse + (seg + c) * a.G + h));
+          float acc = 0.f, wsum = 0.f;
+          if (M != -INFINITY) {
+            for (int c = cf; c <= cl; ++c) {
+              if (cta_range_empty(c, W, N)) continue;
+              const int64_t pc = (seg + c) * a.G + h;
+              const float w = exp2f(__ldcg(a.part_lse + pc) - M);
+              wsum += w;
+              acc += w * __ldcg(a.part_o + pc * D + d);
+            }
+          }
+          a.out[((int64_t)b * a.H_q + g * a.G + h) * D + d] =
+              __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+        }
+        if (tid == 0) a.seg_count[seg] = 0;
+      }
+    }
     named_bar_sync(1, NW * 32);
 
     it_base += n;
@@ -419,79 +467,26 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   }
 }
 
-// Merge pass: one warp per (sequence, query head).  Zero-length sequences
-// get a zero row here; single-piece sequences were finished by the split
-// pass.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t nctas) {
-  constexpr int PER = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
-  if (pair >= (int64_t)a.batch * a.H_q) return;
-  const int b = (int)(pair / a.H_q);
-  const int h = (int)(pair - (int64_t)b * a.H_q);
-  const int g = h / a.G, hh = h - g * a.G;
-  const int64_t W = a.cum[a.batch];
-  const int64_t c0b = a.cum[b], c1b = a.cum[b + 1];
-  const int64_t tiles = (c1b - c0b) / a.H_kv;
-  __nv_bfloat16* orow = a.out + pair * D;
-  if (tiles == 0) {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) orow[lane * PER + i] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  const int64_t seg_start = c0b + g * tiles, seg_end = seg_start + tiles;
-  const int cf = owner_cta(seg_start, W, nctas);
-  const int cl = owner_cta(seg_end - 1, W, nctas);
-  if (cf == cl) return;
-  const int64_t seg = (int64_t)b * a.H_kv + g;
-  // CTAs whose range is empty (possible when the grid has more CTAs than
-  // units) wrote no piece.
-  float M = -INFINITY;
-  for (int c = cf + lane; c <= cl; c += 32)
-    if (!cta_range_empty(c, W, nctas)) M = fmaxf(M, a.part_lse[(seg + c) * a.G + hh]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int c = cf; c <= cl; ++c) {
-      if (cta_range_empty(c, W, nctas)) continue;
-      const int64_t pc = (seg + c) * a.G + hh;
-      const float w = exp2f(a.part_lse[pc] - M);
-      wsum += w;
-      const float* src = a.part_o + pc * D + lane * PER;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += w * src[i];
-    }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) orow[lane * PER + i] = __float2bfloat16_rn(acc[i] * inv);
-}
-
 // --------------------------------------------------------------- host side
 // Launch shape per head_dim: consumer warps, pipeline stages (16-key K+V
 // tiles) per CTA, resident CTAs per SM.  Overridable at build time for
 // tuning sweeps.
 #ifndef PKV_DEC_NW
-#define PKV_DEC_NW 4
+#define PKV_DEC_NW 2
 #endif
 #ifndef PKV_DEC_NSTAGE
-#define PKV_DEC_NSTAGE 8
+#define PKV_DEC_NSTAGE 4
 #endif
 #ifndef PKV_DEC_CTAS
-#define PKV_DEC_CTAS 2
+#define PKV_DEC_CTAS 4
 #endif
 template <int D>
 struct DecodeCfg;
-template <> struct DecodeCfg<64> { static constexpr int NW = 4, NSTAGE = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<64> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 4; };
 template <> struct DecodeCfg<128> {
   static constexpr int NW = PKV_DEC_NW, NSTAGE = PKV_DEC_NSTAGE, CTAS_PER_SM = PKV_DEC_CTAS;
 };
-template <> struct DecodeCfg<256> { static constexpr int NW = 4, NSTAGE = 4, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 2; };
 
 static int decode_ctas_per_sm(int D) {
   switch (D) {
@@ -503,11 +498,12 @@ static int decode_ctas_per_sm(int D) {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace: [seg_count: batch*H_kv int32][part_lse: pieces*G f32][part_o: pieces*G*D f32]
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
   const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
   const int64_t pieces = (int64_t)batch * H_kv + nmax;
   const int64_t G = H_q / H_kv;
-  return align256((size_t)(batch + 1) * 4) + align256((size_t)pieces * G * 4) +
+  return align256((size_t)batch * H_kv * 4) + align256((size_t)pieces * G * 4) +
          align256((size_t)pieces * G * D * 4);
 }
 
@@ -530,7 +526,7 @@ static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const C
     if (e != cudaSuccess) return e;
     configured[dev] = (int)smem;
   }
-  // grid: enough CTAs to fill the GPU, but >= ~4 tiles each on the longest
+  // grid: one wave of resident CTAs, but >= ~4 tiles each on the longest
   // possible batch
   int64_t max_keys = max_seq_len;
   if (a.window > 0 && max_keys > a.window) max_keys = a.window;
@@ -538,12 +534,17 @@ static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const C
   int64_t n = (int64_t)num_sms * C::CTAS_PER_SM;
   if (n > (max_units + 3) / 4) n = (max_units + 3) / 4;
   if (n < 1) n = 1;
-  kern<<<(unsigned)n, (C::NW + 1) * 32, smem, stream>>>(a, tmK, tmV);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t pairs = (int64_t)a.batch * a.H_q;
-  decode_merge_kernel<D><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(a, (int32_t)n);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n);
+  cfg.blockDim = dim3((C::NW + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tmK, tmV);
 }
 
 cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
@@ -569,8 +570,8 @@ cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
   const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
   const int64_t pieces = (int64_t)batch * H_kv + nmax;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.cum = reinterpret_cast<int32_t*>(ws);
-  ws += align256((size_t)(batch + 1) * 4);
+  a.seg_count = reinterpret_cast<int32_t*>(ws);
+  ws += align256((size_t)batch * H_kv * 4);
   a.part_lse = reinterpret_cast<float*>(ws);
   ws += align256((size_t)pieces * a.G * 4);
   a.part_o = reinterpret_cast<float*>(ws);

@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(192, 1)
   const int qt = a.num_qtiles - 1 - (int)blockIdx.x;  // long (late) tiles first
   const int QP = 128 >> a.log2G;                       // query positions per tile
 
+  pdl_wait();  // inputs may come from the previous kernel in the stream
+  pdl_launch_dependents();
   const int q0 = __ldg(a.cu_q + b);
   int q_len = __ldg(a.cu_q + b + 1) - q0;
   int k_len = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
@@ -427,9 +429,17 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps, 
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(a.num_qtiles, a.H_kv, batch);
-  kern<<<grid, 192, S_::kBytes, stream>>>(a, maps.q, maps.k, maps.v);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_qtiles, a.H_kv, batch);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = S_::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, maps.q, maps.k, maps.v);
 }
 
 cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,

@@ -243,3 +243,27 @@ def test_append_large_prefill_sized(pkv):
     hk, hv = oracle.kv_append(kc, vc, k_new, v_new, slots)
     assert np.array_equal(bf16_dev_to_bits(kd), hk)
     assert np.array_equal(bf16_dev_to_bits(vd), hv)
+
+
+def test_decode_workspace_reuse_stays_clean(pkv):
+    """One workspace across many calls of different shapes: the arrival
+    counters must return to zero after every call."""
+    import torch
+    rng = np.random.default_rng(13)
+    ws = torch.zeros(pkv.decode_workspace_size(300, 32, 8, 128) + 4096, dtype=torch.uint8,
+                     device="cuda")
+    for it in range(6):
+        B = int(rng.integers(1, 300))
+        lens = rng.integers(0, 4000, B)
+        q, kc, vc, bt, L = _random_case(rng, B, 32, 8, 128, 16, lens)
+        qd = to_dev_bf16(q)
+        out = torch.empty_like(qd)
+        err = _err(torch)
+        pkv.paged_attn_decode(out, qd, to_dev_bf16(kc), to_dev_bf16(vc), to_dev(bt), to_dev(L),
+                              int(L.max()), 0.088, 0, workspace=ws, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close_attn(bf16_dev_to_f64(out), oracle.paged_decode(q, kc, vc, bt, L, 0.088),
+                          f"reuse {it}")
+    counters = ws[:300 * 8 * 4].view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
