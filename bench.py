@@ -276,6 +276,12 @@ def run_ours(args):
             import torch.distributed as dist
             dist.barrier()
 
+    if args.only == "mixed":
+        mixed = run_mixed(args, device, stream, flush, rank)
+        if rank == 0:
+            print(json.dumps({"metric": "mixed-step tokens/sec", "mixed_step": mixed}), flush=True)
+        return
+
     # ---- headline: Qwen3-shaped decode step -------------------------------
     step = wl.qwen3_decode()
     ds = DeviceStep(step, wl.BASE_SEED + 2 + 1000 * rank, device)

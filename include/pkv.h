@@ -112,6 +112,8 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *                256-byte aligned.  Zero-fill it once before its first use
  *                (e.g. cudaMemsetAsync); every call leaves it zero-filled
  *                again, so it can be reused by later calls in stream order.
+ *                A workspace may be shared by calls with the same head
+ *                shapes and any batch up to the one it was sized for.
  *                Calls that overlap on the GPU need separate workspaces.
  *                After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
  *
@@ -148,12 +150,16 @@ pkv_status paged_attn_decode(void* out, const void* q,
  *   block_table    [batch, max_blocks_per_seq] int32
  *   max_seqlen_q, max_seqlen_k  upper bounds of q_len / k_len (size the
  *                  launch; longer chunks are clamped and flagged)
+ *   scale          >= 0 (negative or NaN: PKV_ERR_INVALID)
  *   causal         1: query i of a chunk sits at position k_len - q_len + i
  *                  (bottom-right) and sees keys <= its position;
  *                  0: every key of the chunk (window must then be <= 0)
  *   window         > 0 (causal only): also require q_pos - k_pos < window
  *
- * Runs QK^T and PV on the tcgen05 tensor cores with TMEM accumulators.
+ * Runs QK^T and PV on the tcgen05 tensor cores with TMEM accumulators in
+ * one persistent launch.  Limits: batch <= 1024 chunks; the per-chunk
+ * schedule (about 4 bytes per 128*2/G query rows of max_seqlen_q) must fit
+ * in shared memory, else PKV_ERR_UNSUPPORTED.
  */
 pkv_status paged_attn_varlen(void* out, const void* q,
                              const void* k_cache, const void* v_cache,

@@ -5,6 +5,11 @@
 
 #include "../../include/pkv.h"
 #include "kernels.h"
+#include "tmap.h"
+
+using pkv::encode_pool_map;
+using pkv::encode_pool_map_rows;
+using pkv::encode_q_map;
 
 namespace {
 
@@ -33,72 +38,6 @@ int num_sms_current(int* out) {
   }
   *out = cache[dev];
   return 0;
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// K or V pool [num_pages, H_kv, P, D] bf16 viewed as {D, P, num_pages*H_kv};
-// box = 64 columns x 16 rows, 128-byte swizzle.
-bool encode_pool_map(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
-                     int H_kv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
-  cuuint32_t box[3] = {64, 16, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// K or V pool for the varlen kernel: same view, box = 64 columns x `rows` rows.
-bool encode_pool_map_rows(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
-                          int H_kv, int rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// q [total_q, H_q, D] viewed as {D, G, H_kv, total_q}; box = 64 x G x 1 x (128/G)
-// so one box holds 128 (position, head) rows of one kv group.
-bool encode_q_map(CUtensorMap* m, const void* base, int D, int G, int H_kv, int total_q) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)H_kv, (cuuint64_t)total_q};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
-                           (cuuint64_t)H_kv * G * D * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G)};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool supported_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
@@ -174,14 +113,10 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
   if (workspace_bytes <
       pkv::decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, sms))
     return PKV_ERR_INVALID;
-  CUtensorMap tmK, tmV;
-  if (!encode_pool_map(&tmK, k_cache, head_dim, page_size, num_pages, num_kv_heads) ||
-      !encode_pool_map(&tmV, v_cache, head_dim, page_size, num_pages, num_kv_heads))
-    return cuda_fail(cudaErrorInvalidValue);
   cudaError_t e = pkv::launch_decode(
-      out, q, tmK, tmV, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+      out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
       num_kv_heads, head_dim, page_size, num_pages, max_seq_len, scale, window, workspace,
-      err_flag, static_cast<cudaStream_t>(stream), sms);
+      workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), sms);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
@@ -197,12 +132,12 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
       total_q < 0)
     return PKV_ERR_INVALID;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
-  if (!(scale == scale)) return PKV_ERR_INVALID;
+  if (!(scale >= 0.f)) return PKV_ERR_INVALID;  // NaN or negative
   if (causal != 0 && causal != 1) return PKV_ERR_INVALID;
   if (!causal && window > 0) return PKV_ERR_INVALID;
   const int G = num_q_heads / num_kv_heads;
   if (!supported_head_dim(head_dim) || page_size % 16 != 0 || (128 % G) != 0 ||
-      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL)
+      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 1024)
     return PKV_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !cu_seq_lens_q || !cu_seq_lens_k || !block_table)
@@ -212,7 +147,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   int sms = 0;
   if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
   pkv::VarlenMaps maps;
-  const int kv_rows = head_dim == 256 ? 64 : 128;  // keys per KV tile
+  const int kv_rows = 64;  // keys per KV tile
   const int box_rows = page_size < kv_rows ? page_size : kv_rows;
   // a KV tile must be whole page slices: page_size divides it or is a
   // multiple of it

@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace pkv {
 
@@ -91,12 +92,28 @@ struct DecodeSmem {
   static constexpr int kMLOff = kCombOff + NW * kGP * kCombStride * 4;  // [NW][8][2]
   static constexpr int kBarOff = kMLOff + NW * kGP * 2 * 4;
   static constexpr int kOkOff = kBarOff + 2 * NSTAGE * 8;
-  static constexpr int kScanOff = kOkOff + NSTAGE * 4 + 16;  // [NW+1] warp sums
+  static constexpr int kMergeOff = kOkOff + NSTAGE * 4 + 16;  // merge max / 1/sum per head
+  static constexpr int kScanOff = kMergeOff + 2 * kGP * 4;    // [NW+1] warp sums
   static constexpr int kCumOff = ((kScanOff + (NW + 1) * 4) + 15) & ~15;
   static size_t bytes(int batch) { return 1024 + kCumOff + (size_t)(batch + 1) * 4; }
 };
 
-template <int D, int NW, int NSTAGE>
+// Shared-memory address of 16-byte chunk c (0..D/8-1) of key row `key` in a
+// staged tile.  Default staging: D/64 boxes of [16 rows x 128 B] (one box
+// per 64-column slice).  ONEBOX (head_dim 128): one box of 32 rows x 128 B,
+// row = 2*key + c/8.  Both are 128-byte swizzled: 16-byte unit u of a row r
+// sits at unit u ^ (r % 8).
+template <int D, bool ONEBOX>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int c) {
+  if (ONEBOX) {
+    const int rp = 2 * key + (c >> 3);
+    return base + rp * 128 + (((c & 7) ^ (rp & 7)) << 4);
+  } else {
+    return base + (c >> 3) * (kTile * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4);
+  }
+}
+
+template <int D, int NW, int NSTAGE, bool ONEBOX>
 __global__ void __launch_bounds__((NW + 1) * 32)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
@@ -118,6 +135,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   int* scan_tmp = reinterpret_cast<int*>(smem + L_::kScanOff);
   int* s_cum = reinterpret_cast<int*>(smem + L_::kCumOff);
   volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + L_::kOkOff + NSTAGE * 4);
+  float* merge_m = reinterpret_cast<float*>(smem + L_::kMergeOff);
+  float* merge_inv = merge_m + kGP;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -225,10 +244,16 @@ __global__ void __launch_bounds__((NW + 1) * 32)
               mbar_arrive_expect_tx(full + s, L_::kStageBytes);
               const int row = key0 % a.P;
               const int z = pg * a.H_kv + g;
+              if (ONEBOX) {
+                tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
+                tma_load_4d(st + L_::kTileBytes, &tmV, full + s, 0, 0, row, z);
+              } else {
 #pragma unroll
-              for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
-                tma_load_3d(st + L_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row, z);
+                for (int c = 0; c < D / 64; ++c) {
+                  tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
+                  tma_load_3d(st + L_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
+                              z);
+                }
               }
             } else {
               raise_err(a.err, PKV_DEVERR_PAGE);
@@ -306,12 +331,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const uint32_t rowaddr = stK + key * 128;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-          const int chunk = 2 * ks + (lane >> 4);
-          const uint32_t addr =
-              rowaddr + (chunk >> 3) * kBoxBytes + (((chunk & 7) ^ (lane & 7)) << 4);
+          const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
           uint32_t a0, a1, a2, a3;
           ldsm_x4(addr, a0, a1, a2, a3);
           if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
@@ -357,12 +379,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       {
         const int j = lane >> 3;
         const int key = (lane & 7) + (j >> 1) * 8;
-        const uint32_t rowaddr = stV + key * 128;
 #pragma unroll
         for (int md = 0; md < KS; ++md) {
-          const int chunk = 2 * md + (j & 1);
-          const uint32_t addr =
-              rowaddr + (chunk >> 3) * kBoxBytes + (((chunk & 7) ^ (lane & 7)) << 4);
+          const uint32_t addr = tile_addr<D, ONEBOX>(stV, key, 2 * md + (j & 1));
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(addr, a0, a1, a2, a3);
           mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
@@ -438,23 +457,52 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       named_bar_sync(1, NW * 32);
       if (*merge_flag) {
         __threadfence();
-        for (int e = tid; e < a.G * D; e += NW * 32) {
-          const int h = e / D, d = e - (e / D) * D;
+        // (1) per head: max and sum of the pieces' log2-sum-exps, one warp
+        //     per head, pieces spread over the lanes
+        for (int h = warp; h < a.G; h += NW) {
           float M = -INFINITY;
-          for (int c = cf; c <= cl; ++c)
+          for (int c = cf + lane; c <= cl; c += 32)
             if (!cta_range_empty(c, W, N)) M = fmaxf(M, __ldcg(a.part_lse + (seg + c) * a.G + h));
-          float acc = 0.f, wsum = 0.f;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          float sum = 0.f;
+          if (M != -INFINITY)
+            for (int c = cf + lane; c <= cl; c += 32)
+              if (!cta_range_empty(c, W, N))
+                sum += exp2f(__ldcg(a.part_lse + (seg + c) * a.G + h) - M);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+          if (lane == 0) {
+            merge_m[h] = M;
+            merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
+          }
+        }
+        named_bar_sync(1, NW * 32);
+        // (2) weighted sum of the pieces' outputs, 4 dims per thread
+        for (int j = tid; j < a.G * (D / 4); j += NW * 32) {
+          const int h = j / (D / 4), d4 = j - h * (D / 4);
+          const float M = merge_m[h];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           if (M != -INFINITY) {
+#pragma unroll 4
             for (int c = cf; c <= cl; ++c) {
               if (cta_range_empty(c, W, N)) continue;
               const int64_t pc = (seg + c) * a.G + h;
               const float w = exp2f(__ldcg(a.part_lse + pc) - M);
-              wsum += w;
-              acc += w * __ldcg(a.part_o + pc * D + d);
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
+              acc.x += w * v.x;
+              acc.y += w * v.y;
+              acc.z += w * v.z;
+              acc.w += w * v.w;
             }
           }
-          a.out[((int64_t)b * a.H_q + g * a.G + h) * D + d] =
-              __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+          const float inv = merge_inv[h];
+          __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * a.G + h) * D + d4 * 4) = pk;
         }
         if (tid == 0) a.seg_count[seg] = 0;
       }
@@ -480,6 +528,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 #ifndef PKV_DEC_CTAS
 #define PKV_DEC_CTAS 4
 #endif
+#ifndef PKV_DEC_OVERSUB
+#define PKV_DEC_OVERSUB 1  // grid = OVERSUB x resident CTAs (more, smaller pieces)
+#endif
+#ifndef PKV_DEC_ONEBOX
+#define PKV_DEC_ONEBOX 0   // head_dim 128: one contiguous 4 KB TMA box per tile
+#endif
 template <int D>
 struct DecodeCfg;
 template <> struct DecodeCfg<64> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 4; };
@@ -490,15 +544,16 @@ template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 4, CTA
 
 static int decode_ctas_per_sm(int D) {
   switch (D) {
-    case 64: return DecodeCfg<64>::CTAS_PER_SM;
-    case 128: return DecodeCfg<128>::CTAS_PER_SM;
-    default: return DecodeCfg<256>::CTAS_PER_SM;
+    case 64: return DecodeCfg<64>::CTAS_PER_SM * PKV_DEC_OVERSUB;
+    case 128: return DecodeCfg<128>::CTAS_PER_SM * PKV_DEC_OVERSUB;
+    default: return DecodeCfg<256>::CTAS_PER_SM * PKV_DEC_OVERSUB;
   }
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: [seg_count: batch*H_kv int32][part_lse: pieces*G f32][part_o: pieces*G*D f32]
+// Workspace: [seg_count: batch*H_kv int32] ... [part_lse: pieces*G f32][part_o: pieces*G*D f32]
+// (partials aligned to the end of the caller's buffer)
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
   const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
   const int64_t pieces = (int64_t)batch * H_kv + nmax;
@@ -508,11 +563,19 @@ size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t 
 }
 
 template <int D>
-static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
   using L_ = DecodeSmem<D, C::NW, C::NSTAGE>;
-  auto kern = decode_split_kernel<D, C::NW, C::NSTAGE>;
+  constexpr bool kOneBox = (D == 128) && (PKV_DEC_ONEBOX != 0);
+  auto kern = decode_split_kernel<D, C::NW, C::NSTAGE, kOneBox>;
+  CUtensorMap tmK, tmV;
+  const bool enc_ok =
+      kOneBox ? (encode_pool_map_halves(&tmK, k_cache, a.P, a.num_pages, a.H_kv) &&
+                 encode_pool_map_halves(&tmV, v_cache, a.P, a.num_pages, a.H_kv))
+              : (encode_pool_map(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv) &&
+                 encode_pool_map(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv));
+  if (!enc_ok) return cudaErrorInvalidValue;
   const size_t smem = L_::bytes(a.batch);
   // Raise the dynamic shared-memory limit once per device (and again only
   // if a larger batch needs more).
@@ -531,7 +594,7 @@ static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const C
   int64_t max_keys = max_seq_len;
   if (a.window > 0 && max_keys > a.window) max_keys = a.window;
   const int64_t max_units = (int64_t)a.batch * a.H_kv * ((max_keys + kTile - 1) / kTile + 1);
-  int64_t n = (int64_t)num_sms * C::CTAS_PER_SM;
+  int64_t n = (int64_t)num_sms * C::CTAS_PER_SM * PKV_DEC_OVERSUB;
   if (n > (max_units + 3) / 4) n = (max_units + 3) / 4;
   if (n < 1) n = 1;
   cudaLaunchConfig_t cfg = {};
@@ -547,12 +610,12 @@ static cudaError_t launch_decode_t(DecodeArgs a, const CUtensorMap& tmK, const C
   return cudaLaunchKernelEx(&cfg, kern, a, tmK, tmV);
 }
 
-cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
-                          const CUtensorMap& tmV, const int32_t* block_table, int32_t max_blocks,
+cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, int32_t max_blocks,
                           const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
-                          float scale, int32_t window, void* workspace, int32_t* err,
-                          cudaStream_t stream, int num_sms) {
+                          float scale, int32_t window, void* workspace, size_t workspace_bytes,
+                          int32_t* err, cudaStream_t stream, int num_sms) {
   DecodeArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -567,19 +630,23 @@ cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
   a.num_pages = num_pages;
   a.window = window;
   a.scale_log2 = scale * 1.4426950408889634f;
+  // Counters sit at the front and the partial results at the back of the
+  // workspace, so calls with different batch sizes that share one
+  // workspace never see each other's partials in their counter slots.
   const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
   const int64_t pieces = (int64_t)batch * H_kv + nmax;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.seg_count = reinterpret_cast<int32_t*>(ws);
-  ws += align256((size_t)batch * H_kv * 4);
-  a.part_lse = reinterpret_cast<float*>(ws);
-  ws += align256((size_t)pieces * a.G * 4);
-  a.part_o = reinterpret_cast<float*>(ws);
+  uint8_t* end = ws + (workspace_bytes & ~size_t(255));
+  end -= align256((size_t)pieces * a.G * D * 4);
+  a.part_o = reinterpret_cast<float*>(end);
+  end -= align256((size_t)pieces * a.G * 4);
+  a.part_lse = reinterpret_cast<float*>(end);
   a.err = err;
   switch (D) {
-    case 64: return launch_decode_t<64>(a, tmK, tmV, max_seq_len, stream, num_sms);
-    case 128: return launch_decode_t<128>(a, tmK, tmV, max_seq_len, stream, num_sms);
-    case 256: return launch_decode_t<256>(a, tmK, tmV, max_seq_len, stream, num_sms);
+    case 64: return launch_decode_t<64>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 128: return launch_decode_t<128>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 256: return launch_decode_t<256>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

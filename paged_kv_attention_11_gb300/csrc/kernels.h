@@ -16,12 +16,12 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
 
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms);
 
-cudaError_t launch_decode(void* out, const void* q, const CUtensorMap& tmK,
-                          const CUtensorMap& tmV, const int32_t* block_table, int32_t max_blocks,
+cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, int32_t max_blocks,
                           const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
-                          float scale, int32_t window, void* workspace, int32_t* err,
-                          cudaStream_t stream, int num_sms);
+                          float scale, int32_t window, void* workspace, size_t workspace_bytes,
+                          int32_t* err, cudaStream_t stream, int num_sms);
 
 struct VarlenMaps {
   CUtensorMap q;  // 4-D view of q: {D, G, H_kv, total_q}

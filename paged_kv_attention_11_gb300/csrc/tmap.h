@@ -1,0 +1,97 @@
+// Host-side TMA descriptor (CUtensorMap) encoding, shared by the launchers.
+// cuTensorMapEncodeTiled is fetched through the runtime's driver entry-point
+// query, so the library does not link libcuda directly.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <mutex>
+#include <stdint.h>
+
+namespace pkv {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// K or V pool [num_pages, H_kv, P, D] bf16 viewed as {D, P, num_pages*H_kv};
+// box = 64 columns x 16 rows, 128-byte swizzle.
+inline bool encode_pool_map(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
+                     int H_kv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
+  cuuint32_t box[3] = {64, 16, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K or V pool for the varlen kernel: same view, box = 64 columns x `rows` rows.
+inline bool encode_pool_map_rows(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
+                          int H_kv, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [total_q, H_q, D] viewed as {D, G, H_kv, total_q}; box = 64 x G x 1 x (128/G)
+// so one box holds 128 (position, head) rows of one kv group.
+inline bool encode_q_map(CUtensorMap* m, const void* base, int D, int G, int H_kv, int total_q) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)H_kv, (cuuint64_t)total_q};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
+                           (cuuint64_t)H_kv * G * D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K or V pool with head_dim 128 viewed as {64, 2, P, num_pages*H_kv}: one
+// box {64, 2, 16, 1} is a whole contiguous 16-key tile (4 KB); in shared
+// memory it lands as 32 rows of 128 bytes (row = 2*key + half), 128-byte
+// swizzled.
+inline bool encode_pool_map_halves(CUtensorMap* m, const void* base, int P, int64_t num_pages,
+                                   int H_kv) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, 2, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
+  cuuint64_t strides[3] = {128, 256, (cuuint64_t)P * 256};
+  cuuint32_t box[4] = {64, 2, 16, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace pkv
