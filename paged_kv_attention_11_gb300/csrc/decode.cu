@@ -6,30 +6,33 @@
 // commit (key allowed iff q_pos - k_pos < window).
 //
 // Design (GB300):
-//  * Work unit = one 16-key tile of one (sequence, kv head).  All units of
-//    the batch are laid end to end (sequence-major, then kv head) and the
-//    grid of N CTAs cuts that line into N equal ranges, so every CTA streams
-//    the same number of bytes whatever the length mix ("balanced split-KV").
-//    A CTA range that covers a whole (sequence, kv head) writes the bf16
-//    output directly; ranges that cut one produce partial (o, lse) pieces.
-//    The last CTA to finish a piece of a (sequence, kv head) -- found with
-//    a per-segment arrival counter in the workspace -- merges all its
-//    pieces (log-sum-exp weighting) and writes the output, then resets the
-//    counter to zero.  No CTA ever waits for another.
-//  * A producer warp walks the range, looks the pages up in the block table
-//    (32 entries per coalesced load) and issues 2-D TMA box loads
-//    (64 x 16 bf16, 128-byte swizzle) of the K and V tile into an NSTAGE
-//    ring guarded by mbarriers.
-//  * NW consumer warps take the tiles round-robin.  Per tile a warp computes
-//    S^T = K Q^T (16 keys x 8 heads, GQA group padded to 8) with mma.sync,
-//    does the online softmax (exp2, warp shuffles), transposes P in
-//    registers with movmatrix and accumulates O^T = V^T P^T with mma.sync.
-//    K/V bytes are read from HBM exactly once; Q (<= 8 heads) lives in
-//    registers.
-//  * Each piece ends with a cross-warp LSE combine in shared memory.
-//  * Launched with programmatic dependent launch: the prologue overlaps the
-//    previous kernel in the stream (e.g. the append that wrote the new
-//    token); griddepcontrol.wait precedes every read of the inputs.
+//  * Work unit = one 16-key tile of one (sequence, kv head) -- a "segment".
+//    All units of the batch are laid end to end (sequence-major, then kv
+//    head) and the grid of N resident CTAs cuts that line into N equal
+//    ranges, so every CTA streams the same number of bytes whatever the
+//    length mix (balanced split-KV).  The part of a segment inside one
+//    CTA's range is a "piece".
+//  * Producer warp: walks the range piece by piece.  For each piece it
+//    writes a record (sequence, head, tiles, ...) and the G query rows into
+//    a 4-deep record ring in shared memory, then streams the piece's K and
+//    V tiles: page ids from the block table (32 per coalesced load), TMA
+//    boxes per 16-key tile (128-byte swizzle) into an NSTAGE ring.
+//  * NW consumer warps: take the tiles of each piece round-robin.  Per tile
+//    a warp computes S^T = K Q^T (16 keys x 8 heads, GQA group padded to
+//    8) with mma.sync, does the online softmax (exp2, warp shuffles),
+//    transposes P in registers with movmatrix and accumulates
+//    O^T = V^T P^T with mma.sync.  At the end of a piece it hands its
+//    (m, l, O) state to the epilogue warp through a double buffer and goes
+//    straight on with the next piece: no CTA-wide barrier in the stream.
+//  * Epilogue warp: combines the consumer states of a piece (log-sum-exp
+//    weights); a piece that is a whole segment is written as the bf16
+//    output, others as a partial (o, lse) in the workspace.  The last CTA
+//    to deliver a piece of a segment -- found with a per-segment arrival
+//    counter in the workspace -- merges all its pieces and writes the
+//    output, then resets the counter to zero.  No CTA waits for another.
+//  * K/V bytes are read from HBM exactly once.  Launched with programmatic
+//    dependent launch: the prologue overlaps the previous kernel in the
+//    stream; griddepcontrol.wait precedes every read of the inputs.
 #include <math.h>
 
 #include "common.cuh"
@@ -40,6 +43,7 @@ namespace pkv {
 
 constexpr int kTile = 16;  // keys per pipeline stage
 constexpr int kGP = 8;     // GQA group padded to the mma N dimension
+constexpr int kNRec = 4;   // piece records in flight
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -53,8 +57,8 @@ struct DecodeArgs {
   int32_t window;
   float scale_log2;
   int32_t* seg_count;  // [batch * H_kv] arrival counters, zero between calls
-  float* part_lse;   // [(S + N) * G]
-  float* part_o;     // [(S + N) * G * D]
+  float* part_lse;     // [(S + N) * G]
+  float* part_o;       // [(S + N) * G * D]
   int32_t* err;
 };
 
@@ -82,20 +86,38 @@ __device__ __forceinline__ bool cta_range_empty(int64_t c, int64_t W, int64_t N)
   return c * W / N == (c + 1) * W / N;
 }
 
+// A piece as the producer hands it to the consumers and the epilogue.
+struct PieceRec {
+  int b, g;          // sequence, kv head
+  int first_tile;    // first 16-key tile (absolute, within the sequence)
+  int n;             // tiles in the piece; -1 terminates the stream
+  int L, lo;         // attended keys [lo, L)
+  int whole;         // the piece is the whole segment
+  int pad;
+  long long seg_start, seg_end;  // segment's unit range on the global line
+};
+
+// Shared-memory plan (byte offsets from the 1024-aligned base); depends on
+// the runtime GQA group and batch.
 template <int D, int NW, int NSTAGE>
-struct DecodeSmem {
-  static constexpr int kTileBytes = kTile * D * 2;           // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;         // K + V
-  static constexpr int kCombStride = D + 4;                  // padded row (floats)
-  static constexpr int kStagesOff = 0;
-  static constexpr int kCombOff = NSTAGE * kStageBytes;      // [NW][8][D+4] fp32
-  static constexpr int kMLOff = kCombOff + NW * kGP * kCombStride * 4;  // [NW][8][2]
-  static constexpr int kBarOff = kMLOff + NW * kGP * 2 * 4;
-  static constexpr int kOkOff = kBarOff + 2 * NSTAGE * 8;
-  static constexpr int kMergeOff = kOkOff + NSTAGE * 4 + 16;  // merge max / 1/sum per head
-  static constexpr int kScanOff = kMergeOff + 2 * kGP * 4;    // [NW+1] warp sums
-  static constexpr int kCumOff = ((kScanOff + (NW + 1) * 4) + 15) & ~15;
-  static size_t bytes(int batch) { return 1024 + kCumOff + (size_t)(batch + 1) * 4; }
+struct DecodePlan {
+  static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+  static constexpr int kCombStride = D + 4;             // padded row (floats)
+  int rec, qbuf, comb, ml, bars, ok, misc, scan, cum, total;
+  __host__ __device__ DecodePlan(int G, int batch) {
+    int o = NSTAGE * kStageBytes;
+    rec = o;   o += kNRec * (int)sizeof(PieceRec);
+    qbuf = o;  o += kNRec * G * D * 2;
+    comb = o;  o += 2 * NW * G * kCombStride * 4;
+    ml = o;    o += 2 * NW * G * 2 * 4;
+    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 4) * 8;
+    ok = o;    o += NSTAGE * 4;
+    misc = o;  o += 2 * kGP * 4 + 16;
+    scan = o;  o += (NW + 2) * 4 + 8;
+    cum = o;   o += (batch + 1) * 4;
+    total = 1024 + o;
+  }
 };
 
 // Shared-memory address of 16-byte chunk c (0..D/8-1) of key row `key` in a
@@ -114,29 +136,38 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int c) {
 }
 
 template <int D, int NW, int NSTAGE, bool ONEBOX>
-__global__ void __launch_bounds__((NW + 1) * 32)
+__global__ void __launch_bounds__((NW + 2) * 32)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
-  using L_ = DecodeSmem<D, NW, NSTAGE>;
-  constexpr int NT = (NW + 1) * 32;
+  using P_ = DecodePlan<D, NW, NSTAGE>;
+  constexpr int NT = (NW + 2) * 32;
   constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
-  constexpr int kBoxBytes = kTile * 128;  // one 64-column box of a tile
+  constexpr int kBoxBytes = kTile * 128;
+  constexpr int CS = P_::kCombStride;
+  const int G = a.G;
+  const P_ plan(G, a.batch);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* comb_o = reinterpret_cast<float*>(smem + L_::kCombOff);
-  float* comb_ml = reinterpret_cast<float*>(smem + L_::kMLOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::kBarOff);
+  PieceRec* recs = reinterpret_cast<PieceRec*>(smem + plan.rec);
+  uint8_t* qbuf = smem + plan.qbuf;
+  float* comb_o = reinterpret_cast<float*>(smem + plan.comb);   // [2][NW][G][CS]
+  float* comb_ml = reinterpret_cast<float*>(smem + plan.ml);    // [2][NW][G][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
   uint64_t* empty = full + NSTAGE;
-  int* stage_ok = reinterpret_cast<int*>(smem + L_::kOkOff);
-  int* scan_tmp = reinterpret_cast<int*>(smem + L_::kScanOff);
-  int* s_cum = reinterpret_cast<int*>(smem + L_::kCumOff);
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + L_::kOkOff + NSTAGE * 4);
-  float* merge_m = reinterpret_cast<float*>(smem + L_::kMergeOff);
+  uint64_t* rec_full = empty + NSTAGE;
+  uint64_t* rec_empty = rec_full + kNRec;
+  uint64_t* comb_full = rec_empty + kNRec;  // [2]
+  uint64_t* comb_empty = comb_full + 2;     // [2]
+  int* stage_ok = reinterpret_cast<int*>(smem + plan.ok);
+  float* merge_m = reinterpret_cast<float*>(smem + plan.misc);
   float* merge_inv = merge_m + kGP;
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(merge_inv + kGP);
+  int* scan_tmp = reinterpret_cast<int*>(smem + plan.scan);
+  int* s_cum = reinterpret_cast<int*>(smem + plan.cum);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -144,7 +175,18 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   const int B = a.batch;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * NSTAGE; ++i) mbar_init(full + i, 1);  // full[] and empty[]
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < kNRec; ++i) {
+      mbar_init(rec_full + i, 32);
+      mbar_init(rec_empty + i, NW * 32 + 32);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(comb_full + i, NW * 32);
+      mbar_init(comb_empty + i, 32);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -162,8 +204,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       local += (th - tl) * a.H_kv;
       // zero-length sequences have no work unit: their zero rows are written here
       if (L == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
-        for (int i = 0; i < a.H_q * D; ++i)
-          a.out[(int64_t)b * a.H_q * D + i] = __float2bfloat16_rn(0.f);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.H_q * D);
+        for (int i = 0; i < a.H_q * D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
     }
     int incl = local;
@@ -193,42 +235,70 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   const int64_t x1 = ((int64_t)blockIdx.x + 1) * W / N;
   if (x0 >= x1) return;
 
-  // first sequence of the range: last b with s_cum[b] <= x0
-  int b_first;
-  {
-    int lo = 0, hi = B;  // s_cum[lo] <= x0 < s_cum[hi]
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (s_cum[mid] <= x0) lo = mid; else hi = mid;
-    }
-    b_first = lo;
-  }
-
   if (warp == NW) {
     // ============================ producer warp ============================
     bool dead = false;
+    int b;
+    {  // first sequence of the range: last b with s_cum[b] <= x0
+      int lo = 0, hi = B;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_cum[mid] <= x0) lo = mid; else hi = mid;
+      }
+      b = lo;
+    }
     int64_t x = x0;
-    int b = b_first;
     int it = 0;  // CTA-wide tile counter
-    while (x < x1) {
-      int L, lo, t_lo, t_hi;
-      seq_extent(a, b, L, lo, t_lo, t_hi, false);
-      const int tiles_b = t_hi - t_lo;
-      const int64_t bstart = s_cum[b];
-      if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) { ++b; continue; }
-      const int g = (int)((x - bstart) / tiles_b);
-      const int64_t seg_start = bstart + (int64_t)g * tiles_b;
-      const int64_t seg_end = seg_start + tiles_b;
-      const int64_t p_end = seg_end < x1 ? seg_end : x1;
-      const int n = (int)(p_end - x);
+    int k = 0;   // piece counter
+    const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
+    while (true) {
+      const bool more = x < x1;
+      int L = 0, lo = 0, t_lo = 0, t_hi = 0, g = 0, n = -1;
+      int64_t seg_start = 0, seg_end = 0;
+      if (more) {
+        seq_extent(a, b, L, lo, t_lo, t_hi, false);
+        const int tiles_b = t_hi - t_lo;
+        const int64_t bstart = s_cum[b];
+        if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) {
+          ++b;
+          continue;
+        }
+        g = (int)((x - bstart) / tiles_b);
+        seg_start = bstart + (int64_t)g * tiles_b;
+        seg_end = seg_start + tiles_b;
+        n = (int)((seg_end < x1 ? seg_end : x1) - x);
+      }
       const int first_tile = t_lo + (int)(x - seg_start);
+      // ---- publish the piece record and its query rows ----
+      const int slot = k % kNRec;
+      if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
+      if (more) {
+        const uint4* qsrc =
+            reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.H_q + g * G) * D);
+        uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * G * D * 2);
+        for (int v = lane; v < qvec; v += 32) qdst[v] = __ldg(qsrc + v);
+      }
+      if (lane == 0) {
+        PieceRec& r = recs[slot];
+        r.b = b;
+        r.g = g;
+        r.first_tile = first_tile;
+        r.n = n;
+        r.L = L;
+        r.lo = lo;
+        r.whole = (seg_start >= x0 && seg_end <= x1) ? 1 : 0;
+        r.seg_start = seg_start;
+        r.seg_end = seg_end;
+      }
+      __syncwarp();
+      mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
+      ++k;
+      if (!more) break;
+      // ---- stream the piece's tiles ----
       const int* bt = a.block_table + (int64_t)b * a.max_blocks;
       for (int k0 = 0; k0 < n; k0 += 32) {
         int page = -1;
-        if (k0 + lane < n) {
-          const int key0 = (first_tile + k0 + lane) * kTile;
-          page = __ldg(bt + key0 / a.P);
-        }
+        if (k0 + lane < n) page = __ldg(bt + ((first_tile + k0 + lane) * kTile) / a.P);
         const int cnt = min(32, n - k0);
         for (int j = 0; j < cnt; ++j) {
           const int pg = __shfl_sync(0xffffffffu, page, j);
@@ -240,18 +310,18 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
             stage_ok[s] = ok ? 1 : 0;
             if (ok) {
-              uint8_t* st = smem + s * L_::kStageBytes;
-              mbar_arrive_expect_tx(full + s, L_::kStageBytes);
+              uint8_t* st = smem + s * P_::kStageBytes;
+              mbar_arrive_expect_tx(full + s, P_::kStageBytes);
               const int row = key0 % a.P;
               const int z = pg * a.H_kv + g;
               if (ONEBOX) {
                 tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
-                tma_load_4d(st + L_::kTileBytes, &tmV, full + s, 0, 0, row, z);
+                tma_load_4d(st + P_::kTileBytes, &tmV, full + s, 0, 0, row, z);
               } else {
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                   tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
-                  tma_load_3d(st + L_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
+                  tma_load_3d(st + P_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
                               z);
                 }
               }
@@ -263,7 +333,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
           ++it;
         }
       }
-      x = p_end;
+      x += n;
       if (x >= seg_end && g == a.H_kv - 1) ++b;
     }
     // drain: every issued load must land before the CTA may exit
@@ -272,253 +342,262 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       for (int i = first; i < it; ++i)
         mbar_wait(full + (i % NSTAGE), (i / NSTAGE) & 1, a.err, dead);
     }
-    return;
-  }
-
-  // ============================== consumer warps ============================
-  const int quad = lane >> 2;  // 0..7: key row (QK) / head (Q frag)
-  const int qlan = lane & 3;   // 0..3: head pair (2*qlan, 2*qlan+1)
-  bool dead = false;
-  int64_t x = x0;
-  int b = b_first;
-  int it_base = 0;
-  while (x < x1) {
-    int L, lo, t_lo, t_hi;
-    seq_extent(a, b, L, lo, t_lo, t_hi, false);
-    const int tiles_b = t_hi - t_lo;
-    const int64_t bstart = s_cum[b];
-    if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) { ++b; continue; }
-    const int g = (int)((x - bstart) / tiles_b);
-    const int64_t seg_start = bstart + (int64_t)g * tiles_b;
-    const int64_t seg_end = seg_start + tiles_b;
-    const int64_t p_end = seg_end < x1 ? seg_end : x1;
-    const int n = (int)(p_end - x);
-    const int first_tile = t_lo + (int)(x - seg_start);
-
-    // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan.
-    uint32_t qb[KS][2];
-    {
-      const bool hv = quad < a.G;
-      const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.H_q + g * a.G + (hv ? quad : 0)) * D;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t v0 = 0, v1 = 0;
-        if (hv) {
-          v0 = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * qlan));
-          v1 = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * qlan));
-        }
-        qb[ks][0] = v0;
-        qb[ks][1] = v1;
-      }
-    }
-    float o[KS][4];
-#pragma unroll
-    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-
-    // tiles k of this piece with (it_base + k) % NW == warp
-    int k = ((warp - it_base) % NW + NW) % NW;
-    for (; k < n; k += NW) {
-      const int it = it_base + k;
-      const int s = it % NSTAGE;
-      const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
-      const bool ok = landed && stage_ok[s] != 0;
-      const uint32_t stK = smem_u32(smem + s * L_::kStageBytes);
-      const uint32_t stV = stK + L_::kTileBytes;
-      const int key0 = (first_tile + k) * kTile;
-
-      // ---- S^T = K Q^T: 16 keys x 8 heads, two accumulation chains ----
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  } else if (warp < NW) {
+    // ============================== consumer warps ==========================
+    const int quad = lane >> 2;  // 0..7: key row (QK) / head (Q frag)
+    const int qlan = lane & 3;   // 0..3: head pair (2*qlan, 2*qlan+1)
+    bool dead = false;
+    int it_base = 0;
+    for (int k = 0;; ++k) {
+      const int slot = k % kNRec;
+      if (!mbar_wait(rec_full + slot, (k / kNRec) & 1, a.err, dead)) break;
+      const PieceRec rec = recs[slot];
+      // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan
+      uint32_t qb[KS][2];
       {
-        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const bool hv = rec.n >= 0 && quad < G;
+        const uint8_t* qrow = qbuf + slot * G * D * 2 + (hv ? quad : 0) * D * 2;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-          const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(addr, a0, a1, a2, a3);
-          if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * qlan) * 2)
+                         : 0u;
+          qb[ks][1] =
+              hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 8 + 2 * qlan) * 2) : 0u;
         }
       }
-      // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
-      const int kA = key0 + quad, kB = kA + 8;
-      const bool vA = ok && kA >= lo && kA < L;
-      const bool vB = ok && kB >= lo && kB < L;
-      float x0A = vA ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;  // key kA, head A
-      float x0B = vA ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;  // key kA, head B
-      float x1A = vB ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;  // key kB, head A
-      float x1B = vB ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;  // key kB, head B
-      float tA = fmaxf(x0A, x1A), tB = fmaxf(x0B, x1B);
+      mbar_arrive(rec_empty + slot);  // record and query rows copied to registers
+      if (rec.n < 0) break;
+
+      float o[KS][4];
+#pragma unroll
+      for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+      const int n = rec.n;
+      for (int kk = ((warp - it_base) % NW + NW) % NW; kk < n; kk += NW) {
+        const int it = it_base + kk;
+        const int s = it % NSTAGE;
+        const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
+        const bool ok = landed && stage_ok[s] != 0;
+        const uint32_t stK = smem_u32(smem + s * P_::kStageBytes);
+        const uint32_t stV = stK + P_::kTileBytes;
+        const int key0 = (rec.first_tile + kk) * kTile;
+
+        // ---- S^T = K Q^T: 16 keys x 8 heads, two accumulation chains ----
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          }
+        }
+        // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
+        const int kA = key0 + quad, kB = kA + 8;
+        const bool vA = ok && kA >= rec.lo && kA < rec.L;
+        const bool vB = ok && kB >= rec.lo && kB < rec.L;
+        const float x0A = vA ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
+        const float x0B = vA ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
+        const float x1A = vB ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
+        const float x1B = vB ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
+        float tA = fmaxf(x0A, x1A), tB = fmaxf(x0B, x1B);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, off));
+          tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, off));
+        }
+        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+        const float uA = nA == -INFINITY ? 0.f : nA;
+        const float uB = nB == -INFINITY ? 0.f : nB;
+        const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
+        const float p0A = exp2f(x0A - uA), p0B = exp2f(x0B - uB);
+        const float p1A = exp2f(x1A - uA), p1B = exp2f(x1B - uB);
+        lA = lA * alA + p0A + p1A;
+        lB = lB * alB + p0B + p1B;
+        mA = nA;
+        mB = nB;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          o[i][0] *= alA;
+          o[i][1] *= alB;
+          o[i][2] *= alA;
+          o[i][3] *= alB;
+        }
+        // P^T as the B operand: transpose the 8x8 (key x head) blocks in registers
+        const uint32_t pb0 = movmatrix_t(pack_bf16(p0A, p0B));
+        const uint32_t pb1 = movmatrix_t(pack_bf16(p1A, p1B));
+
+        // ---- O^T += V^T P^T: D/16 m-tiles of 16 dims x 8 heads ----
+        {
+          const int j = lane >> 3;
+          const int key = (lane & 7) + (j >> 1) * 8;
+#pragma unroll
+          for (int md = 0; md < KS; ++md) {
+            const uint32_t addr = tile_addr<D, ONEBOX>(stV, key, 2 * md + (j & 1));
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(addr, a0, a1, a2, a3);
+            mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + s);
+      }
+      it_base += n;
+
+      // ---- hand (m, l, O) of this warp to the epilogue warp ----
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
-        tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, off));
-        tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, off));
+        lA += __shfl_xor_sync(0xffffffffu, lA, off);
+        lB += __shfl_xor_sync(0xffffffffu, lB, off);
       }
-      const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
-      const float uA = nA == -INFINITY ? 0.f : nA;
-      const float uB = nB == -INFINITY ? 0.f : nB;
-      const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
-      const float p0A = exp2f(x0A - uA), p0B = exp2f(x0B - uB);
-      const float p1A = exp2f(x1A - uA), p1B = exp2f(x1B - uB);
-      lA = lA * alA + p0A + p1A;
-      lB = lB * alB + p0B + p1B;
-      mA = nA;
-      mB = nB;
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        o[i][0] *= alA;
-        o[i][1] *= alB;
-        o[i][2] *= alA;
-        o[i][3] *= alB;
-      }
-      // P^T as the B operand: transpose the 8x8 (key x head) blocks in registers
-      const uint32_t pb0 = movmatrix_t(pack_bf16(p0A, p0B));
-      const uint32_t pb1 = movmatrix_t(pack_bf16(p1A, p1B));
-
-      // ---- O^T += V^T P^T: D/16 m-tiles of 16 dims x 8 heads ----
-      {
-        const int j = lane >> 3;
-        const int key = (lane & 7) + (j >> 1) * 8;
-#pragma unroll
-        for (int md = 0; md < KS; ++md) {
-          const uint32_t addr = tile_addr<D, ONEBOX>(stV, key, 2 * md + (j & 1));
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(addr, a0, a1, a2, a3);
-          mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + s);
-    }
-
-    // ---- combine the NW warps' partial softmax states for this piece ----
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      lA += __shfl_xor_sync(0xffffffffu, lA, off);
-      lB += __shfl_xor_sync(0xffffffffu, lB, off);
-    }
-    {
-      float* co = comb_o + warp * kGP * L_::kCombStride;
+      const int cb = k & 1;
+      if (k >= 2) mbar_wait(comb_empty + cb, ((k >> 1) - 1) & 1, a.err, dead);
+      float* co = comb_o + ((cb * NW + warp) * G) * CS;
+      float* cml = comb_ml + ((cb * NW + warp) * G) * 2;
       const int hA = 2 * qlan, hB = hA + 1;
 #pragma unroll
       for (int md = 0; md < KS; ++md) {
         const int d = md * 16 + quad;
-        co[hA * L_::kCombStride + d] = o[md][0];
-        co[hB * L_::kCombStride + d] = o[md][1];
-        co[hA * L_::kCombStride + d + 8] = o[md][2];
-        co[hB * L_::kCombStride + d + 8] = o[md][3];
+        if (hA < G) {
+          co[hA * CS + d] = o[md][0];
+          co[hA * CS + d + 8] = o[md][2];
+        }
+        if (hB < G) {
+          co[hB * CS + d] = o[md][1];
+          co[hB * CS + d + 8] = o[md][3];
+        }
       }
       if (quad == 0) {
-        comb_ml[(warp * kGP + hA) * 2 + 0] = mA;
-        comb_ml[(warp * kGP + hA) * 2 + 1] = lA;
-        comb_ml[(warp * kGP + hB) * 2 + 0] = mB;
-        comb_ml[(warp * kGP + hB) * 2 + 1] = lB;
-      }
-    }
-    named_bar_sync(1, NW * 32);
-    const bool whole = seg_start >= x0 && seg_end <= x1;
-    const int64_t seg = (int64_t)b * a.H_kv + g;
-    const int64_t piece = seg + blockIdx.x;
-    for (int e = tid; e < a.G * D; e += NW * 32) {
-      const int h = e / D, d = e - (e / D) * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_ml[(w * kGP + h) * 2]);
-      float acc = 0.f, lsum = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = exp2f(comb_ml[(w * kGP + h) * 2] - M);
-          acc += sc * comb_o[(w * kGP + h) * L_::kCombStride + d];
-          lsum += sc * comb_ml[(w * kGP + h) * 2 + 1];
+        if (hA < G) {
+          cml[hA * 2] = mA;
+          cml[hA * 2 + 1] = lA;
+        }
+        if (hB < G) {
+          cml[hB * 2] = mB;
+          cml[hB * 2 + 1] = lB;
         }
       }
-      const float val = lsum > 0.f ? acc / lsum : 0.f;
-      if (whole) {
-        a.out[((int64_t)b * a.H_q + g * a.G + h) * D + d] = __float2bfloat16_rn(val);
-      } else {
-        a.part_o[(piece * a.G + h) * D + d] = val;
-        if (d == 0) a.part_lse[piece * a.G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
-      }
+      mbar_arrive(comb_full + cb);  // every lane releases its own writes
     }
-    if (!whole) {
-      // arrival counter: the last CTA to deliver a piece of this segment
-      // merges all of them (nobody waits; the counter is reset afterwards)
-      __threadfence();
-      named_bar_sync(1, NW * 32);
-      const int cf = owner_cta(seg_start, W, N);
-      const int cl = owner_cta(seg_end - 1, W, N);
-      if (tid == 0) {
-        int npieces = 0;
-        for (int c = cf; c <= cl; ++c) npieces += cta_range_empty(c, W, N) ? 0 : 1;
-        const int old = atomicAdd(a.seg_count + seg, 1);
-        *merge_flag = (old == npieces - 1) ? 1 : 0;
-      }
-      named_bar_sync(1, NW * 32);
-      if (*merge_flag) {
-        __threadfence();
-        // (1) per head: max and sum of the pieces' log2-sum-exps, one warp
-        //     per head, pieces spread over the lanes
-        for (int h = warp; h < a.G; h += NW) {
-          float M = -INFINITY;
-          for (int c = cf + lane; c <= cl; c += 32)
-            if (!cta_range_empty(c, W, N)) M = fmaxf(M, __ldcg(a.part_lse + (seg + c) * a.G + h));
+  } else {
+    // =============================== epilogue warp ==========================
+    bool dead = false;
+    for (int k = 0;; ++k) {
+      const int slot = k % kNRec;
+      if (!mbar_wait(rec_full + slot, (k / kNRec) & 1, a.err, dead)) break;
+      const PieceRec rec = recs[slot];
+      mbar_arrive(rec_empty + slot);
+      if (rec.n < 0) break;
+      const int cb = k & 1;
+      mbar_wait(comb_full + cb, (k >> 1) & 1, a.err, dead);
+      const int b = rec.b, g = rec.g;
+      const int64_t seg = (int64_t)b * a.H_kv + g;
+      const int64_t piece = seg + blockIdx.x;
+      const float* co = comb_o + (cb * NW * G) * CS;
+      const float* cml = comb_ml + (cb * NW * G) * 2;
+      for (int e = lane; e < G * D; e += 32) {
+        const int h = e / D, d = e - (e / D) * D;
+        float M = -INFINITY;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          float sum = 0.f;
-          if (M != -INFINITY)
-            for (int c = cf + lane; c <= cl; c += 32)
-              if (!cta_range_empty(c, W, N))
-                sum += exp2f(__ldcg(a.part_lse + (seg + c) * a.G + h) - M);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, cml[(w * G + h) * 2]);
+        float acc = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-          if (lane == 0) {
-            merge_m[h] = M;
-            merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
+          for (int w = 0; w < NW; ++w) {
+            const float sc = exp2f(cml[(w * G + h) * 2] - M);
+            acc += sc * co[(w * G + h) * CS + d];
+            lsum += sc * cml[(w * G + h) * 2 + 1];
           }
         }
-        named_bar_sync(1, NW * 32);
-        // (2) weighted sum of the pieces' outputs, 4 dims per thread
-        for (int j = tid; j < a.G * (D / 4); j += NW * 32) {
-          const int h = j / (D / 4), d4 = j - h * (D / 4);
-          const float M = merge_m[h];
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (M != -INFINITY) {
-#pragma unroll 4
-            for (int c = cf; c <= cl; ++c) {
-              if (cta_range_empty(c, W, N)) continue;
-              const int64_t pc = (seg + c) * a.G + h;
-              const float w = exp2f(__ldcg(a.part_lse + pc) - M);
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
-              acc.x += w * v.x;
-              acc.y += w * v.y;
-              acc.z += w * v.z;
-              acc.w += w * v.w;
+        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        if (rec.whole) {
+          a.out[((int64_t)b * a.H_q + g * G + h) * D + d] = __float2bfloat16_rn(val);
+        } else {
+          a.part_o[(piece * G + h) * D + d] = val;
+          if (d == 0) a.part_lse[piece * G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+        }
+      }
+      __syncwarp();
+      mbar_arrive(comb_empty + cb);  // the consumers may refill this buffer
+      if (!rec.whole) {
+        // arrival counter: the last CTA to deliver a piece of this segment
+        // merges all of them (nobody waits; the counter is reset afterwards)
+        __threadfence();
+        __syncwarp();
+        const int cf = owner_cta(rec.seg_start, W, N);
+        const int cl = owner_cta(rec.seg_end - 1, W, N);
+        if (lane == 0) {
+          int npieces = 0;
+          for (int c = cf; c <= cl; ++c) npieces += cta_range_empty(c, W, N) ? 0 : 1;
+          const int old = atomicAdd(a.seg_count + seg, 1);
+          *merge_flag = (old == npieces - 1) ? 1 : 0;
+        }
+        __syncwarp();
+        if (*merge_flag) {
+          __threadfence();
+          // (1) per head: max and sum of the pieces' log2-sum-exps
+          for (int h = 0; h < G; ++h) {
+            float M = -INFINITY;
+            for (int c = cf + lane; c <= cl; c += 32)
+              if (!cta_range_empty(c, W, N)) M = fmaxf(M, __ldcg(a.part_lse + (seg + c) * G + h));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+              M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float sum = 0.f;
+            if (M != -INFINITY)
+              for (int c = cf + lane; c <= cl; c += 32)
+                if (!cta_range_empty(c, W, N))
+                  sum += exp2f(__ldcg(a.part_lse + (seg + c) * G + h) - M);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) {
+              merge_m[h] = M;
+              merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
             }
           }
-          const float inv = merge_inv[h];
-          __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * a.G + h) * D + d4 * 4) = pk;
+          __syncwarp();
+          // (2) weighted sum of the pieces' outputs, 4 dims per lane
+          for (int j = lane; j < G * (D / 4); j += 32) {
+            const int h = j / (D / 4), d4 = j - h * (D / 4);
+            const float M = merge_m[h];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
+#pragma unroll 4
+              for (int c = cf; c <= cl; ++c) {
+                if (cta_range_empty(c, W, N)) continue;
+                const int64_t pc = (seg + c) * G + h;
+                const float w = exp2f(__ldcg(a.part_lse + pc) - M);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+              }
+            }
+            const float inv = merge_inv[h];
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
+                pk;
+          }
+          if (lane == 0) a.seg_count[seg] = 0;
+          __syncwarp();
         }
-        if (tid == 0) a.seg_count[seg] = 0;
       }
     }
-    named_bar_sync(1, NW * 32);
-
-    it_base += n;
-    x = p_end;
-    if (x >= seg_end && g == a.H_kv - 1) ++b;
   }
 }
 
 // --------------------------------------------------------------- host side
 // Launch shape per head_dim: consumer warps, pipeline stages (16-key K+V
-// tiles) per CTA, resident CTAs per SM.  Overridable at build time for
-// tuning sweeps.
+// tiles) per CTA, resident CTAs per SM at most.  Overridable at build time
+// for tuning sweeps.
 #ifndef PKV_DEC_NW
 #define PKV_DEC_NW 2
 #endif
@@ -528,11 +607,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 #ifndef PKV_DEC_CTAS
 #define PKV_DEC_CTAS 4
 #endif
-#ifndef PKV_DEC_OVERSUB
-#define PKV_DEC_OVERSUB 1  // grid = OVERSUB x resident CTAs (more, smaller pieces)
-#endif
 #ifndef PKV_DEC_ONEBOX
-#define PKV_DEC_ONEBOX 0   // head_dim 128: one contiguous 4 KB TMA box per tile
+#define PKV_DEC_ONEBOX 1   // head_dim 128: one contiguous 4 KB TMA box per tile
 #endif
 template <int D>
 struct DecodeCfg;
@@ -544,9 +620,9 @@ template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 4, CTA
 
 static int decode_ctas_per_sm(int D) {
   switch (D) {
-    case 64: return DecodeCfg<64>::CTAS_PER_SM * PKV_DEC_OVERSUB;
-    case 128: return DecodeCfg<128>::CTAS_PER_SM * PKV_DEC_OVERSUB;
-    default: return DecodeCfg<256>::CTAS_PER_SM * PKV_DEC_OVERSUB;
+    case 64: return DecodeCfg<64>::CTAS_PER_SM;
+    case 128: return DecodeCfg<128>::CTAS_PER_SM;
+    default: return DecodeCfg<256>::CTAS_PER_SM;
   }
 }
 
@@ -566,7 +642,7 @@ template <int D>
 static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
-  using L_ = DecodeSmem<D, C::NW, C::NSTAGE>;
+  using P_ = DecodePlan<D, C::NW, C::NSTAGE>;
   constexpr bool kOneBox = (D == 128) && (PKV_DEC_ONEBOX != 0);
   auto kern = decode_split_kernel<D, C::NW, C::NSTAGE, kOneBox>;
   CUtensorMap tmK, tmV;
@@ -576,30 +652,40 @@ static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void
               : (encode_pool_map(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv) &&
                  encode_pool_map(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv));
   if (!enc_ok) return cudaErrorInvalidValue;
-  const size_t smem = L_::bytes(a.batch);
+  const size_t smem = P_(a.G, a.batch).total;
+  if (smem > 227 * 1024) return cudaErrorNotSupported;
   // Raise the dynamic shared-memory limit once per device (and again only
-  // if a larger batch needs more).
+  // if a larger batch needs more); cache the resident CTAs per SM for it.
   static int configured[64] = {0};
+  static int occupancy[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (configured[dev] != (int)smem) {
+    if (configured[dev] < (int)smem) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (C::NW + 2) * 32, smem);
     if (e != cudaSuccess) return e;
-    configured[dev] = (int)smem;
+    if (configured[dev] < (int)smem) configured[dev] = (int)smem;
+    occupancy[dev] = occ;
   }
+  int per_sm = occupancy[dev] < C::CTAS_PER_SM ? occupancy[dev] : C::CTAS_PER_SM;
+  if (per_sm < 1) per_sm = 1;
   // grid: one wave of resident CTAs, but >= ~4 tiles each on the longest
   // possible batch
   int64_t max_keys = max_seq_len;
   if (a.window > 0 && max_keys > a.window) max_keys = a.window;
   const int64_t max_units = (int64_t)a.batch * a.H_kv * ((max_keys + kTile - 1) / kTile + 1);
-  int64_t n = (int64_t)num_sms * C::CTAS_PER_SM * PKV_DEC_OVERSUB;
+  int64_t n = (int64_t)num_sms * per_sm;
   if (n > (max_units + 3) / 4) n = (max_units + 3) / 4;
   if (n < 1) n = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n);
-  cfg.blockDim = dim3((C::NW + 1) * 32);
+  cfg.blockDim = dim3((C::NW + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
