@@ -172,6 +172,37 @@ pkv_status paged_attn_varlen(void* out, const void* q,
                              float scale, int32_t causal, int32_t window,
                              int32_t* err_flag, void* stream);
 
+/*
+ * paged_attn_decode_static - paged_attn_decode for callers that cannot
+ * allocate device memory.  (Not an operation of the pages: it exists for
+ * callers of this library that may not call cudaMalloc on the attention
+ * path -- an engine that has already given all free HBM to its KV page
+ * pool, or a plugin host that hands a kernel only its inputs and outputs.)
+ *
+ * Same arguments, semantics and results as paged_attn_decode, minus the
+ * workspace: the scratch lives in one fixed 8 MiB (8388608-byte) array of
+ * device memory inside the library, held by every GPU that loads the
+ * library until the process exits.  A batch whose
+ * paged_attn_decode_workspace_size() exceeds 8 MiB is rejected with
+ * PKV_ERR_UNSUPPORTED (message in pkv_last_cuda_error()).
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  Every call clears the array's arrival counters on
+ * `stream` before its kernel runs.  All calls share the one array: calls
+ * whose work may overlap on the GPU (different streams or host threads)
+ * race and must be serialised by the caller.  No allocation and no free
+ * is made.
+ */
+pkv_status paged_attn_decode_static(void* out, const void* q,
+                                    const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, int32_t batch,
+                                    int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t page_size, int64_t num_pages,
+                                    int32_t max_seq_len, float scale, int32_t window,
+                                    int32_t* err_flag, void* stream);
+
 /* Human-readable name of a pkv_status value (static string). */
 const char* pkv_status_string(int32_t status);
 

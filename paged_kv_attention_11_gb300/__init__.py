@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     lib,
     lib_path,
     paged_attn_decode,
+    paged_attn_decode_static,
     paged_attn_varlen,
     paged_kv_append,
 )

@@ -27,6 +27,9 @@ _SIGS = {
     "paged_attn_varlen": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32,
                           _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f, _c_i32,
                           _c_i32, _c_p, _c_p],
+    "paged_attn_decode_static": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32,
+                                 _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_p,
+                                 _c_p],
     "pkv_status_string": [_c_i32],
     "pkv_last_cuda_error": [],
 }
@@ -149,4 +152,25 @@ def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         cu_seq_lens_q.shape[0] - 1, int(max_seqlen_q), int(max_seqlen_k), total_q, H_q, H_kv,
         D, P, num_pages, float(scale), 1 if causal else 0, int(window), _ptr(err_flag),
         _stream(stream)))
+    return out
+
+
+def paged_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, block_table: torch.Tensor,
+                             seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                             window: int = 0, err_flag: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """paged_attn_decode without a caller workspace: for callers that cannot
+    allocate device memory (the library's own fixed 8 MiB scratch is used;
+    calls that overlap on the GPU race on it)."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    B, H_q, D = q.shape
+    num_pages, H_kv, P, _ = k_cache.shape
+    _check("paged_attn_decode_static", lib().paged_attn_decode_static(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
+        float(scale), int(window), _ptr(err_flag), _stream(stream)))
     return out

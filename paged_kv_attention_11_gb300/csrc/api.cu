@@ -44,6 +44,10 @@ bool supported_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
 
 }  // namespace
 
+namespace pkv {
+void set_last_error(const std::string& msg) { g_last_cuda_error = msg; }
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_status_string(int32_t s) {

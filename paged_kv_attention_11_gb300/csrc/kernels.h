@@ -7,7 +7,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace pkv {
+
+// Message returned by pkv_last_cuda_error() on this host thread.
+void set_last_error(const std::string& msg);
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t H_kv,
