@@ -237,6 +237,10 @@ __global__ void __launch_bounds__((NW + 2) * 32)
 
   if (warp == NW) {
     // ============================ producer warp ============================
+    // The next piece's query rows and first 32 page ids are loaded into
+    // registers before the current piece is streamed, so no global-memory
+    // latency sits between two pieces.
+    constexpr int QV = D / 32;  // query vectors per lane for a group of <= 8 heads
     bool dead = false;
     int b;
     {  // first sequence of the range: last b with s_cum[b] <= x0
@@ -247,15 +251,22 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       }
       b = lo;
     }
-    int64_t x = x0;
-    int it = 0;  // CTA-wide tile counter
-    int k = 0;   // piece counter
     const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
-    while (true) {
-      const bool more = x < x1;
-      int L = 0, lo = 0, t_lo = 0, t_hi = 0, g = 0, n = -1;
-      int64_t seg_start = 0, seg_end = 0;
-      if (more) {
+    struct Piece {
+      bool more;
+      int g, L, lo, first_tile, n, bseq;
+      int64_t seg_start, seg_end;
+    };
+    // the piece that starts at unit x (b advances past finished sequences)
+    auto piece_at = [&](int64_t x) -> Piece {
+      Piece p;
+      p.more = false;
+      p.n = -1;
+      p.g = p.L = p.lo = p.first_tile = 0;
+      p.bseq = b;
+      p.seg_start = p.seg_end = 0;
+      while (x < x1) {
+        int L, lo, t_lo, t_hi;
         seq_extent(a, b, L, lo, t_lo, t_hi, false);
         const int tiles_b = t_hi - t_lo;
         const int64_t bstart = s_cum[b];
@@ -263,42 +274,82 @@ __global__ void __launch_bounds__((NW + 2) * 32)
           ++b;
           continue;
         }
-        g = (int)((x - bstart) / tiles_b);
-        seg_start = bstart + (int64_t)g * tiles_b;
-        seg_end = seg_start + tiles_b;
-        n = (int)((seg_end < x1 ? seg_end : x1) - x);
+        p.more = true;
+        p.bseq = b;
+        p.g = (int)((x - bstart) / tiles_b);
+        p.seg_start = bstart + (int64_t)p.g * tiles_b;
+        p.seg_end = p.seg_start + tiles_b;
+        p.n = (int)((p.seg_end < x1 ? p.seg_end : x1) - x);
+        p.L = L;
+        p.lo = lo;
+        p.first_tile = t_lo + (int)(x - p.seg_start);
+        break;
       }
-      const int first_tile = t_lo + (int)(x - seg_start);
+      return p;
+    };
+    auto prefetch = [&](const Piece& p, uint4 (&qr)[QV], int& pages) {
+      pages = -1;
+      if (!p.more) return;
+      const uint4* qsrc =
+          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.bseq * a.H_q + p.g * G) * D);
+#pragma unroll
+      for (int i = 0; i < QV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < qvec) qr[i] = __ldg(qsrc + v);
+      }
+      if (lane < p.n)
+        pages = __ldg(a.block_table + (int64_t)p.bseq * a.max_blocks +
+                      ((p.first_tile + lane) * kTile) / a.P);
+    };
+
+    int64_t x = x0;
+    Piece cur = piece_at(x);
+    uint4 qcur[QV];
+    int pcur;
+    prefetch(cur, qcur, pcur);
+    int it = 0;  // CTA-wide tile counter
+    int k = 0;   // piece counter
+    while (true) {
       // ---- publish the piece record and its query rows ----
       const int slot = k % kNRec;
       if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
-      if (more) {
-        const uint4* qsrc =
-            reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.H_q + g * G) * D);
+      if (cur.more) {
         uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * G * D * 2);
-        for (int v = lane; v < qvec; v += 32) qdst[v] = __ldg(qsrc + v);
+#pragma unroll
+        for (int i = 0; i < QV; ++i) {
+          const int v = lane + 32 * i;
+          if (v < qvec) qdst[v] = qcur[i];
+        }
       }
       if (lane == 0) {
         PieceRec& r = recs[slot];
-        r.b = b;
-        r.g = g;
-        r.first_tile = first_tile;
-        r.n = n;
-        r.L = L;
-        r.lo = lo;
-        r.whole = (seg_start >= x0 && seg_end <= x1) ? 1 : 0;
-        r.seg_start = seg_start;
-        r.seg_end = seg_end;
+        r.b = cur.bseq;
+        r.g = cur.g;
+        r.first_tile = cur.first_tile;
+        r.n = cur.n;
+        r.L = cur.L;
+        r.lo = cur.lo;
+        r.whole = (cur.seg_start >= x0 && cur.seg_end <= x1) ? 1 : 0;
+        r.seg_start = cur.seg_start;
+        r.seg_end = cur.seg_end;
       }
       __syncwarp();
       mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
       ++k;
-      if (!more) break;
+      if (!cur.more) break;
+      // ---- look ahead: the next piece's inputs load while this one streams ----
+      x += cur.n;
+      const Piece nxt = piece_at(x);
+      uint4 qnxt[QV];
+      int pnxt;
+      prefetch(nxt, qnxt, pnxt);
       // ---- stream the piece's tiles ----
-      const int* bt = a.block_table + (int64_t)b * a.max_blocks;
+      const int* bt = a.block_table + (int64_t)cur.bseq * a.max_blocks;
+      const int n = cur.n;
+      int page = pcur;
       for (int k0 = 0; k0 < n; k0 += 32) {
-        int page = -1;
-        if (k0 + lane < n) page = __ldg(bt + ((first_tile + k0 + lane) * kTile) / a.P);
+        int page_ahead = -1;  // page ids of the following 32 tiles
+        if (k0 + 32 + lane < n) page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
         const int cnt = min(32, n - k0);
         for (int j = 0; j < cnt; ++j) {
           const int pg = __shfl_sync(0xffffffffu, page, j);
@@ -306,14 +357,14 @@ __global__ void __launch_bounds__((NW + 2) * 32)
             const int s = it % NSTAGE;
             const int r = it / NSTAGE;
             if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
-            const int key0 = (first_tile + k0 + j) * kTile;
+            const int key0 = (cur.first_tile + k0 + j) * kTile;
             const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
             stage_ok[s] = ok ? 1 : 0;
             if (ok) {
               uint8_t* st = smem + s * P_::kStageBytes;
               mbar_arrive_expect_tx(full + s, P_::kStageBytes);
               const int row = key0 % a.P;
-              const int z = pg * a.H_kv + g;
+              const int z = pg * a.H_kv + cur.g;
               if (ONEBOX) {
                 tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
                 tma_load_4d(st + P_::kTileBytes, &tmV, full + s, 0, 0, row, z);
@@ -332,9 +383,12 @@ __global__ void __launch_bounds__((NW + 2) * 32)
           }
           ++it;
         }
+        page = page_ahead;
       }
-      x += n;
-      if (x >= seg_end && g == a.H_kv - 1) ++b;
+      cur = nxt;
+#pragma unroll
+      for (int i = 0; i < QV; ++i) qcur[i] = qnxt[i];
+      pcur = pnxt;
     }
     // drain: every issued load must land before the CTA may exit
     if (lane == 0) {
