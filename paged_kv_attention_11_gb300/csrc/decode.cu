@@ -44,6 +44,7 @@ namespace pkv {
 constexpr int kTile = 16;  // keys per pipeline stage
 constexpr int kGP = 8;     // GQA group padded to the mma N dimension
 constexpr int kNRec = 4;   // piece records in flight
+constexpr int kMergeLse = 128;  // (piece, head) log-sum-exps staged in smem for a merge
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -113,7 +114,7 @@ struct DecodePlan {
     ml = o;    o += 2 * NW * G * 2 * 4;
     bars = o;  o += (2 * NSTAGE + 2 * kNRec + 4) * 8;
     ok = o;    o += NSTAGE * 4;
-    misc = o;  o += 2 * kGP * 4 + 16;
+    misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
     scan = o;  o += (NW + 2) * 4 + 8;
     cum = o;   o += (batch + 1) * 4;
     total = 1024 + o;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__((NW + 2) * 32)
   float* merge_m = reinterpret_cast<float*>(smem + plan.misc);
   float* merge_inv = merge_m + kGP;
   volatile int* merge_flag = reinterpret_cast<volatile int*>(merge_inv + kGP);
+  float* merge_lse = merge_inv + kGP + 4;  // [kMergeLse]
   int* scan_tmp = reinterpret_cast<int*>(smem + plan.scan);
   int* s_cum = reinterpret_cast<int*>(smem + plan.cum);
 
@@ -592,43 +594,71 @@ __global__ void __launch_bounds__((NW + 2) * 32)
         __syncwarp();
         if (*merge_flag) {
           __threadfence();
-          // (1) per head: max and sum of the pieces' log2-sum-exps
-          for (int h = 0; h < G; ++h) {
-            float M = -INFINITY;
-            for (int c = cf + lane; c <= cl; c += 32)
-              if (!cta_range_empty(c, W, N)) M = fmaxf(M, __ldcg(a.part_lse + (seg + c) * G + h));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-              M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float sum = 0.f;
-            if (M != -INFINITY)
-              for (int c = cf + lane; c <= cl; c += 32)
-                if (!cta_range_empty(c, W, N))
-                  sum += exp2f(__ldcg(a.part_lse + (seg + c) * G + h) - M);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (lane == 0) {
-              merge_m[h] = M;
-              merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
-            }
+          // (1) every (piece, head) log2-sum-exp in one round of loads, the
+          //     per-head max and weight sum from shared memory
+          const int np = cl - cf + 1;
+          for (int i = lane; i < np * G; i += 32) {
+            const int c = cf + i / G, h = i - (i / G) * G;
+            float v = -INFINITY;
+            if (!cta_range_empty(c, W, N)) v = __ldcg(a.part_lse + (seg + c) * G + h);
+            if (i < kMergeLse) merge_lse[i] = v;
           }
           __syncwarp();
-          // (2) weighted sum of the pieces' outputs, 4 dims per lane
+          if (lane < G) {
+            const int h = lane;
+            float M = -INFINITY;
+            for (int c = 0; c < np; ++c) {
+              const float v = (c * G + h < kMergeLse)
+                                  ? merge_lse[c * G + h]
+                                  : (cta_range_empty(cf + c, W, N)
+                                         ? -INFINITY
+                                         : __ldcg(a.part_lse + (seg + cf + c) * G + h));
+              M = fmaxf(M, v);
+            }
+            float sum = 0.f;
+            if (M != -INFINITY)
+              for (int c = 0; c < np; ++c) {
+                const float v = (c * G + h < kMergeLse)
+                                    ? merge_lse[c * G + h]
+                                    : (cta_range_empty(cf + c, W, N)
+                                           ? -INFINITY
+                                           : __ldcg(a.part_lse + (seg + cf + c) * G + h));
+                sum += exp2f(v - M);
+              }
+            merge_m[h] = M;
+            merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
+          }
+          __syncwarp();
+          // (2) weighted sum of the pieces' outputs, 4 dims per lane; the
+          //     loads of all pieces are issued before any is used
           for (int j = lane; j < G * (D / 4); j += 32) {
             const int h = j / (D / 4), d4 = j - h * (D / 4);
             const float M = merge_m[h];
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (M != -INFINITY) {
-#pragma unroll 4
-              for (int c = cf; c <= cl; ++c) {
-                if (cta_range_empty(c, W, N)) continue;
-                const int64_t pc = (seg + c) * G + h;
-                const float w = exp2f(__ldcg(a.part_lse + pc) - M);
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
+              for (int c0 = 0; c0 < np; c0 += 4) {
+                float4 v[4];
+                float w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int c = c0 + u;
+                  w[u] = 0.f;
+                  v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                  if (c < np && !cta_range_empty(cf + c, W, N)) {
+                    const int64_t pc = (seg + cf + c) * G + h;
+                    v[u] = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
+                    const float l2 = (c * G + h < kMergeLse) ? merge_lse[c * G + h]
+                                                             : __ldcg(a.part_lse + pc);
+                    w[u] = exp2f(l2 - M);
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  acc.x += w[u] * v[u].x;
+                  acc.y += w[u] * v[u].y;
+                  acc.z += w[u] * v[u].z;
+                  acc.w += w[u] * v[u].w;
+                }
               }
             }
             const float inv = merge_inv[h];
