@@ -27,7 +27,9 @@
  * - Supported shapes: head_dim in {64, 128, 256}; page_size a multiple of
  *   16 (16 and 64 are the tested sizes); num_q_heads a multiple of
  *   num_kv_heads with a group of at most 8 for decode and dividing 128 for
- *   varlen.  Anything else returns PKV_ERR_UNSUPPORTED.
+ *   varlen; decode batch <= 4096 and varlen batch <= 1024 (both also bounded
+ *   by the shared memory their schedules need).  Anything else returns
+ *   PKV_ERR_UNSUPPORTED.
  * - Host-detectable argument errors return PKV_ERR_INVALID before anything
  *   is enqueued.  CUDA launch errors return PKV_ERR_CUDA (message from
  *   pkv_last_cuda_error()).
@@ -117,11 +119,11 @@ size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads,
  *                Calls that overlap on the GPU need separate workspaces.
  *                After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
  *
- * One kernel launch: a balanced split-KV pass (every CTA streams the same
- * number of 16-key tiles, cutting across sequence boundaries); partial
- * outputs of a sequence cut between CTAs are merged (log-sum-exp weights)
- * by whichever CTA finishes its piece last, found with an arrival counter
- * kept in the workspace.
+ * One persistent kernel launch: one CTA per SM takes (sequence, kv head)
+ * segments from a longest-first queue kept in the workspace; a segment
+ * longer than half of a CTA's fair share is cut into chunks whose partial
+ * outputs are merged (log-sum-exp weights) by whichever CTA delivers the
+ * last chunk, found with an arrival counter kept in the workspace.
  */
 pkv_status paged_attn_decode(void* out, const void* q,
                              const void* k_cache, const void* v_cache,

@@ -104,7 +104,7 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
   if (!(scale == scale)) return PKV_ERR_INVALID;  // NaN
   if (!supported_head_dim(head_dim) || page_size % 16 != 0 || num_q_heads / num_kv_heads > 8 ||
-      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 16384)
+      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 4096)
     return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens || !workspace)
@@ -121,6 +121,7 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
       out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
       num_kv_heads, head_dim, page_size, num_pages, max_seq_len, scale, window, workspace,
       workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), sms);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 

@@ -6,30 +6,30 @@
 // commit (key allowed iff q_pos - k_pos < window).
 //
 // Design (GB300):
-//  * Work unit = one 16-key tile of one (sequence, kv head) -- a "segment".
-//    All units of the batch are laid end to end (sequence-major, then kv
-//    head) and the grid of N resident CTAs cuts that line into N equal
-//    ranges, so every CTA streams the same number of bytes whatever the
-//    length mix (balanced split-KV).  The part of a segment inside one
-//    CTA's range is a "piece".
-//  * Producer warp: walks the range piece by piece.  For each piece it
-//    writes a record (sequence, head, tiles, ...) and the G query rows into
-//    a 4-deep record ring in shared memory, then streams the piece's K and
-//    V tiles: page ids from the block table (32 per coalesced load), TMA
-//    boxes per 16-key tile (128-byte swizzle) into an NSTAGE ring.
-//  * NW consumer warps: take the tiles of each piece round-robin.  Per tile
+//  * Work item = a (sequence, kv head) "segment" of 16-key tiles, or a chunk
+//    of one: a segment longer than half of a CTA's fair share of the batch
+//    is cut into equal chunks.  One persistent CTA per SM takes items from
+//    a device-side queue (an atomic counter in the workspace) in
+//    longest-first order, so the SMs finish together whatever the length
+//    mix, and only the few long segments need a merge.
+//  * Producer warp: grabs the next item, writes a record (sequence, head,
+//    tiles, ...) and the G query rows into a 4-deep record ring in shared
+//    memory, then streams the item's K and V tiles: page ids from the
+//    block table (32 per coalesced load), TMA boxes per 16-key tile
+//    (128-byte swizzle) into a deep NSTAGE ring.
+//  * NW consumer warps: take the tiles of each item round-robin.  Per tile
 //    a warp computes S^T = K Q^T (16 keys x 8 heads, GQA group padded to
 //    8) with mma.sync, does the online softmax (exp2, warp shuffles),
 //    transposes P in registers with movmatrix and accumulates
-//    O^T = V^T P^T with mma.sync.  At the end of a piece it hands its
+//    O^T = V^T P^T with mma.sync.  At the end of an item it hands its
 //    (m, l, O) state to the epilogue warp through a double buffer and goes
-//    straight on with the next piece: no CTA-wide barrier in the stream.
-//  * Epilogue warp: combines the consumer states of a piece (log-sum-exp
-//    weights); a piece that is a whole segment is written as the bf16
-//    output, others as a partial (o, lse) in the workspace.  The last CTA
-//    to deliver a piece of a segment -- found with a per-segment arrival
-//    counter in the workspace -- merges all its pieces and writes the
-//    output, then resets the counter to zero.  No CTA waits for another.
+//    straight on: no CTA-wide barrier in the stream.
+//  * Epilogue warp: combines the consumer states of an item (log-sum-exp
+//    weights); a whole segment is written as the bf16 output, a chunk as a
+//    partial (o, lse) in the workspace.  The last CTA to deliver a chunk of
+//    a segment -- found with a per-segment arrival counter -- merges the
+//    chunks and writes the output, then resets the counter.  The last CTA
+//    to find the queue empty resets the queue.  No CTA waits for another.
 //  * K/V bytes are read from HBM exactly once.  Launched with programmatic
 //    dependent launch: the prologue overlaps the previous kernel in the
 //    stream; griddepcontrol.wait precedes every read of the inputs.
@@ -58,6 +58,7 @@ struct DecodeArgs {
   int32_t window;
   float scale_log2;
   int32_t* seg_count;  // [batch * H_kv] arrival counters, zero between calls
+  int32_t* queue;      // [2]: next item, CTAs done; zero between calls
   float* part_lse;     // [(S + N) * G]
   float* part_o;       // [(S + N) * G * D]
   int32_t* err;
@@ -78,24 +79,16 @@ __device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, i
   t_hi = (len + kTile - 1) / kTile;
 }
 
-// CTA c of N owns units [c*W/N, (c+1)*W/N).  The CTA that owns unit x:
-__device__ __forceinline__ int owner_cta(int64_t x, int64_t W, int64_t N) {
-  return (int)(((x + 1) * N + W - 1) / W - 1);
-}
-
-__device__ __forceinline__ bool cta_range_empty(int64_t c, int64_t W, int64_t N) {
-  return c * W / N == (c + 1) * W / N;
-}
-
 // A piece as the producer hands it to the consumers and the epilogue.
 struct PieceRec {
   int b, g;          // sequence, kv head
   int first_tile;    // first 16-key tile (absolute, within the sequence)
-  int n;             // tiles in the piece; -1 terminates the stream
+  int n;             // tiles in the item; -1 terminates the stream
   int L, lo;         // attended keys [lo, L)
-  int whole;         // the piece is the whole segment
+  int nch;           // chunks of the segment (1: the item is the whole segment)
+  int slot0;         // partial slot of chunk 0 of the segment
+  int chunk;         // this item's chunk
   int pad;
-  long long seg_start, seg_end;  // segment's unit range on the global line
 };
 
 // Shared-memory plan (byte offsets from the 1024-aligned base); depends on
@@ -115,8 +108,8 @@ struct DecodePlan {
     bars = o;  o += (2 * NSTAGE + 2 * kNRec + 4) * 8;
     ok = o;    o += NSTAGE * 4;
     misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
-    scan = o;  o += (NW + 2) * 4 + 8;
-    cum = o;   o += (batch + 1) * 4;
+    scan = o;  o += (NW + 2) * 4 + 8 + 16;
+    cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
     total = 1024 + o;
   }
 };
@@ -137,7 +130,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int c) {
 }
 
 template <int D, int NW, int NSTAGE, bool ONEBOX>
-__global__ void __launch_bounds__((NW + 2) * 32)
+__global__ void __launch_bounds__((NW + 2) * 32, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
@@ -169,7 +162,10 @@ __global__ void __launch_bounds__((NW + 2) * 32)
   volatile int* merge_flag = reinterpret_cast<volatile int*>(merge_inv + kGP);
   float* merge_lse = merge_inv + kGP + 4;  // [kMergeLse]
   int* scan_tmp = reinterpret_cast<int*>(smem + plan.scan);
-  int* s_cum = reinterpret_cast<int*>(smem + plan.cum);
+  int* s_misc = scan_tmp + NW + 4;                              // [4]
+  int* s_nat = reinterpret_cast<int*>(smem + plan.cum);         // [B+1] items before b
+  int* s_sp = s_nat + (a.batch + 1);                            // [B+1] sorted prefix
+  int* s_order = s_sp + (a.batch + 1);                          // [B] sequences, longest first
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -195,124 +191,168 @@ __global__ void __launch_bounds__((NW + 2) * 32)
   }
   pdl_wait();  // inputs may come from the previous kernel in the stream
 
-  // ---- prefix sum of work units over sequences (every CTA, in smem) ----
+  // ---- work items (every CTA computes the same list, in smem) ----
+  // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
+  // than S_max = max(32, W / (2N)) tiles is cut into nch_b equal chunks.
+  auto tiles_of = [&](int b, bool flag) {
+    int L, lo, tl, th;
+    seq_extent(a, b, L, lo, tl, th, flag);
+    return th - tl;
+  };
   {
-    const int per = (B + NT - 1) / NT;
-    const int b0 = tid * per;
     int local = 0;
-    for (int b = b0; b < b0 + per && b < B; ++b) {
-      int L, lo, tl, th;
-      seq_extent(a, b, L, lo, tl, th, blockIdx.x == 0);
-      local += (th - tl) * a.H_kv;
-      // zero-length sequences have no work unit: their zero rows are written here
-      if (L == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
+    for (int b = tid; b < B; b += NT) {
+      const int t = tiles_of(b, blockIdx.x == 0);
+      local += t;
+      // zero-length sequences have no work item: their zero rows are written here
+      if (t == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
         uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.H_q * D);
         for (int i = 0; i < a.H_q * D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0) scan_tmp[warp] = local;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t tot = 0;
+      for (int w = 0; w < NT / 32; ++w) tot += scan_tmp[w];
+      const int64_t W = tot * a.H_kv;
+      const int64_t half_share = (W + 2 * (int64_t)gridDim.x - 1) / (2 * (int64_t)gridDim.x);
+      s_misc[0] = (int)(half_share > 32 ? half_share : 32);  // S_max
+    }
+    __syncthreads();
+  }
+  const int smax = s_misc[0];
+  auto nch_of = [&](int t) { return (t + smax - 1) / smax; };
+  // exclusive prefix over n values held in smem (in place), n+1 entries
+  // written; each thread scans a contiguous run, warps and runs combine
+  auto block_scan = [&](int* arr, int n) {
+    const int per = (n + NT - 1) / NT;
+    const int i0 = tid * per;
+    int local = 0;
+    for (int i = i0; i < i0 + per && i < n; ++i) local += arr[i];
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
+    __syncthreads();
     if (lane == 31) scan_tmp[warp] = incl;
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += scan_tmp[w];
-    int run = base + incl - local;
-    for (int b = b0; b < b0 + per && b < B; ++b) {
-      s_cum[b] = run;
-      int L, lo, tl, th;
-      seq_extent(a, b, L, lo, tl, th, false);
-      run += (th - tl) * a.H_kv;
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += scan_tmp[w];
+    for (int i = i0; i < i0 + per && i < n; ++i) {
+      const int v = arr[i];
+      arr[i] = run;
+      run += v;
     }
-    if (tid == NT - 1) s_cum[B] = run;
+    if (tid == NT - 1) arr[n] = run;
     __syncthreads();
+  };
+  // items per sequence (natural order) and chunk length (queue order key)
+  for (int b = tid; b < B; b += NT) {
+    const int t = tiles_of(b, false);
+    const int nch = nch_of(t);
+    s_nat[b] = nch * a.H_kv;
+    s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
   }
+  __syncthreads();
+  // queue order: sequences by chunk length, longest first (ties by index);
+  // beyond 512 sequences the natural order is kept
+  if (B <= 512) {
+    for (int b = tid; b < B; b += NT) {
+      const int cb = s_sp[b];
+      int rank = 0;
+      for (int c = 0; c < B; ++c) {
+        const int cc = s_sp[c];
+        rank += (cc > cb || (cc == cb && c < b)) ? 1 : 0;
+      }
+      s_order[rank] = b;
+    }
+  } else {
+    for (int b = tid; b < B; b += NT) s_order[b] = b;
+  }
+  __syncthreads();
+  for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
+  __syncthreads();
+  block_scan(s_nat, B);
+  block_scan(s_sp, B);
   pdl_launch_dependents();
-  const int64_t W = s_cum[B];
-  const int64_t N = gridDim.x;
-  const int64_t x0 = (int64_t)blockIdx.x * W / N;
-  const int64_t x1 = ((int64_t)blockIdx.x + 1) * W / N;
-  if (x0 >= x1) return;
+  const int T = s_nat[B];  // work items in the batch
 
   if (warp == NW) {
     // ============================ producer warp ============================
-    // The next piece's query rows and first 32 page ids are loaded into
-    // registers before the current piece is streamed, so no global-memory
-    // latency sits between two pieces.
+    // Items come from the queue one at a time; the next item's query rows
+    // and first 32 page ids are loaded into registers before the current
+    // item is streamed, so no global-memory latency sits between items.
     constexpr int QV = D / 32;  // query vectors per lane for a group of <= 8 heads
     bool dead = false;
-    int b;
-    {  // first sequence of the range: last b with s_cum[b] <= x0
-      int lo = 0, hi = B;
+    const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
+    struct Item {
+      bool more;
+      int b, g, L, lo, first_tile, n, nch, slot0, chunk;
+    };
+    auto grab = [&]() -> int {
+      int i = 0;
+      if (lane == 0) i = atomicAdd(a.queue, 1);
+      return __shfl_sync(0xffffffffu, i, 0);
+    };
+    // queue index -> item (sorted sequences; heads; chunks)
+    auto item_at = [&](int i) -> Item {
+      Item it;
+      it.more = i < T;
+      it.b = it.g = it.L = it.lo = it.first_tile = it.nch = it.slot0 = it.chunk = 0;
+      it.n = -1;
+      if (!it.more) return it;
+      int lo = 0, hi = B;  // s_sp[lo] <= i < s_sp[lo+1]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (s_cum[mid] <= x0) lo = mid; else hi = mid;
+        if (s_sp[mid] <= i) lo = mid; else hi = mid;
       }
-      b = lo;
-    }
-    const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
-    struct Piece {
-      bool more;
-      int g, L, lo, first_tile, n, bseq;
-      int64_t seg_start, seg_end;
+      const int b = s_order[lo];
+      const int j = i - s_sp[lo];
+      int L, klo, t_lo, t_hi;
+      seq_extent(a, b, L, klo, t_lo, t_hi, false);
+      const int t = t_hi - t_lo;
+      const int nch = nch_of(t);
+      const int csz = (t + nch - 1) / nch;
+      const int g = j / nch, chunk = j - (j / nch) * nch;
+      it.b = b;
+      it.g = g;
+      it.L = L;
+      it.lo = klo;
+      it.first_tile = t_lo + chunk * csz;
+      it.n = min(csz, t - chunk * csz);
+      it.nch = nch;
+      it.slot0 = s_nat[b] + g * nch;
+      it.chunk = chunk;
+      return it;
     };
-    // the piece that starts at unit x (b advances past finished sequences)
-    auto piece_at = [&](int64_t x) -> Piece {
-      Piece p;
-      p.more = false;
-      p.n = -1;
-      p.g = p.L = p.lo = p.first_tile = 0;
-      p.bseq = b;
-      p.seg_start = p.seg_end = 0;
-      while (x < x1) {
-        int L, lo, t_lo, t_hi;
-        seq_extent(a, b, L, lo, t_lo, t_hi, false);
-        const int tiles_b = t_hi - t_lo;
-        const int64_t bstart = s_cum[b];
-        if (tiles_b == 0 || x >= bstart + (int64_t)tiles_b * a.H_kv) {
-          ++b;
-          continue;
-        }
-        p.more = true;
-        p.bseq = b;
-        p.g = (int)((x - bstart) / tiles_b);
-        p.seg_start = bstart + (int64_t)p.g * tiles_b;
-        p.seg_end = p.seg_start + tiles_b;
-        p.n = (int)((p.seg_end < x1 ? p.seg_end : x1) - x);
-        p.L = L;
-        p.lo = lo;
-        p.first_tile = t_lo + (int)(x - p.seg_start);
-        break;
-      }
-      return p;
-    };
-    auto prefetch = [&](const Piece& p, uint4 (&qr)[QV], int& pages) {
+    auto prefetch = [&](const Item& p, uint4 (&qr)[QV], int& pages) {
       pages = -1;
       if (!p.more) return;
       const uint4* qsrc =
-          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.bseq * a.H_q + p.g * G) * D);
+          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.b * a.H_q + p.g * G) * D);
 #pragma unroll
       for (int i = 0; i < QV; ++i) {
         const int v = lane + 32 * i;
         if (v < qvec) qr[i] = __ldg(qsrc + v);
       }
       if (lane < p.n)
-        pages = __ldg(a.block_table + (int64_t)p.bseq * a.max_blocks +
+        pages = __ldg(a.block_table + (int64_t)p.b * a.max_blocks +
                       ((p.first_tile + lane) * kTile) / a.P);
     };
 
-    int64_t x = x0;
-    Piece cur = piece_at(x);
+    Item cur = item_at(grab());
     uint4 qcur[QV];
     int pcur;
     prefetch(cur, qcur, pcur);
     int it = 0;  // CTA-wide tile counter
-    int k = 0;   // piece counter
+    int k = 0;   // item counter
     while (true) {
-      // ---- publish the piece record and its query rows ----
+      // ---- publish the item record and its query rows ----
       const int slot = k % kNRec;
       if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
       if (cur.more) {
@@ -325,33 +365,33 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       }
       if (lane == 0) {
         PieceRec& r = recs[slot];
-        r.b = cur.bseq;
+        r.b = cur.b;
         r.g = cur.g;
         r.first_tile = cur.first_tile;
         r.n = cur.n;
         r.L = cur.L;
         r.lo = cur.lo;
-        r.whole = (cur.seg_start >= x0 && cur.seg_end <= x1) ? 1 : 0;
-        r.seg_start = cur.seg_start;
-        r.seg_end = cur.seg_end;
+        r.nch = cur.nch;
+        r.slot0 = cur.slot0;
+        r.chunk = cur.chunk;
       }
       __syncwarp();
       mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
       ++k;
       if (!cur.more) break;
-      // ---- look ahead: the next piece's inputs load while this one streams ----
-      x += cur.n;
-      const Piece nxt = piece_at(x);
+      // ---- look ahead: the next item's inputs load while this one streams ----
+      const Item nxt = item_at(grab());
       uint4 qnxt[QV];
       int pnxt;
       prefetch(nxt, qnxt, pnxt);
-      // ---- stream the piece's tiles ----
-      const int* bt = a.block_table + (int64_t)cur.bseq * a.max_blocks;
+      // ---- stream the item's tiles ----
+      const int* bt = a.block_table + (int64_t)cur.b * a.max_blocks;
       const int n = cur.n;
       int page = pcur;
       for (int k0 = 0; k0 < n; k0 += 32) {
         int page_ahead = -1;  // page ids of the following 32 tiles
-        if (k0 + 32 + lane < n) page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
+        if (k0 + 32 + lane < n)
+          page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
         const int cnt = min(32, n - k0);
         for (int j = 0; j < cnt; ++j) {
           const int pg = __shfl_sync(0xffffffffu, page, j);
@@ -392,6 +432,15 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       for (int i = 0; i < QV; ++i) qcur[i] = qnxt[i];
       pcur = pnxt;
     }
+    // queue exhausted for this CTA: the last CTA to get here resets it
+    if (lane == 0) {
+      __threadfence();
+      const int done = atomicAdd(a.queue + 1, 1);
+      if (done == (int)gridDim.x - 1) {
+        a.queue[0] = 0;
+        a.queue[1] = 0;
+      }
+    }
     // drain: every issued load must land before the CTA may exit
     if (lane == 0) {
       const int first = it > NSTAGE ? it - NSTAGE : 0;
@@ -429,7 +478,11 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
       const int n = rec.n;
-      for (int kk = ((warp - it_base) % NW + NW) % NW; kk < n; kk += NW) {
+      // this warp takes the item's tiles kk = r, r+NW, ...; r depends only on
+      // where the item starts in the stage ring, and the epilogue combines
+      // the warps in r order, so the result does not depend on the CTA
+      const int r0 = ((warp - it_base) % NW + NW) % NW;
+      for (int kk = r0; kk < n; kk += NW) {
         const int it = it_base + kk;
         const int s = it % NSTAGE;
         const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
@@ -511,8 +564,8 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       }
       const int cb = k & 1;
       if (k >= 2) mbar_wait(comb_empty + cb, ((k >> 1) - 1) & 1, a.err, dead);
-      float* co = comb_o + ((cb * NW + warp) * G) * CS;
-      float* cml = comb_ml + ((cb * NW + warp) * G) * 2;
+      float* co = comb_o + ((cb * NW + r0) * G) * CS;
+      float* cml = comb_ml + ((cb * NW + r0) * G) * 2;
       const int hA = 2 * qlan, hB = hA + 1;
 #pragma unroll
       for (int md = 0; md < KS; ++md) {
@@ -550,10 +603,10 @@ __global__ void __launch_bounds__((NW + 2) * 32)
       const int cb = k & 1;
       mbar_wait(comb_full + cb, (k >> 1) & 1, a.err, dead);
       const int b = rec.b, g = rec.g;
-      const int64_t seg = (int64_t)b * a.H_kv + g;
-      const int64_t piece = seg + blockIdx.x;
+      const bool whole = rec.nch == 1;
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
+      const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
       for (int e = lane; e < G * D; e += 32) {
         const int h = e / D, d = e - (e / D) * D;
         float M = -INFINITY;
@@ -569,68 +622,51 @@ __global__ void __launch_bounds__((NW + 2) * 32)
           }
         }
         const float val = lsum > 0.f ? acc / lsum : 0.f;
-        if (rec.whole) {
+        if (whole) {
           a.out[((int64_t)b * a.H_q + g * G + h) * D + d] = __float2bfloat16_rn(val);
         } else {
-          a.part_o[(piece * G + h) * D + d] = val;
-          if (d == 0) a.part_lse[piece * G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+          a.part_o[(pslot * G + h) * D + d] = val;
+          if (d == 0) a.part_lse[pslot * G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
         }
       }
       __syncwarp();
       mbar_arrive(comb_empty + cb);  // the consumers may refill this buffer
-      if (!rec.whole) {
-        // arrival counter: the last CTA to deliver a piece of this segment
+      if (!whole) {
+        // arrival counter: the last CTA to deliver a chunk of this segment
         // merges all of them (nobody waits; the counter is reset afterwards)
+        const int64_t seg = (int64_t)b * a.H_kv + g;
         __threadfence();
         __syncwarp();
-        const int cf = owner_cta(rec.seg_start, W, N);
-        const int cl = owner_cta(rec.seg_end - 1, W, N);
         if (lane == 0) {
-          int npieces = 0;
-          for (int c = cf; c <= cl; ++c) npieces += cta_range_empty(c, W, N) ? 0 : 1;
           const int old = atomicAdd(a.seg_count + seg, 1);
-          *merge_flag = (old == npieces - 1) ? 1 : 0;
+          *merge_flag = (old == rec.nch - 1) ? 1 : 0;
         }
         __syncwarp();
         if (*merge_flag) {
           __threadfence();
-          // (1) every (piece, head) log2-sum-exp in one round of loads, the
+          const int np = rec.nch;
+          // (1) every (chunk, head) log2-sum-exp in one round of loads, the
           //     per-head max and weight sum from shared memory
-          const int np = cl - cf + 1;
-          for (int i = lane; i < np * G; i += 32) {
-            const int c = cf + i / G, h = i - (i / G) * G;
-            float v = -INFINITY;
-            if (!cta_range_empty(c, W, N)) v = __ldcg(a.part_lse + (seg + c) * G + h);
-            if (i < kMergeLse) merge_lse[i] = v;
-          }
+          for (int i = lane; i < np * G && i < kMergeLse; i += 32)
+            merge_lse[i] = __ldcg(a.part_lse + ((int64_t)rec.slot0 + i / G) * G + (i % G));
           __syncwarp();
+          auto lse_at = [&](int c, int h) -> float {
+            return c * G + h < kMergeLse ? merge_lse[c * G + h]
+                                         : __ldcg(a.part_lse + ((int64_t)rec.slot0 + c) * G + h);
+          };
           if (lane < G) {
             const int h = lane;
             float M = -INFINITY;
-            for (int c = 0; c < np; ++c) {
-              const float v = (c * G + h < kMergeLse)
-                                  ? merge_lse[c * G + h]
-                                  : (cta_range_empty(cf + c, W, N)
-                                         ? -INFINITY
-                                         : __ldcg(a.part_lse + (seg + cf + c) * G + h));
-              M = fmaxf(M, v);
-            }
+            for (int c = 0; c < np; ++c) M = fmaxf(M, lse_at(c, h));
             float sum = 0.f;
             if (M != -INFINITY)
-              for (int c = 0; c < np; ++c) {
-                const float v = (c * G + h < kMergeLse)
-                                    ? merge_lse[c * G + h]
-                                    : (cta_range_empty(cf + c, W, N)
-                                           ? -INFINITY
-                                           : __ldcg(a.part_lse + (seg + cf + c) * G + h));
-                sum += exp2f(v - M);
-              }
+              for (int c = 0; c < np; ++c) sum += exp2f(lse_at(c, h) - M);
             merge_m[h] = M;
             merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
           }
           __syncwarp();
-          // (2) weighted sum of the pieces' outputs, 4 dims per lane; the
-          //     loads of all pieces are issued before any is used
+          // (2) weighted sum of the chunks' outputs, 4 dims per lane; the
+          //     loads of 4 chunks are issued before any is used
           for (int j = lane; j < G * (D / 4); j += 32) {
             const int h = j / (D / 4), d4 = j - h * (D / 4);
             const float M = merge_m[h];
@@ -644,12 +680,10 @@ __global__ void __launch_bounds__((NW + 2) * 32)
                   const int c = c0 + u;
                   w[u] = 0.f;
                   v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                  if (c < np && !cta_range_empty(cf + c, W, N)) {
-                    const int64_t pc = (seg + cf + c) * G + h;
+                  if (c < np) {
+                    const int64_t pc = ((int64_t)rec.slot0 + c) * G + h;
                     v[u] = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
-                    const float l2 = (c * G + h < kMergeLse) ? merge_lse[c * G + h]
-                                                             : __ldcg(a.part_lse + pc);
-                    w[u] = exp2f(l2 - M);
+                    w[u] = exp2f(lse_at(c, h) - M);
                   }
                 }
 #pragma unroll
@@ -680,27 +714,27 @@ __global__ void __launch_bounds__((NW + 2) * 32)
 
 // --------------------------------------------------------------- host side
 // Launch shape per head_dim: consumer warps, pipeline stages (16-key K+V
-// tiles) per CTA, resident CTAs per SM at most.  Overridable at build time
-// for tuning sweeps.
+// tiles) per CTA, resident CTAs per SM.  Overridable at build time for
+// tuning sweeps.
 #ifndef PKV_DEC_NW
-#define PKV_DEC_NW 2
+#define PKV_DEC_NW 4
 #endif
 #ifndef PKV_DEC_NSTAGE
-#define PKV_DEC_NSTAGE 4
+#define PKV_DEC_NSTAGE 16
 #endif
 #ifndef PKV_DEC_CTAS
-#define PKV_DEC_CTAS 4
+#define PKV_DEC_CTAS 1
 #endif
 #ifndef PKV_DEC_ONEBOX
 #define PKV_DEC_ONEBOX 1   // head_dim 128: one contiguous 4 KB TMA box per tile
 #endif
 template <int D>
 struct DecodeCfg;
-template <> struct DecodeCfg<64> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 4; };
+template <> struct DecodeCfg<64> { static constexpr int NW = 4, NSTAGE = 16, CTAS_PER_SM = 1; };
 template <> struct DecodeCfg<128> {
   static constexpr int NW = PKV_DEC_NW, NSTAGE = PKV_DEC_NSTAGE, CTAS_PER_SM = PKV_DEC_CTAS;
 };
-template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 2; };
+template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 8, CTAS_PER_SM = 1; };
 
 static int decode_ctas_per_sm(int D) {
   switch (D) {
@@ -712,13 +746,19 @@ static int decode_ctas_per_sm(int D) {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: [seg_count: batch*H_kv int32] ... [part_lse: pieces*G f32][part_o: pieces*G*D f32]
+// Work items (and so partial slots) are at most one per segment plus 2 per
+// CTA: a segment is cut into chunks of >= W/(2N) tiles.
+static int64_t decode_max_pieces(int32_t batch, int32_t H_kv, int32_t D, int num_sms) {
+  return (int64_t)batch * H_kv + 2 * (int64_t)num_sms * decode_ctas_per_sm(D);
+}
+
+// Workspace: [seg_count: batch*H_kv int32][queue: 2 int32] ...
+//            [part_lse: pieces*G f32][part_o: pieces*G*D f32]
 // (partials aligned to the end of the caller's buffer)
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
-  const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
-  const int64_t pieces = (int64_t)batch * H_kv + nmax;
+  const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
   const int64_t G = H_q / H_kv;
-  return align256((size_t)batch * H_kv * 4) + align256((size_t)pieces * G * 4) +
+  return align256(((size_t)batch * H_kv + 2) * 4) + align256((size_t)pieces * G * 4) +
          align256((size_t)pieces * G * D * 4);
 }
 
@@ -729,6 +769,7 @@ static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void
   using P_ = DecodePlan<D, C::NW, C::NSTAGE>;
   constexpr bool kOneBox = (D == 128) && (PKV_DEC_ONEBOX != 0);
   auto kern = decode_split_kernel<D, C::NW, C::NSTAGE, kOneBox>;
+  (void)max_seq_len;
   CUtensorMap tmK, tmV;
   const bool enc_ok =
       kOneBox ? (encode_pool_map_halves(&tmK, k_cache, a.P, a.num_pages, a.H_kv) &&
@@ -759,14 +800,8 @@ static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void
   }
   int per_sm = occupancy[dev] < C::CTAS_PER_SM ? occupancy[dev] : C::CTAS_PER_SM;
   if (per_sm < 1) per_sm = 1;
-  // grid: one wave of resident CTAs, but >= ~4 tiles each on the longest
-  // possible batch
-  int64_t max_keys = max_seq_len;
-  if (a.window > 0 && max_keys > a.window) max_keys = a.window;
-  const int64_t max_units = (int64_t)a.batch * a.H_kv * ((max_keys + kTile - 1) / kTile + 1);
-  int64_t n = (int64_t)num_sms * per_sm;
-  if (n > (max_units + 3) / 4) n = (max_units + 3) / 4;
-  if (n < 1) n = 1;
+  // persistent grid: every resident CTA takes items until the queue is empty
+  const int64_t n = (int64_t)num_sms * per_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n);
   cfg.blockDim = dim3((C::NW + 2) * 32);
@@ -803,10 +838,10 @@ cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const v
   // Counters sit at the front and the partial results at the back of the
   // workspace, so calls with different batch sizes that share one
   // workspace never see each other's partials in their counter slots.
-  const int64_t nmax = (int64_t)num_sms * decode_ctas_per_sm(D);
-  const int64_t pieces = (int64_t)batch * H_kv + nmax;
+  const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.seg_count = reinterpret_cast<int32_t*>(ws);
+  a.queue = a.seg_count + (int64_t)batch * H_kv;
   uint8_t* end = ws + (workspace_bytes & ~size_t(255));
   end -= align256((size_t)pieces * a.G * D * 4);
   a.part_o = reinterpret_cast<float*>(end);

@@ -79,8 +79,9 @@ pkv_status paged_attn_decode_static(void* out, const void* q, const void* k_cach
   void* scratch = nullptr;
   if (e == cudaSuccess) e = scratch_address(dev, &scratch);
   if (e == cudaSuccess) {
-    // the arrival counters (the first batch*num_kv_heads int32) must start at zero
-    e = cudaMemsetAsync(scratch, 0, (size_t)batch * num_kv_heads * sizeof(int32_t),
+    // the arrival and queue counters (the first batch*num_kv_heads + 2
+    // int32) must start at zero
+    e = cudaMemsetAsync(scratch, 0, ((size_t)batch * num_kv_heads + 2) * sizeof(int32_t),
                         static_cast<cudaStream_t>(stream));
   }
   if (e != cudaSuccess) {
