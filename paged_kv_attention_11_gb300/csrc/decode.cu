@@ -140,6 +140,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
   constexpr int kBoxBytes = kTile * 128;
   constexpr int CS = P_::kCombStride;
+  constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;  // producer lanes issuing TMA
   const int G = a.G;
   const P_ plan(G, a.batch);
 
@@ -393,11 +394,15 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         if (k0 + 32 + lane < n)
           page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
         const int cnt = min(32, n - k0);
-        for (int j = 0; j < cnt; ++j) {
-          const int pg = __shfl_sync(0xffffffffu, page, j);
-          if (lane == 0) {
-            const int s = it % NSTAGE;
-            const int r = it / NSTAGE;
+        // NL lanes issue NL tiles at once, each into its own stage: one warp
+        // instruction launches NL TMA copies instead of one
+        for (int j0 = 0; j0 < cnt; j0 += kIssueLanes) {
+          const int j = j0 + lane;
+          const int pg = __shfl_sync(0xffffffffu, page, j & 31);
+          if (lane < kIssueLanes && j < cnt) {
+            const int itj = it + j;
+            const int s = itj % NSTAGE;
+            const int r = itj / NSTAGE;
             if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
             const int key0 = (cur.first_tile + k0 + j) * kTile;
             const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
@@ -423,8 +428,9 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
               mbar_arrive(full + s);
             }
           }
-          ++it;
+          __syncwarp();
         }
+        it += cnt;
         page = page_ahead;
       }
       cur = nxt;

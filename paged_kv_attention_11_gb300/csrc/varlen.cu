@@ -43,6 +43,7 @@
 namespace pkv {
 
 constexpr int kVBN = 64;  // keys per K/V tile
+constexpr int kMaxSortPairs = 512;  // (chunk, item) pairs ordered by exact length
 
 struct VarlenArgs {
   __nv_bfloat16* out;
@@ -53,6 +54,7 @@ struct VarlenArgs {
   int32_t max_blocks;
   int32_t max_q;       // clamp for q_len (max_seqlen_q)
   int32_t R;           // max items per (chunk, head) = ceil(max_q / (NQ*QP))
+  int32_t pairs_max;   // batch * R: an upper bound of the (chunk, item) pairs
   int32_t H_q, H_kv, G, log2G, P, box_rows;
   int64_t num_pages;
   float scale_log2;
@@ -75,11 +77,14 @@ struct VarlenSmem {
   // s_full[NQ], s_free[NQ], p_full[NQ], o_done[NQ]
   static constexpr int kNumBars = 10 + 4 * NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
-  static constexpr int kSchedOff = kTmemOff + 16;        // then: order[B] n_items[B] cum[R+1]
-  // at least 116 KB so that only one CTA (and its 512 TMEM columns) fits
-  // on an SM
-  static size_t bytes(int batch, int R) {
-    const size_t need = kSchedOff + (size_t)batch * 8 + (size_t)(R + 1) * 4 + 16;
+  static constexpr int kSchedOff = kTmemOff + 16;
+  // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
+  // P = min(pairs, kMaxSortPairs)
+  static size_t bytes(int batch, int pairs) {
+    const size_t np = (size_t)(pairs < kMaxSortPairs ? pairs : kMaxSortPairs);
+    const size_t need = kSchedOff + (size_t)batch * 8 + (size_t)(batch + 1) * 4 + np * 8 + 16;
+    // at least 116 KB so that only one CTA (and its 512 TMEM columns) fits
+    // on an SM
     return 1024 + (need > 116 * 1024 ? need : 116 * 1024);
   }
 };
@@ -88,6 +93,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA/ALU pipes, for x <= 8 (the softmax's stale-max bound):
+// x = n + f with n = round(x) (added to the exponent field) and
+// f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise relative error on
+// that interval (max relative error 2.2e-4, below bf16 resolution of P).
+// x < -125 returns 0 like the hardware exp2 of a masked (-inf) score.
+__device__ __forceinline__ float poly_exp2(float x) {
+  const float xc = fmaxf(x, -125.f);
+  const float t = xc + 12582912.f;  // 1.5 * 2^23: rounds xc to an integer
+  const int n = __float_as_int(t) - 0x4B400000;
+  const float f = xc - (t - 12582912.f);
+  float p = fmaf(0.05286737531423569f, f, 0.24215202033519745f);
+  p = fmaf(p, f, 0.6935867667198181f);
+  p = fmaf(p, f, 0.9999627470970154f);
+  const float y = __int_as_float(__float_as_int(p) + (n << 23));
+  return x < -125.f ? 0.f : y;
 }
 
 // Item geometry shared by every role of the CTA.
@@ -152,9 +174,11 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
   uint64_t* p_full = bars + 10 + 2 * NQ;  // [NQ]
   uint64_t* o_done = bars + 10 + 3 * NQ;  // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
-  int* s_order = reinterpret_cast<int*>(smem + S_::kSchedOff);  // chunks by item count
-  int* s_nitem = s_order + a.batch;                            // items per (chunk, head)
-  int* s_cum = s_nitem + a.batch;                              // [R+1] items before group r
+  int* s_qlen = reinterpret_cast<int*>(smem + S_::kSchedOff);  // clamped q_len per chunk
+  int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
+  int* s_pfx = s_klen + a.batch;                               // [B+1] pairs before chunk b
+  int* s_key = s_pfx + a.batch + 1;                            // KV tiles of pair p
+  int* s_porder = s_key + min(a.pairs_max, kMaxSortPairs);     // pairs, most tiles first
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -189,66 +213,80 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
   pdl_wait();  // inputs may come from the previous kernel in the stream
 
   // ------------------------------------------------ schedule (every CTA)
+  // A pair (chunk b, item qp) covers NQ Q tiles of chunk b; with the H_kv
+  // heads it makes H_kv work items of equal cost.  Pairs are ordered by
+  // their number of KV tiles, most first (exactly, up to kMaxSortPairs
+  // pairs; beyond that in chunk order), and the sorted items are dealt to
+  // the CTAs in a snake (0..N-1, N-1..0, ...) so that every CTA gets a
+  // similar total.
+  const int kcap = a.max_blocks * a.P;
   for (int b = tid; b < B; b += NT) {
-    const int q0 = __ldg(a.cu_q + b);
-    int ql = __ldg(a.cu_q + b + 1) - q0;
-    if (ql < 0) ql = 0;
-    if (ql > a.max_q) ql = a.max_q;
-    int ni = (ql + NQ * QP - 1) / (NQ * QP);
-    if (ni > a.R) ni = a.R;
-    s_nitem[b] = ni;
-  }
-  __syncthreads();
-  // chunks ordered by item count, descending (ties by index): rank sort
-  for (int b = tid; b < B; b += NT) {
-    const int nb = s_nitem[b];
-    int rank = 0;
-    for (int c = 0; c < B; ++c) {
-      const int nc = s_nitem[c];
-      rank += (nc > nb || (nc == nb && c < b)) ? 1 : 0;
-    }
-    s_order[rank] = b;
-  }
-  __syncthreads();
-  // group r holds the item at distance r from the end of every chunk that
-  // has more than r items; those chunks are a prefix of s_order
-  for (int r = tid; r < a.R; r += NT) {
-    int lo = 0, hi = B;  // first position whose chunk has <= r items
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s_nitem[s_order[mid]] > r) lo = mid + 1; else hi = mid;
-    }
-    s_cum[r + 1] = lo * a.H_kv;
-  }
-  if (tid == 0) s_cum[0] = 0;
-  __syncthreads();
-  if (tid == 0) {  // prefix over groups (R = chunk length / rows per item: small)
-    for (int r = 1; r <= a.R; ++r) s_cum[r] += s_cum[r - 1];
-  }
-  __syncthreads();
-  const int T = s_cum[a.R];
-  pdl_launch_dependents();
-
-  // item i -> (chunk, head, index within chunk); identical in every role
-  auto item_at = [&](int i) -> Item {
-    int lo = 0, hi = a.R;  // group r: s_cum[r] <= i < s_cum[r+1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_cum[mid] <= i) lo = mid; else hi = mid;
-    }
-    const int r = lo;
-    const int j = i - s_cum[r];
-    const int b = s_order[j / a.H_kv];
-    const int g = j - (j / a.H_kv) * a.H_kv;
     const int q0 = __ldg(a.cu_q + b);
     int ql = __ldg(a.cu_q + b + 1) - q0;
     int kl = __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b);
-    if (ql < 0) ql = 0;
-    if (ql > a.max_q) ql = a.max_q;
-    const int kcap = a.max_blocks * a.P;
-    if (kl < 0) kl = 0;
-    if (kl > kcap) kl = kcap;
-    return make_item<NQ>(a, b, g, s_nitem[b] - 1 - r, q0, ql, kl);
+    ql = ql < 0 ? 0 : (ql > a.max_q ? a.max_q : ql);
+    kl = kl < 0 ? 0 : (kl > kcap ? kcap : kl);
+    s_qlen[b] = ql;
+    s_klen[b] = kl;
+  }
+  __syncthreads();
+  if (tid == 0) {  // pair prefix over chunks (B <= 1024)
+    int run = 0;
+    for (int b = 0; b < B; ++b) {
+      s_pfx[b] = run;
+      int ni = (s_qlen[b] + NQ * QP - 1) / (NQ * QP);
+      run += ni < a.R ? ni : a.R;
+    }
+    s_pfx[B] = run;
+  }
+  __syncthreads();
+  const int TP = s_pfx[B];
+  const bool sorted = TP <= kMaxSortPairs;
+  auto pair_at = [&](int p, int& b, int& qp) {
+    int lo = 0, hi = B;  // s_pfx[lo] <= p < s_pfx[lo+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pfx[mid] <= p) lo = mid; else hi = mid;
+    }
+    b = lo;
+    qp = p - s_pfx[lo];
+  };
+  if (sorted) {
+    for (int p = tid; p < TP; p += NT) {
+      int b, qp;
+      pair_at(p, b, qp);
+      s_key[p] = make_item<NQ>(a, b, 0, qp, 0, s_qlen[b], s_klen[b]).n;
+    }
+    __syncthreads();
+    for (int p = tid; p < TP; p += NT) {
+      const int kp = s_key[p];
+      int rank = 0;
+      for (int j = 0; j < TP; ++j) {
+        const int kj = s_key[j];
+        rank += (kj > kp || (kj == kp && j < p)) ? 1 : 0;
+      }
+      s_porder[rank] = p;
+    }
+  }
+  __syncthreads();
+  const int T = TP * a.H_kv;
+  pdl_launch_dependents();
+
+  // item i (sorted order) -> (chunk, head, item within chunk); identical in
+  // every role
+  auto item_at = [&](int i) -> Item {
+    const int sp = i / a.H_kv;
+    const int g = i - sp * a.H_kv;
+    const int p = sorted ? s_porder[sp] : sp;
+    int b, qp;
+    pair_at(p, b, qp);
+    return make_item<NQ>(a, b, g, qp, __ldg(a.cu_q + b), s_qlen[b], s_klen[b]);
+  };
+  // the k-th item of this CTA (snake over the CTAs)
+  const int NC = gridDim.x;
+  auto my_item = [&](int k) -> int {
+    const int c = (k & 1) ? NC - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    return k * NC + c;
   };
 
   tc::fence_before_sync();
@@ -278,7 +316,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
     const int oob = (int)(a.num_pages * a.H_kv);  // first z past the pool: zero fill
     int t = 0;      // KV tiles issued by this CTA
     int nitem = 0;  // non-empty items loaded by this CTA
-    for (int i = blockIdx.x; i < T; i += gridDim.x) {
+    for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
       const Item it = item_at(i);
       if (it.n == 0) continue;
       const int* bt = a.block_table + (int64_t)it.b * a.max_blocks;
@@ -368,7 +406,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
         }
         tc::commit(v_empty + vb);
       };
-      for (int i = blockIdx.x; i < T; i += gridDim.x) {
+      for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
         const Item it = item_at(i);
         if (it.n == 0) continue;
         mbar_wait(q_full, nitem & 1, a.err, dead);
@@ -418,7 +456,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
     const uint32_t prow = sP + x * S_::kPBytes + r * 128;
     const float sl2 = a.scale_log2;
     int t = 0;
-    for (int i = blockIdx.x; i < T; i += gridDim.x) {
+    for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
       const Item it = item_at(i);
       const int p = it.p_begin + x * QP + (r >> a.log2G);  // chunk row of this thread
       const bool row_valid = p < it.q_len;
@@ -488,8 +526,11 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(s[u * 8 + 2 * e]), sl2, -mu));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(s[u * 8 + 2 * e + 1]), sl2, -mu));
+            // half of the exponentials on the SFU, half on the FMA pipes
+            const float x0 = fmaf(__uint_as_float(s[u * 8 + 2 * e]), sl2, -mu);
+            const float x1 = fmaf(__uint_as_float(s[u * 8 + 2 * e + 1]), sl2, -mu);
+            const float p0 = (u & 1) ? poly_exp2(x0) : fast_exp2(x0);
+            const float p1 = (u & 1) ? poly_exp2(x1) : fast_exp2(x1);
             sum += p0 + p1;
             w[e] = pack_bf16(p0, p1);
           }
@@ -555,7 +596,7 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
                                    cudaStream_t stream, int num_sms) {
   using S_ = VarlenSmem<D, NQ>;
   auto kern = varlen_fwd_kernel<D, NQ>;
-  const size_t smem = S_::bytes(a.batch, a.R);
+  const size_t smem = S_::bytes(a.batch, a.pairs_max);
   if (smem > 227 * 1024) return cudaErrorNotSupported;
   static int configured[64] = {0};
   int dev = 0;
@@ -618,12 +659,15 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
   switch (D) {
     case 64:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
+      a.pairs_max = batch * a.R;
       return launch_varlen_t<64, 2>(a, maps, stream, num_sms);
     case 128:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
+      a.pairs_max = batch * a.R;
       return launch_varlen_t<128, 2>(a, maps, stream, num_sms);
     case 256:
       a.R = (max_seqlen_q + QP - 1) / QP;
+      a.pairs_max = batch * a.R;
       return launch_varlen_t<256, 1>(a, maps, stream, num_sms);
     default:
       return cudaErrorNotSupported;
