@@ -108,7 +108,7 @@ struct DecodePlan {
     bars = o;  o += (2 * NSTAGE + 2 * kNRec + 4) * 8;
     ok = o;    o += NSTAGE * 4;
     misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
-    scan = o;  o += (NW + 2) * 4 + 8 + 16;
+    scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
     cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
     total = 1024 + o;
   }
@@ -191,19 +191,21 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     tma_prefetch_desc(&tmV);
   }
   pdl_wait();  // inputs may come from the previous kernel in the stream
+  // the producer's first queue grab is issued now; its latency hides behind
+  // the prologue
+  int first_grab = 0;
+  if (warp == NW && lane == 0) first_grab = atomicAdd(a.queue, 1);
 
   // ---- work items (every CTA computes the same list, in smem) ----
   // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
   // than S_max = max(32, W / (2N)) tiles is cut into nch_b equal chunks.
-  auto tiles_of = [&](int b, bool flag) {
-    int L, lo, tl, th;
-    seq_extent(a, b, L, lo, tl, th, flag);
-    return th - tl;
-  };
   {
     int local = 0;
     for (int b = tid; b < B; b += NT) {
-      const int t = tiles_of(b, blockIdx.x == 0);
+      int L, lo, tl, th;
+      seq_extent(a, b, L, lo, tl, th, blockIdx.x == 0);
+      const int t = th - tl;
+      s_nat[b] = t;  // tiles, for now
       local += t;
       // zero-length sequences have no work item: their zero rows are written here
       if (t == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
@@ -226,35 +228,9 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   }
   const int smax = s_misc[0];
   auto nch_of = [&](int t) { return (t + smax - 1) / smax; };
-  // exclusive prefix over n values held in smem (in place), n+1 entries
-  // written; each thread scans a contiguous run, warps and runs combine
-  auto block_scan = [&](int* arr, int n) {
-    const int per = (n + NT - 1) / NT;
-    const int i0 = tid * per;
-    int local = 0;
-    for (int i = i0; i < i0 + per && i < n; ++i) local += arr[i];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    __syncthreads();
-    if (lane == 31) scan_tmp[warp] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int w = 0; w < warp; ++w) run += scan_tmp[w];
-    for (int i = i0; i < i0 + per && i < n; ++i) {
-      const int v = arr[i];
-      arr[i] = run;
-      run += v;
-    }
-    if (tid == NT - 1) arr[n] = run;
-    __syncthreads();
-  };
   // items per sequence (natural order) and chunk length (queue order key)
   for (int b = tid; b < B; b += NT) {
-    const int t = tiles_of(b, false);
+    const int t = s_nat[b];
     const int nch = nch_of(t);
     s_nat[b] = nch * a.H_kv;
     s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
@@ -277,9 +253,49 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   }
   __syncthreads();
   for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
-  __syncthreads();
-  block_scan(s_nat, B);
-  block_scan(s_sp, B);
+  // both exclusive prefixes in one pass: each thread scans a contiguous run
+  {
+    const int per = (B + NT - 1) / NT;
+    const int i0 = tid * per;
+    __syncthreads();
+    int l1 = 0, l2 = 0;
+    for (int i = i0; i < i0 + per && i < B; ++i) {
+      l1 += s_nat[i];
+      l2 += s_sp[i];
+    }
+    int c1 = l1, c2 = l2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v1 = __shfl_up_sync(0xffffffffu, c1, o);
+      const int v2 = __shfl_up_sync(0xffffffffu, c2, o);
+      if (lane >= o) {
+        c1 += v1;
+        c2 += v2;
+      }
+    }
+    if (lane == 31) {
+      scan_tmp[warp] = c1;
+      s_misc[4 + warp] = c2;
+    }
+    __syncthreads();
+    int r1 = c1 - l1, r2 = c2 - l2;
+    for (int w = 0; w < warp; ++w) {
+      r1 += scan_tmp[w];
+      r2 += s_misc[4 + w];
+    }
+    for (int i = i0; i < i0 + per && i < B; ++i) {
+      const int v1 = s_nat[i], v2 = s_sp[i];
+      s_nat[i] = r1;
+      s_sp[i] = r2;
+      r1 += v1;
+      r2 += v2;
+    }
+    if (tid == NT - 1) {
+      s_nat[B] = r1;
+      s_sp[B] = r2;
+    }
+    __syncthreads();
+  }
   pdl_launch_dependents();
   const int T = s_nat[B];  // work items in the batch
 
@@ -346,7 +362,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
                       ((p.first_tile + lane) * kTile) / a.P);
     };
 
-    Item cur = item_at(grab());
+    Item cur = item_at(__shfl_sync(0xffffffffu, first_grab, 0));
     uint4 qcur[QV];
     int pcur;
     prefetch(cur, qcur, pcur);
@@ -380,11 +396,6 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
       ++k;
       if (!cur.more) break;
-      // ---- look ahead: the next item's inputs load while this one streams ----
-      const Item nxt = item_at(grab());
-      uint4 qnxt[QV];
-      int pnxt;
-      prefetch(nxt, qnxt, pnxt);
       // ---- stream the item's tiles ----
       const int* bt = a.block_table + (int64_t)cur.b * a.max_blocks;
       const int n = cur.n;
@@ -433,10 +444,10 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         it += cnt;
         page = page_ahead;
       }
-      cur = nxt;
-#pragma unroll
-      for (int i = 0; i < QV; ++i) qcur[i] = qnxt[i];
-      pcur = pnxt;
+      // ---- next item: grabbed only once this one is issued, so no CTA holds
+      //      work in reserve at the end; the stage ring covers the latency ----
+      cur = item_at(grab());
+      prefetch(cur, qcur, pcur);
     }
     // queue exhausted for this CTA: the last CTA to get here resets it
     if (lane == 0) {
@@ -613,26 +624,51 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
       const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
-      for (int e = lane; e < G * D; e += 32) {
-        const int h = e / D, d = e - (e / D) * D;
+      // per head: weight of each consumer warp's state, 1/l, log2-sum-exp
+      float* wsc = merge_lse;  // [NW][G] scratch (the merge below reloads it)
+      if (lane < G) {
+        const int h = lane;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, cml[(w * G + h) * 2]);
-        float acc = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
+        float lsum = 0.f;
 #pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            const float sc = exp2f(cml[(w * G + h) * 2] - M);
-            acc += sc * co[(w * G + h) * CS + d];
-            lsum += sc * cml[(w * G + h) * 2 + 1];
-          }
+        for (int w = 0; w < NW; ++w) {
+          const float sc = M == -INFINITY ? 0.f : exp2f(cml[(w * G + h) * 2] - M);
+          wsc[w * G + h] = sc;
+          lsum += sc * cml[(w * G + h) * 2 + 1];
         }
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        merge_m[h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+        merge_inv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
+      }
+      __syncwarp();
+      for (int j = lane; j < G * (D / 4); j += 32) {
+        const int h = j / (D / 4), d4 = j - h * (D / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float sc = wsc[w * G + h];
+          const float4 v = *reinterpret_cast<const float4*>(co + (w * G + h) * CS + d4 * 4);
+          acc.x += sc * v.x;
+          acc.y += sc * v.y;
+          acc.z += sc * v.z;
+          acc.w += sc * v.w;
+        }
+        const float inv = merge_inv[h];
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
         if (whole) {
-          a.out[((int64_t)b * a.H_q + g * G + h) * D + d] = __float2bfloat16_rn(val);
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+          __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+          *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) = pk;
         } else {
-          a.part_o[(pslot * G + h) * D + d] = val;
-          if (d == 0) a.part_lse[pslot * G + h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+          *reinterpret_cast<float4*>(a.part_o + (pslot * G + h) * D + d4 * 4) = acc;
+          if (d4 == 0) a.part_lse[pslot * G + h] = merge_m[h];
         }
       }
       __syncwarp();
