@@ -43,7 +43,7 @@
 namespace pkv {
 
 constexpr int kVBN = 64;  // keys per K/V tile
-constexpr int kMaxSortPairs = 512;  // (chunk, item) pairs ordered by exact length
+constexpr int kMaxSortPairs = 256;  // (chunk, item) pairs ordered by exact length
 
 struct VarlenArgs {
   __nv_bfloat16* out;
@@ -62,7 +62,7 @@ struct VarlenArgs {
   int32_t* err;
 };
 
-template <int D, int NQ>
+template <int D, int NQ, int NKV>
 struct VarlenSmem {
   static constexpr int kQBytes = 128 * D * 2;            // one Q tile
   static constexpr int kKVChunk = kVBN * 128;            // one 64-column chunk of a K/V tile
@@ -70,12 +70,12 @@ struct VarlenSmem {
   static constexpr int kPBytes = 128 * kVBN * 2;         // one P tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + NQ * kQBytes;
-  static constexpr int kVOff = kKOff + 2 * kKVBytes;
-  static constexpr int kPOff = kVOff + 2 * kKVBytes;
+  static constexpr int kVOff = kKOff + NKV * kKVBytes;
+  static constexpr int kPOff = kVOff + NKV * kKVBytes;
   static constexpr int kBarOff = kPOff + NQ * kPBytes;
-  // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2],
+  // q_full, q_empty, k_full[NKV], k_empty[NKV], v_full[NKV], v_empty[NKV],
   // s_full[NQ], s_free[NQ], p_full[NQ], o_done[NQ]
-  static constexpr int kNumBars = 10 + 4 * NQ;
+  static constexpr int kNumBars = 2 + 4 * NKV + 4 * NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
@@ -147,13 +147,13 @@ __device__ __forceinline__ Item make_item(const VarlenArgs& a, int b, int g, int
   return it;
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
+template <int D, int NQ, int NKV>
+__global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
     varlen_fwd_kernel(const VarlenArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-  using S_ = VarlenSmem<D, NQ>;
-  constexpr int NT = (2 + 4 * NQ) * 32;
+  using S_ = VarlenSmem<D, NQ, NKV>;
+  constexpr int NT = (3 + 4 * NQ) * 32;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kVBN, false);
   constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, D, true);
@@ -165,14 +165,14 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S_::kBarOff);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;   // [2]
-  uint64_t* k_empty = bars + 4;  // [2]
-  uint64_t* v_full = bars + 6;   // [2]
-  uint64_t* v_empty = bars + 8;  // [2]
-  uint64_t* s_full = bars + 10;           // [NQ]
-  uint64_t* s_free = bars + 10 + NQ;      // [NQ]
-  uint64_t* p_full = bars + 10 + 2 * NQ;  // [NQ]
-  uint64_t* o_done = bars + 10 + 3 * NQ;  // [NQ]
+  uint64_t* k_full = bars + 2;               // [NKV]
+  uint64_t* k_empty = k_full + NKV;          // [NKV]
+  uint64_t* v_full = k_empty + NKV;          // [NKV]
+  uint64_t* v_empty = v_full + NKV;          // [NKV]
+  uint64_t* s_full = v_empty + NKV;          // [NQ]
+  uint64_t* s_free = s_full + NQ;            // [NQ]
+  uint64_t* p_full = s_free + NQ;            // [NQ]
+  uint64_t* o_done = p_full + NQ;            // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
   int* s_qlen = reinterpret_cast<int*>(smem + S_::kSchedOff);  // clamped q_len per chunk
   int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
   if (tid == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NKV; ++i) {
       mbar_init(k_full + i, 1);
       mbar_init(k_empty + i, 1);
       mbar_init(v_full + i, 1);
@@ -308,19 +308,27 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
     }
   }
 
-  if (warp == 0) {
-    // ============================== TMA producer ============================
+  if (warp == 0 || warp == 2 + 4 * NQ) {
+    // ========================= TMA producers (K and V) ======================
+    // Warp 0 loads Q and K, the last warp loads V: the two rings run
+    // independently, so a K tile never waits for a V stage to be released
+    // (which would tie the K prefetch to the PV progress).
+    const bool isK = warp == 0;
     bool dead = false;
     const int R = a.box_rows;
     const int nsub = kVBN / R;
     const int oob = (int)(a.num_pages * a.H_kv);  // first z past the pool: zero fill
+    uint64_t* ring_full = isK ? k_full : v_full;
+    uint64_t* ring_empty = isK ? k_empty : v_empty;
+    const CUtensorMap* tm = isK ? &tmK : &tmV;
+    const int ring_off = isK ? S_::kKOff : S_::kVOff;
     int t = 0;      // KV tiles issued by this CTA
     int nitem = 0;  // non-empty items loaded by this CTA
     for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
       const Item it = item_at(i);
       if (it.n == 0) continue;
       const int* bt = a.block_table + (int64_t)it.b * a.max_blocks;
-      if (lane == 0) {
+      if (isK && lane == 0) {
         if (nitem > 0) mbar_wait(q_empty, (nitem - 1) & 1, a.err, dead);
         mbar_arrive_expect_tx(q_full, NQ * S_::kQBytes);
 #pragma unroll
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
           if (key0 < it.kv_hi && key0 + R > it.kv_lo) {
             const int pg = __ldg(bt + key0 / a.P);
             if (pg >= 0 && (int64_t)pg < a.num_pages) z = pg * a.H_kv + it.g;
-            else raise_err(a.err, PKV_DEVERR_PAGE);
+            else if (isK) raise_err(a.err, PKV_DEVERR_PAGE);
           }
         }
         int zs[4], rows[4];
@@ -350,97 +358,90 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
           rows[i2] = __shfl_sync(0xffffffffu, row, i2);
         }
         if (lane == 0) {
-          const int s = t & 1;
-          if (t >= 2) mbar_wait(k_empty + s, ((t >> 1) - 1) & 1, a.err, dead);
-          mbar_arrive_expect_tx(k_full + s, S_::kKVBytes);
-          uint8_t* kdst = smem + S_::kKOff + s * S_::kKVBytes;
+          const int s = t % NKV;
+          const int rr = t / NKV;
+          if (rr >= 1) mbar_wait(ring_empty + s, (rr - 1) & 1, a.err, dead);
+          mbar_arrive_expect_tx(ring_full + s, S_::kKVBytes);
+          uint8_t* dst = smem + ring_off + s * S_::kKVBytes;
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2)
             if (i2 < nsub)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(kdst + c * S_::kKVChunk + i2 * R * 128, &tmK, k_full + s, c * 64,
-                            rows[i2], zs[i2]);
-          if (t >= 2) mbar_wait(v_empty + s, ((t >> 1) - 1) & 1, a.err, dead);
-          mbar_arrive_expect_tx(v_full + s, S_::kKVBytes);
-          uint8_t* vdst = smem + S_::kVOff + s * S_::kKVBytes;
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2)
-            if (i2 < nsub)
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(vdst + c * S_::kKVChunk + i2 * R * 128, &tmV, v_full + s, c * 64,
+                tma_load_3d(dst + c * S_::kKVChunk + i2 * R * 128, tm, ring_full + s, c * 64,
                             rows[i2], zs[i2]);
         }
         __syncwarp();
       }
     }
     if (lane == 0) {  // every issued copy must land before the CTA exits
-      for (int u = (t > 2 ? t - 2 : 0); u < t; ++u) {
-        mbar_wait(k_full + (u & 1), (u >> 1) & 1, a.err, dead);
-        mbar_wait(v_full + (u & 1), (u >> 1) & 1, a.err, dead);
-      }
-      if (nitem > 0) mbar_wait(q_full, (nitem - 1) & 1, a.err, dead);
+      for (int u = (t > NKV ? t - NKV : 0); u < t; ++u)
+        mbar_wait(ring_full + (u % NKV), (u / NKV) & 1, a.err, dead);
+      if (isK && nitem > 0) mbar_wait(q_full, (nitem - 1) & 1, a.err, dead);
     }
   } else if (warp == 1) {
     // =============================== MMA issuer =============================
     if (lane == 0) {
       bool dead = false;
       int t = 0, nitem = 0;
-      auto pv = [&](int u, bool first) {
-        const int vb = u & 1;
-        mbar_wait(v_full + vb, (u >> 1) & 1, a.err, dead);
-        const uint32_t vbase = sV + vb * S_::kKVBytes;
+      // descriptor low halves of the operand bases (K-major Q, K, P: LBO 16;
+      // MN-major V: LBO = the 64-column chunk stride); all share one high half
+      constexpr uint32_t kHi = tc::sw128_hi(1024);
+      const uint32_t q_lo0 = tc::sw128_lo(sQ, 16);
+      const uint32_t k_lo0 = tc::sw128_lo(sK, 16);
+      const uint32_t p_lo0 = tc::sw128_lo(sP, 16);
+      const uint32_t v_lo0 = tc::sw128_lo(sV, S_::kKVChunk);
+      // O_x += P_x V(u) for Q tile x; V(u) must have landed
+      auto pv_x = [&](int u, int x, bool first) {
+        const int vb = u % NKV;
+        mbar_wait(v_full + vb, (u / NKV) & 1, a.err, dead);
+        mbar_wait(p_full + x, u & 1, a.err, dead);
+        tc::fence_after_sync();
+        const uint32_t alo = p_lo0 + x * (S_::kPBytes >> 4);
+        const uint32_t blo = v_lo0 + vb * (S_::kKVBytes >> 4);
 #pragma unroll
-        for (int x = 0; x < NQ; ++x) {
-          mbar_wait(p_full + x, u & 1, a.err, dead);
-          tc::fence_after_sync();
-          const uint32_t pbase = sP + x * S_::kPBytes;
-#pragma unroll
-          for (int ks = 0; ks < kVBN / 16; ++ks) {
-            const uint64_t ad = tc::smem_desc_sw128(pbase + ks * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(vbase + ks * 2048, S_::kKVChunk, 1024);
-            tc::mma_ss(tmem + kOCol + x * D, ad, bd, kIdescO, (!first || ks > 0) ? 1u : 0u);
-          }
-          tc::commit(o_done + x);
-        }
-        tc::commit(v_empty + vb);
+        for (int ks = 0; ks < kVBN / 16; ++ks)
+          tc::mma_ss_h(tmem + kOCol + x * D, alo + ks * (32 >> 4), kHi, blo + ks * (2048 >> 4),
+                       kHi, kIdescO, (!first || ks > 0) ? 1u : 0u);
+        tc::commit(o_done + x);
       };
       for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
         const Item it = item_at(i);
         if (it.n == 0) continue;
         mbar_wait(q_full, nitem & 1, a.err, dead);
         for (int j = 0; j < it.n; ++j, ++t) {
-          const int kb = t & 1;
-          mbar_wait(k_full + kb, (t >> 1) & 1, a.err, dead);
-          const uint32_t kbase = sK + kb * S_::kKVBytes;
+          const int kb = t % NKV;
+          mbar_wait(k_full + kb, (t / NKV) & 1, a.err, dead);
+          const uint32_t klo = k_lo0 + kb * (S_::kKVBytes >> 4);
+          // per Q tile: S_x of this KV tile, then PV_x of the previous one, so
+          // one warpgroup's softmax never waits on the other's progress
 #pragma unroll
           for (int x = 0; x < NQ; ++x) {
             if (t >= 1) mbar_wait(s_free + x, (t - 1) & 1, a.err, dead);
             tc::fence_after_sync();
-            const uint32_t qbase = sQ + x * S_::kQBytes;
+            const uint32_t qlo = q_lo0 + x * (S_::kQBytes >> 4);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint64_t ad =
-                  tc::smem_desc_sw128(qbase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = tc::smem_desc_sw128(
-                  kbase + (ks >> 2) * S_::kKVChunk + (ks & 3) * 32, 16, 1024);
-              tc::mma_ss(tmem + x * kVBN, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
-            }
+            for (int ks = 0; ks < D / 16; ++ks)
+              tc::mma_ss_h(tmem + x * kVBN, qlo + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), kHi,
+                           klo + (((ks >> 2) * S_::kKVChunk + (ks & 3) * 32) >> 4), kHi,
+                           kIdescS, ks > 0 ? 1u : 0u);
             tc::commit(s_full + x);
+            if (j >= 1) pv_x(t - 1, x, j == 1);
           }
           if (j == it.n - 1) tc::commit(q_empty);
           tc::commit(k_empty + kb);
-          if (j >= 1) pv(t - 1, j == 1);
+          if (j >= 1) tc::commit(v_empty + ((t - 1) % NKV));
         }
-        pv(t - 1, it.n == 1);
+#pragma unroll
+        for (int x = 0; x < NQ; ++x) pv_x(t - 1, x, it.n == 1);
+        tc::commit(v_empty + ((t - 1) % NKV));
         ++nitem;
       }
       // the stage-release arrivals must land before the CTA (and its smem)
       // goes away
-      for (int u = (t > 2 ? t - 2 : 0); u < t; ++u) {
-        mbar_wait(k_empty + (u & 1), (u >> 1) & 1, a.err, dead);
-        mbar_wait(v_empty + (u & 1), (u >> 1) & 1, a.err, dead);
+      for (int u = (t > NKV ? t - NKV : 0); u < t; ++u) {
+        mbar_wait(k_empty + (u % NKV), (u / NKV) & 1, a.err, dead);
+        mbar_wait(v_empty + (u % NKV), (u / NKV) & 1, a.err, dead);
       }
       if (nitem > 0) mbar_wait(q_empty, (nitem - 1) & 1, a.err, dead);
     }
@@ -491,19 +492,23 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
         // mask only where a key of this tile falls outside a row's range
         const int key0 = (it.t_lo + j) * kVBN;
         const bool inside = key0 >= klo && key0 + kVBN <= khi;
-        float mx = -INFINITY;
+        float mxp[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mxp[c] = -INFINITY;
         if (__all_sync(0xffffffffu, inside)) {
 #pragma unroll
-          for (int c = 0; c < kVBN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+          for (int c = 0; c < kVBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], __uint_as_float(s[c]));
         } else {
 #pragma unroll
           for (int c = 0; c < kVBN; ++c) {
             const int k = key0 + c;
             const float v = (k >= klo && k < khi) ? __uint_as_float(s[c]) : -INFINITY;
             s[c] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+            mxp[c & 7] = fmaxf(mxp[c & 7], v);
           }
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         // running max in the log2 domain (scale > 0 commutes with max)
         const float mt = mx * sl2;
         const float m_new = fmaxf(m, mt);
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
           mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
           tc::fence_after_sync();
         }
-        float sum = 0.f;
+        float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < kVBN / 8; ++u) {
           uint32_t w[4];
@@ -531,7 +536,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
             const float x1 = fmaf(__uint_as_float(s[u * 8 + 2 * e + 1]), sl2, -mu);
             const float p0 = (u & 1) ? poly_exp2(x0) : fast_exp2(x0);
             const float p1 = (u & 1) ? poly_exp2(x1) : fast_exp2(x1);
-            sum += p0 + p1;
+            sp[e] += p0 + p1;
             w[e] = pack_bf16(p0, p1);
           }
           const uint32_t addr = prow + ((u ^ (r & 7)) << 4);
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
         }
-        l += sum;
+        l += (sp[0] + sp[1]) + (sp[2] + sp[3]);
         if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -591,13 +596,17 @@ __global__ void __launch_bounds__((2 + 4 * NQ) * 32, 1)
 }
 
 // --------------------------------------------------------------- host side
-template <int D, int NQ>
+template <int D, int NQ, int NKV>
 static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
                                    cudaStream_t stream, int num_sms) {
-  using S_ = VarlenSmem<D, NQ>;
-  auto kern = varlen_fwd_kernel<D, NQ>;
+  using S_ = VarlenSmem<D, NQ, NKV>;
+  auto kern = varlen_fwd_kernel<D, NQ, NKV>;
   const size_t smem = S_::bytes(a.batch, a.pairs_max);
-  if (smem > 227 * 1024) return cudaErrorNotSupported;
+  if (smem > 227 * 1024) {
+    // the deep K/V ring does not fit next to this batch's schedule: use 2 stages
+    if (NKV > 2) return launch_varlen_t<D, NQ, 2>(a, maps, stream, num_sms);
+    return cudaErrorNotSupported;
+  }
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -614,7 +623,7 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
   if (grid <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((2 + 4 * NQ) * 32);
+  cfg.blockDim = dim3((3 + 4 * NQ) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -660,15 +669,15 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
     case 64:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<64, 2>(a, maps, stream, num_sms);
+      return launch_varlen_t<64, 2, 4>(a, maps, stream, num_sms);
     case 128:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<128, 2>(a, maps, stream, num_sms);
+      return launch_varlen_t<128, 2, 4>(a, maps, stream, num_sms);
     case 256:
       a.R = (max_seqlen_q + QP - 1) / QP;
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<256, 1>(a, maps, stream, num_sms);
+      return launch_varlen_t<256, 1, 2>(a, maps, stream, num_sms);
     default:
       return cudaErrorNotSupported;
   }
