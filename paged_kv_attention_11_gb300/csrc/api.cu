@@ -152,7 +152,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   int sms = 0;
   if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
   pkv::VarlenMaps maps;
-  const int kv_rows = 64;  // keys per KV tile
+  const int kv_rows = pkv::varlen_kv_tile(head_dim);  // keys per KV tile
   const int box_rows = page_size < kv_rows ? page_size : kv_rows;
   // a KV tile must be whole page slices: page_size divides it or is a
   // multiple of it

@@ -34,6 +34,10 @@ struct VarlenMaps {
   CUtensorMap v;  // same for V
 };
 
+// keys per KV tile of the varlen kernel for a head_dim (page_size must
+// divide it or be a multiple of it)
+int varlen_kv_tile(int head_dim);
+
 cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,
                           const int32_t* cu_k, const int32_t* block_table, int32_t max_blocks,
                           int32_t batch, int32_t max_seqlen_q, int32_t total_q, int32_t H_q,

@@ -100,6 +100,19 @@ __device__ __forceinline__ void mma_ss_h(uint32_t d_tmem, uint32_t a_lo, uint32_
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc given as halves]: A is M=128 lanes x
+// K columns of packed 16-bit pairs.
+__device__ __forceinline__ void mma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(

@@ -17,23 +17,30 @@
 //    the kv head, so a K/V tile staged once in shared memory feeds the
 //    whole GQA group and, with NQ = 2, two Q tiles.
 //  * Every CTA derives the same schedule from cu_seq_lens in its prologue:
-//    items are ordered by their distance from the end of their chunk (the
-//    last item of each chunk -- the one that sees the most keys -- first),
-//    chunks with more items first; CTA c takes items c, c+grid, ...
-//  * Warp 0: TMA producer (Q tiles per item; K and V 64-key tiles through
-//    two 2-deep rings, one box per page slice, 128-byte swizzle).  Boxes
-//    outside the attended key range or the pool are fetched at an
-//    out-of-range coordinate, which fills zeros.
-//  * Warp 1: allocates 512 TMEM columns and issues tcgen05.mma
-//    (cta_group::1, kind::f16, bf16 in, fp32 accumulate):
-//        S_x  = Q_x K^T   (M=128, N=64, K=D)   one S buffer per Q tile
-//        O_x += P_x V     (M=128, N=D,  K=64)  P from smem, V MN-major
+//    (chunk, item) pairs sorted by their number of KV tiles, most first,
+//    dealt to the CTAs in a snake so that every CTA gets a similar total.
+//  * The CTA's items form one stream of KV tiles; no role drains at an
+//    item boundary.  Warp 0 loads (TMA, 128-byte swizzle, one box per page
+//    slice, lane-parallel issue) in the order the tensor core consumes:
+//    K of the first NS tiles, then V(t), K(t+NS) for every tile t, through
+//    one ring of NSLOT slots; Q tiles when the stream enters an item.
+//  * Warp 1 allocates 512 TMEM columns and issues tcgen05.mma (cta_group::1,
+//    kind::f16, bf16 in, fp32 accumulate):
+//        S_x(t)  = Q_x K(t)^T        smem x smem -> TMEM  (M=128, N=BN)
+//        O_x    += P_x(t) V(t)       TMEM x smem -> TMEM  (M=128, N=D)
+//    P_x(t) is written by the softmax into the TMEM columns of S_x(t), as
+//    bf16 pairs, and read from there by the PV MMA.  Per tile t and Q tile
+//    x the issue order is PV_x(t), QK_x(t+NS): the tensor pipe runs in
+//    issue order, so S_x(t+NS) may reuse the columns P_x(t) was read from.
+//    With NQ = 2 (NS = 1) the two Q tiles' softmaxes alternate with the
+//    tensor core; with NQ = 1 (NS = 2, head_dim 256) S is double-buffered
+//    so that QK of the next tile runs under the softmax of this one.
 //  * One softmax warpgroup per Q tile (one thread per row): tcgen05.ld the
-//    S row, mask, online softmax in the exp2 domain, write P (bf16,
-//    swizzled) to smem, rescale O in TMEM only when the running max grew
-//    by more than 2^8 (the stale max is exact math: O and l share it),
-//    epilogue O / l -> bf16.  The two warpgroups alternate with the tensor
-//    core: while one runs its softmax the MMAs of the other proceed.
+//    S row, mask (boundary tiles only), online softmax in the exp2 domain
+//    (packed f32x2 arithmetic; a quarter of the exponentials on the FMA
+//    pipes, the rest on the SFU), P -> TMEM, rescale O in TMEM only when the
+//    running max grew by more than 2^8 (the stale max is exact math: O and
+//    l share it), epilogue O / l -> bf16.
 #include <math.h>
 
 #include "common.cuh"
@@ -42,7 +49,6 @@
 
 namespace pkv {
 
-constexpr int kVBN = 64;  // keys per K/V tile
 constexpr int kMaxSortPairs = 256;  // (chunk, item) pairs ordered by exact length
 
 struct VarlenArgs {
@@ -62,20 +68,17 @@ struct VarlenArgs {
   int32_t* err;
 };
 
-template <int D, int NQ, int NKV>
+template <int D, int NQ, int BN, int NS, int NSLOT>
 struct VarlenSmem {
-  static constexpr int kQBytes = 128 * D * 2;            // one Q tile
-  static constexpr int kKVChunk = kVBN * 128;            // one 64-column chunk of a K/V tile
-  static constexpr int kKVBytes = (D / 64) * kKVChunk;   // one K (or V) tile
-  static constexpr int kPBytes = 128 * kVBN * 2;         // one P tile
+  static constexpr int kQBytes = 128 * D * 2;              // one Q tile
+  static constexpr int kKVChunk = BN * 128;                // one 64-column chunk of a K/V tile
+  static constexpr int kSlotBytes = (D / 64) * kKVChunk;   // one K or V tile
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + NQ * kQBytes;
-  static constexpr int kVOff = kKOff + NKV * kKVBytes;
-  static constexpr int kPOff = kVOff + NKV * kKVBytes;
-  static constexpr int kBarOff = kPOff + NQ * kPBytes;
-  // q_full, q_empty, k_full[NKV], k_empty[NKV], v_full[NKV], v_empty[NKV],
-  // s_full[NQ], s_free[NQ], p_full[NQ], o_done[NQ]
-  static constexpr int kNumBars = 2 + 4 * NKV + 4 * NQ;
+  static constexpr int kSlotOff = kQOff + NQ * kQBytes;
+  static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
+  // q_full[NQ] q_empty[NQ] slot_full[NSLOT] slot_empty[NSLOT]
+  // s_full[NQ*NS] p_full[NQ*NS] o_done[NQ]
+  static constexpr int kNumBars = 2 * NQ + 2 * NSLOT + 2 * NQ * NS + NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
@@ -95,21 +98,67 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x on the FMA/ALU pipes, for x <= 8 (the softmax's stale-max bound):
-// x = n + f with n = round(x) (added to the exponent field) and
-// f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise relative error on
-// that interval (max relative error 2.2e-4, below bf16 resolution of P).
-// x < -125 returns 0 like the hardware exp2 of a masked (-inf) score.
-__device__ __forceinline__ float poly_exp2(float x) {
-  const float xc = fmaxf(x, -125.f);
-  const float t = xc + 12582912.f;  // 1.5 * 2^23: rounds xc to an integer
-  const int n = __float_as_int(t) - 0x4B400000;
-  const float f = xc - (t - 12582912.f);
-  float p = fmaf(0.05286737531423569f, f, 0.24215202033519745f);
-  p = fmaf(p, f, 0.6935867667198181f);
-  p = fmaf(p, f, 0.9999627470970154f);
-  const float y = __int_as_float(__float_as_int(p) + (n << 23));
-  return x < -125.f ? 0.f : y;
+// packed pairs of fp32 (one 64-bit register pair; the f32x2 forms issue two
+// lanes of FMA-pipe work per instruction)
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair, on the FMA/ALU pipes, for x <= 8 (the softmax's
+// stale-max bound): x = n + f with n = round(x) (added to the exponent
+// field) and f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise
+// relative error on that interval (max relative error 2.2e-4, below bf16
+// resolution of P).  x is clamped at -125 (a masked, -inf score gives
+// 2^-125 * 2^f instead of 0: below 2^-100 of the row sum, which holds at
+// least one term >= 2^-8).
+__device__ __forceinline__ uint64_t poly_exp2x2(uint64_t x) {
+  float x0, x1;
+  f2_split(x, x0, x1);
+  const uint64_t xc = f2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
+  const uint64_t kMagic = f2(12582912.f, 12582912.f);  // 1.5 * 2^23: rounds to an integer
+  const uint64_t tt = f2_add(xc, kMagic);
+  const uint64_t f = f2_sub(xc, f2_sub(tt, kMagic));
+  uint64_t p = f2_fma(f2(0.05286737531423569f, 0.05286737531423569f), f,
+                      f2(0.24215202033519745f, 0.24215202033519745f));
+  p = f2_fma(p, f, f2(0.6935867667198181f, 0.6935867667198181f));
+  p = f2_fma(p, f, f2(0.9999627470970154f, 0.9999627470970154f));
+  float t0, t1, p0, p1;
+  f2_split(tt, t0, t1);
+  f2_split(p, p0, p1);
+  const int n0 = __float_as_int(t0) - 0x4B400000;
+  const int n1 = __float_as_int(t1) - 0x4B400000;
+  return f2(__int_as_float(__float_as_int(p0) + (n0 << 23)),
+            __int_as_float(__float_as_int(p1) + (n1 << 23)));
 }
 
 // Item geometry shared by every role of the CTA.
@@ -121,7 +170,7 @@ struct Item {
   int kv_lo, kv_hi;      // attended key range of the item
 };
 
-template <int NQ>
+template <int NQ, int BN>
 __device__ __forceinline__ Item make_item(const VarlenArgs& a, int b, int g, int qp, int q0,
                                           int q_len, int k_len) {
   Item it;
@@ -142,37 +191,54 @@ __device__ __forceinline__ Item make_item(const VarlenArgs& a, int b, int g, int
   }
   it.kv_lo = lo;
   it.kv_hi = hi;
-  it.t_lo = lo / kVBN;
-  it.n = hi > lo ? (hi + kVBN - 1) / kVBN - it.t_lo : 0;
+  it.t_lo = lo / BN;
+  it.n = hi > lo ? (hi + BN - 1) / BN - it.t_lo : 0;
   return it;
 }
 
-template <int D, int NQ, int NKV>
-__global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
+// Position in the CTA's stream of KV tiles: item ordinal k of this CTA,
+// tile j of that item, and m, the ordinal of the item among the CTA's
+// non-empty items (the phase count of the Q buffers).
+struct Cursor {
+  int k, j, m;
+  Item it;
+};
+
+// Warps: 4*NQ softmax warps (warpgroup x = Q tile x), then one warpgroup
+// holding the TMA producer, the MMA issuer and two idle warps (whole
+// warpgroups, so that registers can move to the softmax with setmaxnreg).
+template <int NQ>
+__host__ __device__ constexpr int varlen_threads() {
+  return (4 * NQ + 4) * 32;
+}
+
+template <int D, int NQ, int BN, int NS, int NSLOT>
+__global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     varlen_fwd_kernel(const VarlenArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-  using S_ = VarlenSmem<D, NQ, NKV>;
-  constexpr int NT = (3 + 4 * NQ) * 32;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NSLOT>;
+  constexpr int NT = varlen_threads<NQ>();
+  constexpr int kProdWarp = 4 * NQ;
+  constexpr int kMmaWarp = 4 * NQ + 1;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kVBN, false);
+  constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, BN, false);
   constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, D, true);
-  constexpr int kOCol = NQ * kVBN;  // O_x at kOCol + x*D; S_x at x*kVBN
+  constexpr int kOCol = NQ * NS * BN;  // S/P buffer (x, b) at (x*NS + b)*BN; O_x at kOCol + x*D
+  static_assert(kOCol + NQ * D <= (int)kTmemCols, "TMEM columns");
+  static_assert(BN == 64 || BN == 128, "KV tile");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S_::kBarOff);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;               // [NKV]
-  uint64_t* k_empty = k_full + NKV;          // [NKV]
-  uint64_t* v_full = k_empty + NKV;          // [NKV]
-  uint64_t* v_empty = v_full + NKV;          // [NKV]
-  uint64_t* s_full = v_empty + NKV;          // [NQ]
-  uint64_t* s_free = s_full + NQ;            // [NQ]
-  uint64_t* p_full = s_free + NQ;            // [NQ]
-  uint64_t* o_done = p_full + NQ;            // [NQ]
+  uint64_t* q_full = bars;                     // [NQ]
+  uint64_t* q_empty = q_full + NQ;             // [NQ]
+  uint64_t* slot_full = q_empty + NQ;          // [NSLOT]
+  uint64_t* slot_empty = slot_full + NSLOT;    // [NSLOT]
+  uint64_t* s_full = slot_empty + NSLOT;       // [NQ*NS]
+  uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS]
+  uint64_t* o_done = p_full + NQ * NS;         // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
   int* s_qlen = reinterpret_cast<int*>(smem + S_::kSchedOff);  // clamped q_len per chunk
   int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
@@ -187,26 +253,25 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
   const int QP = 128 >> a.log2G;
 
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int i = 0; i < NKV; ++i) {
-      mbar_init(k_full + i, 1);
-      mbar_init(k_empty + i, 1);
-      mbar_init(v_full + i, 1);
-      mbar_init(v_empty + i, 1);
-    }
     for (int x = 0; x < NQ; ++x) {
-      mbar_init(s_full + x, 1);
-      mbar_init(s_free + x, 128);
-      mbar_init(p_full + x, 128);
+      mbar_init(q_full + x, 1);
+      mbar_init(q_empty + x, 1);
       mbar_init(o_done + x, 1);
+    }
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(slot_full + i, 1);
+      mbar_init(slot_empty + i, 1);
+    }
+    for (int i = 0; i < NQ * NS; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 128);
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(tmem_holder, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -255,7 +320,7 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
     for (int p = tid; p < TP; p += NT) {
       int b, qp;
       pair_at(p, b, qp);
-      s_key[p] = make_item<NQ>(a, b, 0, qp, 0, s_qlen[b], s_klen[b]).n;
+      s_key[p] = make_item<NQ, BN>(a, b, 0, qp, 0, s_qlen[b], s_klen[b]).n;
     }
     __syncthreads();
     for (int p = tid; p < TP; p += NT) {
@@ -280,7 +345,7 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
     const int p = sorted ? s_porder[sp] : sp;
     int b, qp;
     pair_at(p, b, qp);
-    return make_item<NQ>(a, b, g, qp, __ldg(a.cu_q + b), s_qlen[b], s_klen[b]);
+    return make_item<NQ, BN>(a, b, g, qp, __ldg(a.cu_q + b), s_qlen[b], s_klen[b]);
   };
   // the k-th item of this CTA (snake over the CTAs)
   const int NC = gridDim.x;
@@ -288,15 +353,39 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
     const int c = (k & 1) ? NC - 1 - (int)blockIdx.x : (int)blockIdx.x;
     return k * NC + c;
   };
+  // step to the next KV tile of the CTA's stream (skipping items without
+  // keys); false at the end.  Start from {k = -1, j = 0, m = -1, it.n = 0}.
+  auto next_tile = [&](Cursor& c) -> bool {
+    if (++c.j < c.it.n) return true;
+    while (true) {
+      const int i = my_item(++c.k);
+      if (i >= T) {
+        c.it.n = 0;
+        return false;
+      }
+      c.it = item_at(i);
+      if (c.it.n > 0) {
+        c.j = 0;
+        ++c.m;
+        return true;
+      }
+    }
+  };
+  auto cursor0 = []() {
+    Cursor c;
+    c.k = -1;
+    c.j = 0;
+    c.m = -1;
+    c.it.n = 0;
+    return c;
+  };
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
   const uint32_t sQ = smem_u32(smem + S_::kQOff);
-  const uint32_t sK = smem_u32(smem + S_::kKOff);
-  const uint32_t sV = smem_u32(smem + S_::kVOff);
-  const uint32_t sP = smem_u32(smem + S_::kPOff);
+  const uint32_t sSlot = smem_u32(smem + S_::kSlotOff);
 
   if (blockIdx.x == 0 && tid == 0) {  // report clamped lengths once
     for (int b = 0; b < B; ++b) {
@@ -308,154 +397,191 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
     }
   }
 
-  if (warp == 0 || warp == 2 + 4 * NQ) {
-    // ========================= TMA producers (K and V) ======================
-    // Warp 0 loads Q and K, the last warp loads V: the two rings run
-    // independently, so a K tile never waits for a V stage to be released
-    // (which would tie the K prefetch to the PV progress).
-    const bool isK = warp == 0;
+  // the producer and the MMA issuer hold few registers, the softmax many;
+  // each role's code sits under its own register change.  Launch: 384
+  // threads x 168 registers; after the change 4 warps x 104 + 8 warps x 200
+  // use the same total, and every SM sub-partition holds at most 504 per lane.
+  if (warp >= kProdWarp) {
+    if (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+  if (warp == kProdWarp) {
+    // ============================== TMA producer ==============================
     bool dead = false;
     const int R = a.box_rows;
-    const int nsub = kVBN / R;
+    const int nbox = BN / R;                      // boxes per tile (<= 8)
     const int oob = (int)(a.num_pages * a.H_kv);  // first z past the pool: zero fill
-    uint64_t* ring_full = isK ? k_full : v_full;
-    uint64_t* ring_empty = isK ? k_empty : v_empty;
-    const CUtensorMap* tm = isK ? &tmK : &tmV;
-    const int ring_off = isK ? S_::kKOff : S_::kVOff;
-    int t = 0;      // KV tiles issued by this CTA
-    int nitem = 0;  // non-empty items loaded by this CTA
-    for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
-      const Item it = item_at(i);
-      if (it.n == 0) continue;
-      const int* bt = a.block_table + (int64_t)it.b * a.max_blocks;
-      if (isK && lane == 0) {
-        if (nitem > 0) mbar_wait(q_empty, (nitem - 1) & 1, a.err, dead);
-        mbar_arrive_expect_tx(q_full, NQ * S_::kQBytes);
-#pragma unroll
-        for (int x = 0; x < NQ; ++x)
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(smem + S_::kQOff + x * S_::kQBytes + c * 16384, &tmQ, q_full, c * 64, 0,
-                        it.g, it.q0 + it.p_begin + x * QP);
+    // (z, row) of this lane's box of the cursor's tile; boxes outside the
+    // attended range (or on a bad page) are fetched at z = oob: zeros
+    auto tile_box = [&](const Cursor& c, int& z, int& row) {
+      z = oob;
+      row = 0;
+      if (lane < nbox) {
+        const int key0 = (c.it.t_lo + c.j) * BN + lane * R;
+        row = key0 % a.P;
+        if (key0 < c.it.kv_hi && key0 + R > c.it.kv_lo) {
+          const int pg = __ldg(a.block_table + (int64_t)c.it.b * a.max_blocks + key0 / a.P);
+          if (pg >= 0 && (int64_t)pg < a.num_pages) z = pg * a.H_kv + c.it.g;
+          else raise_err(a.err, PKV_DEVERR_PAGE);
+        }
       }
-      ++nitem;
-      for (int j = 0; j < it.n; ++j, ++t) {
-        const int key_base = (it.t_lo + j) * kVBN;
-        int z = oob, row = 0;
-        if (lane < nsub) {
-          const int key0 = key_base + lane * R;
-          row = key0 % a.P;
-          if (key0 < it.kv_hi && key0 + R > it.kv_lo) {
-            const int pg = __ldg(bt + key0 / a.P);
-            if (pg >= 0 && (int64_t)pg < a.num_pages) z = pg * a.H_kv + it.g;
-            else if (isK) raise_err(a.err, PKV_DEVERR_PAGE);
-          }
-        }
-        int zs[4], rows[4];
+    };
+    int ev = 0;  // load events issued (K and V tiles, in consumption order)
+    auto load_tile = [&](int z, int row, const CUtensorMap* tm) {
+      const int s = ev % NSLOT;
+      if (lane == 0) {
+        if (ev >= NSLOT) mbar_wait(slot_empty + s, ((ev / NSLOT) - 1) & 1, a.err, dead);
+        mbar_arrive_expect_tx(slot_full + s, S_::kSlotBytes);
+      }
+      __syncwarp();
+      if (lane < nbox) {
+        uint8_t* dst = smem + S_::kSlotOff + s * S_::kSlotBytes + lane * R * 128;
 #pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) {
-          zs[i2] = __shfl_sync(0xffffffffu, z, i2);
-          rows[i2] = __shfl_sync(0xffffffffu, row, i2);
-        }
-        if (lane == 0) {
-          const int s = t % NKV;
-          const int rr = t / NKV;
-          if (rr >= 1) mbar_wait(ring_empty + s, (rr - 1) & 1, a.err, dead);
-          mbar_arrive_expect_tx(ring_full + s, S_::kKVBytes);
-          uint8_t* dst = smem + ring_off + s * S_::kKVBytes;
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(dst + c * S_::kKVChunk, tm, slot_full + s, c * 64, row, z);
+      }
+      ++ev;
+    };
+    auto load_q = [&](const Cursor& c) {  // lane 0: the Q tiles of the cursor's item
 #pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2)
-            if (i2 < nsub)
+      for (int x = 0; x < NQ; ++x) {
+        if (c.m >= 1) mbar_wait(q_empty + x, (c.m - 1) & 1, a.err, dead);
+        mbar_arrive_expect_tx(q_full + x, S_::kQBytes);
 #pragma unroll
-              for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(dst + c * S_::kKVChunk + i2 * R * 128, tm, ring_full + s, c * 64,
-                            rows[i2], zs[i2]);
-        }
-        __syncwarp();
+        for (int ch = 0; ch < D / 64; ++ch)
+          tma_load_4d(smem + S_::kQOff + x * S_::kQBytes + ch * 16384, &tmQ, q_full + x, ch * 64,
+                      0, c.it.g, c.it.q0 + c.it.p_begin + x * QP);
+      }
+    };
+    Cursor ck = cursor0();
+    bool hk = next_tile(ck);
+    int zk = oob, rk = 0;
+    if (hk) tile_box(ck, zk, rk);  // page ids one K tile ahead of its load
+    int zq[NS], rq[NS];            // boxes of the tiles whose V is still to load
+    bool vq[NS];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+      vq[u] = hk;
+      zq[u] = zk;
+      rq[u] = rk;
+      if (hk) {
+        if (ck.j == 0 && lane == 0) load_q(ck);
+        load_tile(zk, rk, &tmK);
+        hk = next_tile(ck);
+        if (hk) tile_box(ck, zk, rk);
+      }
+    }
+    while (vq[0]) {
+      load_tile(zq[0], rq[0], &tmV);
+#pragma unroll
+      for (int u = 0; u + 1 < NS; ++u) {
+        vq[u] = vq[u + 1];
+        zq[u] = zq[u + 1];
+        rq[u] = rq[u + 1];
+      }
+      vq[NS - 1] = hk;
+      if (hk) {
+        zq[NS - 1] = zk;
+        rq[NS - 1] = rk;
+        if (ck.j == 0 && lane == 0) load_q(ck);
+        load_tile(zk, rk, &tmK);
+        hk = next_tile(ck);
+        if (hk) tile_box(ck, zk, rk);
       }
     }
     if (lane == 0) {  // every issued copy must land before the CTA exits
-      for (int u = (t > NKV ? t - NKV : 0); u < t; ++u)
-        mbar_wait(ring_full + (u % NKV), (u / NKV) & 1, a.err, dead);
-      if (isK && nitem > 0) mbar_wait(q_full, (nitem - 1) & 1, a.err, dead);
+      for (int u = (ev > NSLOT ? ev - NSLOT : 0); u < ev; ++u)
+        mbar_wait(slot_full + (u % NSLOT), (u / NSLOT) & 1, a.err, dead);
+      if (ck.m >= 0)
+#pragma unroll
+        for (int x = 0; x < NQ; ++x) mbar_wait(q_full + x, ck.m & 1, a.err, dead);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // =============================== MMA issuer =============================
     if (lane == 0) {
       bool dead = false;
-      int t = 0, nitem = 0;
-      // descriptor low halves of the operand bases (K-major Q, K, P: LBO 16;
+      // descriptor low halves of the operand bases (K-major Q and K: LBO 16;
       // MN-major V: LBO = the 64-column chunk stride); all share one high half
       constexpr uint32_t kHi = tc::sw128_hi(1024);
       const uint32_t q_lo0 = tc::sw128_lo(sQ, 16);
-      const uint32_t k_lo0 = tc::sw128_lo(sK, 16);
-      const uint32_t p_lo0 = tc::sw128_lo(sP, 16);
-      const uint32_t v_lo0 = tc::sw128_lo(sV, S_::kKVChunk);
-      // O_x += P_x V(u) for Q tile x; V(u) must have landed
-      auto pv_x = [&](int u, int x, bool first) {
-        const int vb = u % NKV;
-        mbar_wait(v_full + vb, (u / NKV) & 1, a.err, dead);
-        mbar_wait(p_full + x, u & 1, a.err, dead);
+      const uint32_t k_lo0 = tc::sw128_lo(sSlot, 16);
+      const uint32_t v_lo0 = tc::sw128_lo(sSlot, S_::kKVChunk);
+      int ev = 0;  // load events consumed, in the producer's order
+      // S_x(ta) = Q_x K(ta)^T into S buffer (x, ta % NS); K(ta) is event e
+      auto qk_x = [&](const Cursor& c, int ta, int e, int x) {
+        if (x == 0) mbar_wait(slot_full + (e % NSLOT), (e / NSLOT) & 1, a.err, dead);
+        if (c.j == 0) mbar_wait(q_full + x, c.m & 1, a.err, dead);
         tc::fence_after_sync();
-        const uint32_t alo = p_lo0 + x * (S_::kPBytes >> 4);
-        const uint32_t blo = v_lo0 + vb * (S_::kKVBytes >> 4);
+        const uint32_t qlo = q_lo0 + x * (S_::kQBytes >> 4);
+        const uint32_t klo = k_lo0 + (e % NSLOT) * (S_::kSlotBytes >> 4);
+        const int sb = x * NS + ta % NS;
 #pragma unroll
-        for (int ks = 0; ks < kVBN / 16; ++ks)
-          tc::mma_ss_h(tmem + kOCol + x * D, alo + ks * (32 >> 4), kHi, blo + ks * (2048 >> 4),
-                       kHi, kIdescO, (!first || ks > 0) ? 1u : 0u);
-        tc::commit(o_done + x);
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc::mma_ss_h(tmem + sb * BN, qlo + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), kHi,
+                       klo + (((ks >> 2) * S_::kKVChunk + (ks & 3) * 32) >> 4), kHi, kIdescS,
+                       ks > 0 ? 1u : 0u);
+        tc::commit(s_full + sb);
+        if (c.j == c.it.n - 1) tc::commit(q_empty + x);  // last use of this item's Q_x
       };
-      for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
-        const Item it = item_at(i);
-        if (it.n == 0) continue;
-        mbar_wait(q_full, nitem & 1, a.err, dead);
-        for (int j = 0; j < it.n; ++j, ++t) {
-          const int kb = t % NKV;
-          mbar_wait(k_full + kb, (t / NKV) & 1, a.err, dead);
-          const uint32_t klo = k_lo0 + kb * (S_::kKVBytes >> 4);
-          // per Q tile: S_x of this KV tile, then PV_x of the previous one, so
-          // one warpgroup's softmax never waits on the other's progress
+      Cursor ca = cursor0();  // tile of the next QK (NS ahead of the PV)
+      bool ha = next_tile(ca);
+      int ta = 0;
 #pragma unroll
-          for (int x = 0; x < NQ; ++x) {
-            if (t >= 1) mbar_wait(s_free + x, (t - 1) & 1, a.err, dead);
-            tc::fence_after_sync();
-            const uint32_t qlo = q_lo0 + x * (S_::kQBytes >> 4);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              tc::mma_ss_h(tmem + x * kVBN, qlo + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), kHi,
-                           klo + (((ks >> 2) * S_::kKVChunk + (ks & 3) * 32) >> 4), kHi,
-                           kIdescS, ks > 0 ? 1u : 0u);
-            tc::commit(s_full + x);
-            if (j >= 1) pv_x(t - 1, x, j == 1);
-          }
-          if (j == it.n - 1) tc::commit(q_empty);
-          tc::commit(k_empty + kb);
-          if (j >= 1) tc::commit(v_empty + ((t - 1) % NKV));
+      for (int u = 0; u < NS; ++u) {
+        if (ha) {
+          for (int x = 0; x < NQ; ++x) qk_x(ca, ta, ev, x);
+          tc::commit(slot_empty + (ev % NSLOT));
+          ++ev;
+          ++ta;
+          ha = next_tile(ca);
         }
+      }
+      Cursor cv = cursor0();
+      int t = 0;
+      while (next_tile(cv)) {
+        const int eV = ev++;
+        const int eK = ev;
+        const int sv = eV % NSLOT;
+        for (int x = 0; x < NQ; ++x) {
+          // O_x (+)= P_x(t) V(t): A = P in the TMEM columns of S buffer (x, t % NS)
+          const int sb = x * NS + t % NS;
+          mbar_wait(p_full + sb, (t / NS) & 1, a.err, dead);
+          if (x == 0) mbar_wait(slot_full + sv, (eV / NSLOT) & 1, a.err, dead);
+          tc::fence_after_sync();
+          const uint32_t blo = v_lo0 + sv * (S_::kSlotBytes >> 4);
 #pragma unroll
-        for (int x = 0; x < NQ; ++x) pv_x(t - 1, x, it.n == 1);
-        tc::commit(v_empty + ((t - 1) % NKV));
-        ++nitem;
+          for (int ks = 0; ks < BN / 16; ++ks)
+            tc::mma_ts_h(tmem + kOCol + x * D, tmem + sb * BN + ks * 8, blo + ks * (2048 >> 4),
+                         kHi, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
+          tc::commit(o_done + x);
+          if (ha) qk_x(ca, ta, eK, x);
+        }
+        tc::commit(slot_empty + sv);
+        if (ha) {
+          tc::commit(slot_empty + (eK % NSLOT));
+          ++ev;
+          ++ta;
+          ha = next_tile(ca);
+        }
+        ++t;
       }
       // the stage-release arrivals must land before the CTA (and its smem)
       // goes away
-      for (int u = (t > NKV ? t - NKV : 0); u < t; ++u) {
-        mbar_wait(k_empty + (u % NKV), (u / NKV) & 1, a.err, dead);
-        mbar_wait(v_empty + (u % NKV), (u / NKV) & 1, a.err, dead);
-      }
-      if (nitem > 0) mbar_wait(q_empty, (nitem - 1) & 1, a.err, dead);
+      for (int u = (ev > NSLOT ? ev - NSLOT : 0); u < ev; ++u)
+        mbar_wait(slot_empty + (u % NSLOT), (u / NSLOT) & 1, a.err, dead);
+      if (cv.m >= 0)
+        for (int x = 0; x < NQ; ++x) mbar_wait(q_empty + x, cv.m & 1, a.err, dead);
     }
+  }
   } else {
+    if (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     // ======================== softmax warpgroups ============================
     bool dead = false;
-    const int x = (warp - 2) >> 2;  // which Q tile of the item
+    const int x = warp >> 2;  // which Q tile of the item
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t s_addr = lane_base + x * kVBN;
     const uint32_t o_addr = lane_base + kOCol + x * D;
-    const uint32_t prow = sP + x * S_::kPBytes + r * 128;
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
     int t = 0;
     for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
       const Item it = item_at(i);
@@ -480,35 +606,36 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
       }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.n; ++j, ++t) {
-        mbar_wait(s_full + x, t & 1, a.err, dead);
+        const int sb = x * NS + t % NS;
+        const uint32_t s_addr = lane_base + sb * BN;
+        mbar_wait(s_full + sb, (t / NS) & 1, a.err, dead);
         tc::fence_after_sync();
-        uint32_t s[kVBN];
-        tc::ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tc::ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        uint32_t s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tc::ld_32x32b_x32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
         tc::wait_ld();
-        tc::fence_before_sync();
-        mbar_arrive(s_free + x);
 
         // mask only where a key of this tile falls outside a row's range
-        const int key0 = (it.t_lo + j) * kVBN;
-        const bool inside = key0 >= klo && key0 + kVBN <= khi;
-        float mxp[8];
+        const int key0 = (it.t_lo + j) * BN;
+        const bool inside = key0 >= klo && key0 + BN <= khi;
+        if (!__all_sync(0xffffffffu, inside)) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mxp[c] = -INFINITY;
-        if (__all_sync(0xffffffffu, inside)) {
-#pragma unroll
-          for (int c = 0; c < kVBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], __uint_as_float(s[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < kVBN; ++c) {
+          for (int c = 0; c < BN; ++c) {
             const int k = key0 + c;
-            const float v = (k >= klo && k < khi) ? __uint_as_float(s[c]) : -INFINITY;
-            s[c] = __float_as_uint(v);
-            mxp[c & 7] = fmaxf(mxp[c & 7], v);
+            if (k < klo || k >= khi) s[c] = __float_as_uint(-INFINITY);
           }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        float mxp[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          mxp[c] = fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+#pragma unroll
+        for (int c = 16; c < BN; c += 2)
+          mxp[(c >> 1) & 7] =
+              max3f(mxp[(c >> 1) & 7], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+        const float mx = fmaxf(max3f(mxp[0], mxp[1], mxp[2]),
+                               fmaxf(max3f(mxp[3], mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
         // running max in the log2 domain (scale > 0 commutes with max)
         const float mt = mx * sl2;
         const float m_new = fmaxf(m, mt);
@@ -521,47 +648,66 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
         const float mu = m == -INFINITY ? 0.f : m;
         l *= alpha;
 
-        if (t >= 1) {  // PV of the previous tile must be done with P and O
+        // P = 2^(s*scale_log2 - m) as bf16 pairs over the S columns; a
+        // quarter of the pairs on the FMA pipes
+        const uint64_t negm = f2(-mu, -mu);
+        uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          const uint64_t xx =
+              f2_fma(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, negm);
+          uint64_t pp;
+          if ((c & 7) == 7) {
+            pp = poly_exp2x2(xx);
+          } else {
+            float x0, x1;
+            f2_split(xx, x0, x1);
+            pp = f2(fast_exp2(x0), fast_exp2(x1));
+          }
+          sum2[c & 3] = (c < 4) ? pp : f2_add(sum2[c & 3], pp);
+          float p0, p1;
+          f2_split(pp, p0, p1);
+          s[c] = pack_bf16(p0, p1);  // P pair c over the consumed S column c
+        }
+        float l0, l1;
+        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), l0, l1);
+        l += l0 + l1;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+          tc::st_32x32b_x32(s_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&s[c * 32]));
+        if (NS > 1 && j >= 1) {
+          // With two S buffers nothing else orders PV(t-1) before this
+          // point.  Wait for it on every tile: O may then be rescaled, and
+          // the waits on o_done advance one phase at a time, which a parity
+          // wait needs (at the epilogue a wait two phases ahead of the
+          // barrier would return at once).  With one S buffer, S(t) itself
+          // comes after PV(t-1).
           mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
           tc::fence_after_sync();
         }
-        float sp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int u = 0; u < kVBN / 8; ++u) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // half of the exponentials on the SFU, half on the FMA pipes
-            const float x0 = fmaf(__uint_as_float(s[u * 8 + 2 * e]), sl2, -mu);
-            const float x1 = fmaf(__uint_as_float(s[u * 8 + 2 * e + 1]), sl2, -mu);
-            const float p0 = (u & 1) ? poly_exp2(x0) : fast_exp2(x0);
-            const float p1 = (u & 1) ? poly_exp2(x1) : fast_exp2(x1);
-            sp[e] += p0 + p1;
-            w[e] = pack_bf16(p0, p1);
-          }
-          const uint32_t addr = prow + ((u ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
-        }
-        l += (sp[0] + sp[1]) + (sp[2] + sp[3]);
         if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
+          const uint64_t al2 = f2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tc::ld_32x32b_x32(o_addr + c * 32, o);
             tc::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            for (int e = 0; e < 16; ++e) {
+              float o0, o1;
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), al2),
+                       o0, o1);
+              o[2 * e] = __float_as_uint(o0);
+              o[2 * e + 1] = __float_as_uint(o1);
+            }
             tc::st_32x32b_x32(o_addr + c * 32, o);
           }
-          tc::wait_st();
         }
-        tc::fence_proxy_async_smem();
+        tc::wait_st();
         tc::fence_before_sync();
-        mbar_arrive(p_full + x);
+        mbar_arrive(p_full + sb);
       }
-      // epilogue: O / l -> bf16 rows
+      // epilogue: O / l -> bf16 rows (after the item's last PV)
       mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -588,7 +734,7 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -596,15 +742,16 @@ __global__ void __launch_bounds__((3 + 4 * NQ) * 32, 1)
 }
 
 // --------------------------------------------------------------- host side
-template <int D, int NQ, int NKV>
+template <int D, int NQ, int BN, int NS, int NSLOT>
 static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
                                    cudaStream_t stream, int num_sms) {
-  using S_ = VarlenSmem<D, NQ, NKV>;
-  auto kern = varlen_fwd_kernel<D, NQ, NKV>;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NSLOT>;
+  auto kern = varlen_fwd_kernel<D, NQ, BN, NS, NSLOT>;
   const size_t smem = S_::bytes(a.batch, a.pairs_max);
   if (smem > 227 * 1024) {
-    // the deep K/V ring does not fit next to this batch's schedule: use 2 stages
-    if (NKV > 2) return launch_varlen_t<D, NQ, 2>(a, maps, stream, num_sms);
+    // the deep K/V ring does not fit next to this batch's schedule: fewer slots
+    if (NSLOT > 3) return launch_varlen_t<D, NQ, BN, NS, (NSLOT > 3 ? NSLOT - 1 : 3)>(
+        a, maps, stream, num_sms);
     return cudaErrorNotSupported;
   }
   static int configured[64] = {0};
@@ -613,6 +760,16 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (configured[dev] < (int)smem) {
+    if (NQ == 2) {
+      // the softmax warps raise their registers to 200 with what the other
+      // warpgroup gives back (down to 104): that needs the launch to hold
+      // 168 per thread, else the raise would never be granted
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * varlen_threads<NQ>() < 8 * 32 * 200 + 4 * 32 * 104)
+        return cudaErrorNotSupported;
+    }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = (int)smem;
@@ -623,7 +780,7 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
   if (grid <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((3 + 4 * NQ) * 32);
+  cfg.blockDim = dim3(varlen_threads<NQ>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -633,6 +790,8 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a, maps.q, maps.k, maps.v);
 }
+
+int varlen_kv_tile(int head_dim) { return head_dim == 256 ? 64 : 128; }
 
 cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,
                           const int32_t* cu_k, const int32_t* block_table, int32_t max_blocks,
@@ -657,8 +816,9 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
   if ((1 << a.log2G) != a.G || a.G > 128) return cudaErrorNotSupported;
   if (batch > 1024) return cudaErrorNotSupported;
   const int QP = 128 / a.G;
+  const int BN = varlen_kv_tile(D);
   a.P = P;
-  a.box_rows = P < kVBN ? P : kVBN;
+  a.box_rows = P < BN ? P : BN;
   a.num_pages = num_pages;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
@@ -669,15 +829,15 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
     case 64:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<64, 2, 4>(a, maps, stream, num_sms);
+      return launch_varlen_t<64, 2, 128, 1, 8>(a, maps, stream, num_sms);
     case 128:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<128, 2, 4>(a, maps, stream, num_sms);
+      return launch_varlen_t<128, 2, 128, 1, 4>(a, maps, stream, num_sms);
     case 256:
       a.R = (max_seqlen_q + QP - 1) / QP;
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<256, 1, 2>(a, maps, stream, num_sms);
+      return launch_varlen_t<256, 1, 64, 2, 4>(a, maps, stream, num_sms);
     default:
       return cudaErrorNotSupported;
   }
