@@ -8,7 +8,7 @@
 #include "tmap.h"
 
 using pkv::encode_pool_map;
-using pkv::encode_pool_map_rows;
+using pkv::encode_pool_map_groups;
 using pkv::encode_q_map;
 
 namespace {
@@ -158,10 +158,10 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   // multiple of it
   if (kv_rows % page_size != 0 && page_size % kv_rows != 0) return PKV_ERR_UNSUPPORTED;
   if (!encode_q_map(&maps.q, q, head_dim, G, num_kv_heads, total_q) ||
-      !encode_pool_map_rows(&maps.k, k_cache, head_dim, page_size, num_pages, num_kv_heads,
-                            box_rows) ||
-      !encode_pool_map_rows(&maps.v, v_cache, head_dim, page_size, num_pages, num_kv_heads,
-                            box_rows))
+      !encode_pool_map_groups(&maps.k, k_cache, head_dim, page_size, num_pages, num_kv_heads,
+                              box_rows) ||
+      !encode_pool_map_groups(&maps.v, v_cache, head_dim, page_size, num_pages, num_kv_heads,
+                              box_rows))
     return cuda_fail(cudaErrorInvalidValue);
   cudaError_t e = pkv::launch_varlen(out, maps, cu_seq_lens_q, cu_seq_lens_k, block_table,
                                      max_blocks_per_seq, batch, max_seqlen_q, total_q,

@@ -113,6 +113,92 @@ __device__ __forceinline__ void mma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
+// Warp-converged forms: every lane of the warp executes them with the same
+// operands and one elected lane issues, so the operands can stay in
+// uniform registers.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                         uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+      : "memory");
+}
+
+// Four consecutive K=16 steps of one accumulation, issued from one asm block
+// (one election, the descriptor advances as immediates): the first step
+// accumulates iff `acc`, the others always.
+//   SS: A and B K-major; step k reads A at a_lo + k*A_STEP and B at
+//       b_lo + k*B_STEP (descriptor units of 16 bytes).
+template <uint32_t A_STEP, uint32_t B_STEP>
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b64 da, db;\n\t.reg .b32 al, bl;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t"
+      "add.u32 al, %1, %7;\n\tadd.u32 bl, %3, %8;\n\t"
+      "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, 1;\n\t"
+      "add.u32 al, %1, %9;\n\tadd.u32 bl, %3, %10;\n\t"
+      "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, 1;\n\t"
+      "add.u32 al, %1, %11;\n\tadd.u32 bl, %3, %12;\n\t"
+      "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc), "n"(A_STEP),
+      "n"(B_STEP), "n"(2 * A_STEP), "n"(2 * B_STEP), "n"(3 * A_STEP), "n"(3 * B_STEP)
+      : "memory");
+}
+//   TS: A in TMEM (8 columns per step), B from shared memory at
+//       b_lo + k*B_STEP.
+template <uint32_t B_STEP>
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b64 db;\n\t.reg .b32 at, bl;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t"
+      "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, %6;\n\tmov.b64 db, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, 1;\n\t"
+      "add.u32 at, %1, 16;\n\tadd.u32 bl, %2, %7;\n\tmov.b64 db, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, 1;\n\t"
+      "add.u32 at, %1, 24;\n\tadd.u32 bl, %2, %8;\n\tmov.b64 db, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc), "n"(B_STEP), "n"(2 * B_STEP),
+      "n"(3 * B_STEP)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(

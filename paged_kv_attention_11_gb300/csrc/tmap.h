@@ -45,16 +45,23 @@ inline bool encode_pool_map(CUtensorMap* m, const void* base, int D, int P, int6
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K or V pool for the varlen kernel: same view, box = 64 columns x `rows` rows.
-inline bool encode_pool_map_rows(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
-                          int H_kv, int rows) {
+// K or V pool for the varlen kernel, viewed as {64 columns, 8 rows, D/64
+// column chunks, P/8 row groups, num_pages*H_kv}: one box {64, 8, D/64,
+// rows/8, 1} is `rows` keys of one page and head, and lands in shared memory
+// as [row group][column chunk][8 rows][128 bytes], 128-byte swizzled: every
+// 8-row block of a chunk is one swizzle atom, atoms of one chunk sit
+// (D/64)*1024 bytes apart and chunks 1024 bytes apart, uniformly across the
+// boxes of a tile.
+inline bool encode_pool_map_groups(CUtensorMap* m, const void* base, int D, int P,
+                                   int64_t num_pages, int H_kv, int rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(P / 8),
+                        (cuuint64_t)(num_pages * H_kv)};
+  cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)8 * D * 2, (cuuint64_t)P * D * 2};
+  cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(rows / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

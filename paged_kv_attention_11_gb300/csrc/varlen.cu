@@ -20,10 +20,10 @@
 //    (chunk, item) pairs sorted by their number of KV tiles, most first,
 //    dealt to the CTAs in a snake so that every CTA gets a similar total.
 //  * The CTA's items form one stream of KV tiles; no role drains at an
-//    item boundary.  Warp 0 loads (TMA, 128-byte swizzle, one box per page
-//    slice, lane-parallel issue) in the order the tensor core consumes:
-//    K of the first NS tiles, then V(t), K(t+NS) for every tile t, through
-//    one ring of NSLOT slots; Q tiles when the stream enters an item.
+//    item boundary.  Two producer warps load with TMA (128-byte swizzle, one
+//    box per page slice, lane-parallel issue): one the K tiles (and the Q
+//    tiles when the stream enters an item), one the V tiles, each through
+//    its own ring.
 //  * Warp 1 allocates 512 TMEM columns and issues tcgen05.mma (cta_group::1,
 //    kind::f16, bf16 in, fp32 accumulate):
 //        S_x(t)  = Q_x K(t)^T        smem x smem -> TMEM  (M=128, N=BN)
@@ -68,17 +68,20 @@ struct VarlenArgs {
   int32_t* err;
 };
 
-template <int D, int NQ, int BN, int NS, int NSLOT>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS>
 struct VarlenSmem {
   static constexpr int kQBytes = 128 * D * 2;              // one Q tile
-  static constexpr int kKVChunk = BN * 128;                // one 64-column chunk of a K/V tile
-  static constexpr int kSlotBytes = (D / 64) * kKVChunk;   // one K or V tile
+  // a K/V tile is [row group][64-column chunk][8 rows][128 B]: 8-row atoms
+  // of a chunk kAtomStride apart, chunks 1024 B apart
+  static constexpr int kAtomStride = (D / 64) * 1024;
+  static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
   static constexpr int kQOff = 0;
-  static constexpr int kSlotOff = kQOff + NQ * kQBytes;
-  static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
-  // q_full[NQ] q_empty[NQ] slot_full[NSLOT] slot_empty[NSLOT]
+  static constexpr int kKOff = kQOff + NQ * kQBytes;   // K ring: NKS tiles
+  static constexpr int kVOff = kKOff + NKS * kSlotBytes;  // V ring: NVS tiles
+  static constexpr int kBarOff = kVOff + NVS * kSlotBytes;
+  // q_full[NQ] q_empty[NQ] k_full[NKS] k_empty[NKS] v_full[NVS] v_empty[NVS]
   // s_full[NQ*NS] p_full[NQ*NS] o_done[NQ]
-  static constexpr int kNumBars = 2 * NQ + 2 * NSLOT + 2 * NQ * NS + NQ;
+  static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 2 * NQ * NS + NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
@@ -212,12 +215,12 @@ __host__ __device__ constexpr int varlen_threads() {
   return (4 * NQ + 4) * 32;
 }
 
-template <int D, int NQ, int BN, int NS, int NSLOT>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS>
 __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     varlen_fwd_kernel(const VarlenArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-  using S_ = VarlenSmem<D, NQ, BN, NS, NSLOT>;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS>;
   constexpr int NT = varlen_threads<NQ>();
   constexpr int kProdWarp = 4 * NQ;
   constexpr int kMmaWarp = 4 * NQ + 1;
@@ -234,9 +237,11 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S_::kBarOff);
   uint64_t* q_full = bars;                     // [NQ]
   uint64_t* q_empty = q_full + NQ;             // [NQ]
-  uint64_t* slot_full = q_empty + NQ;          // [NSLOT]
-  uint64_t* slot_empty = slot_full + NSLOT;    // [NSLOT]
-  uint64_t* s_full = slot_empty + NSLOT;       // [NQ*NS]
+  uint64_t* k_full = q_empty + NQ;             // [NKS]
+  uint64_t* k_empty = k_full + NKS;            // [NKS]
+  uint64_t* v_full = k_empty + NKS;            // [NVS]
+  uint64_t* v_empty = v_full + NVS;            // [NVS]
+  uint64_t* s_full = v_empty + NVS;            // [NQ*NS]
   uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS]
   uint64_t* o_done = p_full + NQ * NS;         // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
@@ -258,9 +263,13 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
       mbar_init(q_empty + x, 1);
       mbar_init(o_done + x, 1);
     }
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(slot_full + i, 1);
-      mbar_init(slot_empty + i, 1);
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(v_full + i, 1);
+      mbar_init(v_empty + i, 1);
     }
     for (int i = 0; i < NQ * NS; ++i) {
       mbar_init(s_full + i, 1);
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     c.k = -1;
     c.j = 0;
     c.m = -1;
-    c.it.n = 0;
+    c.it = Item{0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     return c;
   };
 
@@ -385,7 +394,6 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
   const uint32_t sQ = smem_u32(smem + S_::kQOff);
-  const uint32_t sSlot = smem_u32(smem + S_::kSlotOff);
 
   if (blockIdx.x == 0 && tid == 0) {  // report clamped lengths once
     for (int b = 0; b < B; ++b) {
@@ -403,42 +411,39 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   // use the same total, and every SM sub-partition holds at most 504 per lane.
   if (warp >= kProdWarp) {
     if (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
-  if (warp == kProdWarp) {
-    // ============================== TMA producer ==============================
+  if (warp == kProdWarp || warp == kProdWarp + 2) {
+    // ====================== TMA producers: K (+Q) and V ======================
+    // Warp kProdWarp loads the Q tiles and the K tiles, warp kProdWarp+2 the
+    // V tiles, each through its own ring (one issuing warp sustains about
+    // half the box rate of two).
+    const bool isK = warp == kProdWarp;
     bool dead = false;
     const int R = a.box_rows;
-    const int nbox = BN / R;                      // boxes per tile (<= 8)
+    const int nbox = BN / R;                      // boxes (page slices) per tile
     const int oob = (int)(a.num_pages * a.H_kv);  // first z past the pool: zero fill
-    // (z, row) of this lane's box of the cursor's tile; boxes outside the
-    // attended range (or on a bad page) are fetched at z = oob: zeros
-    auto tile_box = [&](const Cursor& c, int& z, int& row) {
-      z = oob;
-      row = 0;
+    // This lane's box of the cursor's tile: its row in the page and the
+    // block-table entry, requested two tiles ahead and checked only when
+    // the box is issued (box_z).  Boxes outside the attended range (or on a
+    // bad page) are fetched at z = oob: zeros.
+    struct Box {
+      int pg, row, g;
+      bool inr;
+    };
+    auto box_req = [&](const Cursor& c) -> Box {
+      Box bx = {0, 0, c.it.g, false};
       if (lane < nbox) {
         const int key0 = (c.it.t_lo + c.j) * BN + lane * R;
-        row = key0 % a.P;
-        if (key0 < c.it.kv_hi && key0 + R > c.it.kv_lo) {
-          const int pg = __ldg(a.block_table + (int64_t)c.it.b * a.max_blocks + key0 / a.P);
-          if (pg >= 0 && (int64_t)pg < a.num_pages) z = pg * a.H_kv + c.it.g;
-          else raise_err(a.err, PKV_DEVERR_PAGE);
-        }
+        bx.row = key0 % a.P;
+        bx.inr = key0 < c.it.kv_hi && key0 + R > c.it.kv_lo;
+        if (bx.inr) bx.pg = __ldg(a.block_table + (int64_t)c.it.b * a.max_blocks + key0 / a.P);
       }
+      return bx;
     };
-    int ev = 0;  // load events issued (K and V tiles, in consumption order)
-    auto load_tile = [&](int z, int row, const CUtensorMap* tm) {
-      const int s = ev % NSLOT;
-      if (lane == 0) {
-        if (ev >= NSLOT) mbar_wait(slot_empty + s, ((ev / NSLOT) - 1) & 1, a.err, dead);
-        mbar_arrive_expect_tx(slot_full + s, S_::kSlotBytes);
-      }
-      __syncwarp();
-      if (lane < nbox) {
-        uint8_t* dst = smem + S_::kSlotOff + s * S_::kSlotBytes + lane * R * 128;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(dst + c * S_::kKVChunk, tm, slot_full + s, c * 64, row, z);
-      }
-      ++ev;
+    auto box_z = [&](const Box& bx) -> int {
+      if (!bx.inr) return oob;
+      if (bx.pg >= 0 && (int64_t)bx.pg < a.num_pages) return bx.pg * a.H_kv + bx.g;
+      raise_err(a.err, PKV_DEVERR_PAGE);
+      return oob;
     };
     auto load_q = [&](const Cursor& c) {  // lane 0: the Q tiles of the cursor's item
 #pragma unroll
@@ -451,75 +456,83 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
                       0, c.it.g, c.it.q0 + c.it.p_begin + x * QP);
       }
     };
-    Cursor ck = cursor0();
-    bool hk = next_tile(ck);
-    int zk = oob, rk = 0;
-    if (hk) tile_box(ck, zk, rk);  // page ids one K tile ahead of its load
-    int zq[NS], rq[NS];            // boxes of the tiles whose V is still to load
-    bool vq[NS];
-#pragma unroll
-    for (int u = 0; u < NS; ++u) {
-      vq[u] = hk;
-      zq[u] = zk;
-      rq[u] = rk;
-      if (hk) {
-        if (ck.j == 0 && lane == 0) load_q(ck);
-        load_tile(zk, rk, &tmK);
-        hk = next_tile(ck);
-        if (hk) tile_box(ck, zk, rk);
+    const int nring = isK ? NKS : NVS;
+    uint64_t* rfull = isK ? k_full : v_full;
+    uint64_t* rempty = isK ? k_empty : v_empty;
+    uint8_t* rbase = smem + (isK ? S_::kKOff : S_::kVOff);
+    const CUtensorMap* tm = isK ? &tmK : &tmV;
+    const Box none = {0, 0, 0, false};
+    Cursor c0 = cursor0();  // tile being loaded
+    bool h0 = next_tile(c0);
+    Cursor c1 = c0;  // the next one
+    bool h1 = h0 && next_tile(c1);
+    Box b0 = h0 ? box_req(c0) : none;
+    Box b1 = h1 ? box_req(c1) : none;
+    int t = 0, s = 0, ph = 0;  // tiles loaded; ring slot and its phase
+    while (h0) {
+      if (isK && c0.j == 0 && lane == 0) load_q(c0);
+      if (lane == 0) {
+        if (t >= nring) mbar_wait(rempty + s, ph ^ 1, a.err, dead);
+        mbar_arrive_expect_tx(rfull + s, S_::kSlotBytes);
       }
-    }
-    while (vq[0]) {
-      load_tile(zq[0], rq[0], &tmV);
-#pragma unroll
-      for (int u = 0; u + 1 < NS; ++u) {
-        vq[u] = vq[u + 1];
-        zq[u] = zq[u + 1];
-        rq[u] = rq[u + 1];
+      __syncwarp();
+      const int z = box_z(b0);
+      if (lane < nbox)  // one box: this lane's page slice of the tile, all columns
+        tma_load_5d(rbase + s * S_::kSlotBytes + lane * R * D * 2, tm, rfull + s, 0, 0, 0,
+                    b0.row / 8, z);
+      ++t;
+      if (++s == nring) {
+        s = 0;
+        ph ^= 1;
       }
-      vq[NS - 1] = hk;
-      if (hk) {
-        zq[NS - 1] = zk;
-        rq[NS - 1] = rk;
-        if (ck.j == 0 && lane == 0) load_q(ck);
-        load_tile(zk, rk, &tmK);
-        hk = next_tile(ck);
-        if (hk) tile_box(ck, zk, rk);
+      c0 = c1;
+      h0 = h1;
+      b0 = b1;
+      if (h1) {
+        h1 = next_tile(c1);
+        if (h1) b1 = box_req(c1);
       }
     }
     if (lane == 0) {  // every issued copy must land before the CTA exits
-      for (int u = (ev > NSLOT ? ev - NSLOT : 0); u < ev; ++u)
-        mbar_wait(slot_full + (u % NSLOT), (u / NSLOT) & 1, a.err, dead);
-      if (ck.m >= 0)
+      for (int u = (t > nring ? t - nring : 0); u < t; ++u)
+        mbar_wait(rfull + (u % nring), (u / nring) & 1, a.err, dead);
+      if (isK && c0.m >= 0)
 #pragma unroll
-        for (int x = 0; x < NQ; ++x) mbar_wait(q_full + x, ck.m & 1, a.err, dead);
+        for (int x = 0; x < NQ; ++x) mbar_wait(q_full + x, c0.m & 1, a.err, dead);
     }
   } else if (warp == kMmaWarp) {
     // =============================== MMA issuer =============================
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues each tcgen05 op
       bool dead = false;
-      // descriptor low halves of the operand bases (K-major Q and K: LBO 16;
-      // MN-major V: LBO = the 64-column chunk stride); all share one high half
+      // descriptor halves of the operand bases: K-major Q (atoms 1024 B
+      // apart) and K (atoms kAtomStride apart), LBO 16 (unused); MN-major V:
+      // LBO = the 1024 B chunk stride, atoms along the keys kAtomStride apart
       constexpr uint32_t kHi = tc::sw128_hi(1024);
+      constexpr uint32_t kHiKV = tc::sw128_hi(S_::kAtomStride);
       const uint32_t q_lo0 = tc::sw128_lo(sQ, 16);
-      const uint32_t k_lo0 = tc::sw128_lo(sSlot, 16);
-      const uint32_t v_lo0 = tc::sw128_lo(sSlot, S_::kKVChunk);
-      int ev = 0;  // load events consumed, in the producer's order
-      // S_x(ta) = Q_x K(ta)^T into S buffer (x, ta % NS); K(ta) is event e
-      auto qk_x = [&](const Cursor& c, int ta, int e, int x) {
-        if (x == 0) mbar_wait(slot_full + (e % NSLOT), (e / NSLOT) & 1, a.err, dead);
-        if (c.j == 0) mbar_wait(q_full + x, c.m & 1, a.err, dead);
+      const uint32_t k_lo0 = tc::sw128_lo(smem_u32(smem + S_::kKOff), 16);
+      const uint32_t v_lo0 = tc::sw128_lo(smem_u32(smem + S_::kVOff), 1024);
+      // Every wait is followed by __syncwarp() (mbar_wait_converged): the
+      // lanes leave a spin at different times, and the issue below runs
+      // several times faster from a converged warp.
+      // S_x(ta) = Q_x K(ta)^T into S buffer (x, ta % NS)
+      auto qk_x = [&](const Cursor& c, int ta, int x) {
+        const int sk = ta % NKS;
+        if (x == 0) mbar_wait_converged(k_full + sk, (ta / NKS) & 1, a.err, dead);
+        if (c.j == 0) mbar_wait_converged(q_full + x, c.m & 1, a.err, dead);
         tc::fence_after_sync();
         const uint32_t qlo = q_lo0 + x * (S_::kQBytes >> 4);
-        const uint32_t klo = k_lo0 + (e % NSLOT) * (S_::kSlotBytes >> 4);
+        const uint32_t klo = k_lo0 + sk * (S_::kSlotBytes >> 4);
         const int sb = x * NS + ta % NS;
+        // K=16 steps: 32 B apart inside a 64-column chunk; chunks 16 KB
+        // apart in Q and 1 KB apart in K
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc::mma_ss_h(tmem + sb * BN, qlo + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), kHi,
-                       klo + (((ks >> 2) * S_::kKVChunk + (ks & 3) * 32) >> 4), kHi, kIdescS,
-                       ks > 0 ? 1u : 0u);
-        tc::commit(s_full + sb);
-        if (c.j == c.it.n - 1) tc::commit(q_empty + x);  // last use of this item's Q_x
+        for (int ch = 0; ch < D / 64; ++ch)
+          tc::mma_ss_x4<2, 2>(tmem + sb * BN, qlo + ch * (16384 >> 4), kHi, klo + ch * (1024 >> 4),
+                              kHiKV, kIdescS, ch > 0 ? 1u : 0u);
+        tc::commit_w(s_full + sb);
+        if (c.j == c.it.n - 1) tc::commit_w(q_empty + x);  // last use of this item's Q_x
+        if (x == NQ - 1) tc::commit_w(k_empty + sk);       // last use of K(ta)
       };
       Cursor ca = cursor0();  // tile of the next QK (NS ahead of the PV)
       bool ha = next_tile(ca);
@@ -527,9 +540,7 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
 #pragma unroll
       for (int u = 0; u < NS; ++u) {
         if (ha) {
-          for (int x = 0; x < NQ; ++x) qk_x(ca, ta, ev, x);
-          tc::commit(slot_empty + (ev % NSLOT));
-          ++ev;
+          for (int x = 0; x < NQ; ++x) qk_x(ca, ta, x);
           ++ta;
           ha = next_tile(ca);
         }
@@ -537,27 +548,26 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
       Cursor cv = cursor0();
       int t = 0;
       while (next_tile(cv)) {
-        const int eV = ev++;
-        const int eK = ev;
-        const int sv = eV % NSLOT;
+        const int sv = t % NVS;
         for (int x = 0; x < NQ; ++x) {
           // O_x (+)= P_x(t) V(t): A = P in the TMEM columns of S buffer (x, t % NS)
           const int sb = x * NS + t % NS;
-          mbar_wait(p_full + sb, (t / NS) & 1, a.err, dead);
-          if (x == 0) mbar_wait(slot_full + sv, (eV / NSLOT) & 1, a.err, dead);
+          mbar_wait_converged(p_full + sb, (t / NS) & 1, a.err, dead);
+          if (x == 0) mbar_wait_converged(v_full + sv, (t / NVS) & 1, a.err, dead);
           tc::fence_after_sync();
           const uint32_t blo = v_lo0 + sv * (S_::kSlotBytes >> 4);
+          // K=16 steps: 8 P columns and two 8-key atoms of V apart
+          constexpr uint32_t kVStep = (2 * S_::kAtomStride) >> 4;
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
-            tc::mma_ts_h(tmem + kOCol + x * D, tmem + sb * BN + ks * 8, blo + ks * (2048 >> 4),
-                         kHi, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
-          tc::commit(o_done + x);
-          if (ha) qk_x(ca, ta, eK, x);
+          for (int g = 0; g < BN / 64; ++g)
+            tc::mma_ts_x4<kVStep>(tmem + kOCol + x * D, tmem + sb * BN + g * 32,
+                                  blo + g * 4 * kVStep, kHiKV, kIdescO,
+                                  (cv.j > 0 || g > 0) ? 1u : 0u);
+          tc::commit_w(o_done + x);
+          if (x == NQ - 1) tc::commit_w(v_empty + sv);  // last use of V(t)
+          if (ha) qk_x(ca, ta, x);
         }
-        tc::commit(slot_empty + sv);
         if (ha) {
-          tc::commit(slot_empty + (eK % NSLOT));
-          ++ev;
           ++ta;
           ha = next_tile(ca);
         }
@@ -565,8 +575,10 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
       }
       // the stage-release arrivals must land before the CTA (and its smem)
       // goes away
-      for (int u = (ev > NSLOT ? ev - NSLOT : 0); u < ev; ++u)
-        mbar_wait(slot_empty + (u % NSLOT), (u / NSLOT) & 1, a.err, dead);
+      for (int u = (ta > NKS ? ta - NKS : 0); u < ta; ++u)
+        mbar_wait(k_empty + (u % NKS), (u / NKS) & 1, a.err, dead);
+      for (int u = (t > NVS ? t - NVS : 0); u < t; ++u)
+        mbar_wait(v_empty + (u % NVS), (u / NVS) & 1, a.err, dead);
       if (cv.m >= 0)
         for (int x = 0; x < NQ; ++x) mbar_wait(q_empty + x, cv.m & 1, a.err, dead);
     }
@@ -742,16 +754,20 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
 }
 
 // --------------------------------------------------------------- host side
-template <int D, int NQ, int BN, int NS, int NSLOT>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS>
 static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
                                    cudaStream_t stream, int num_sms) {
-  using S_ = VarlenSmem<D, NQ, BN, NS, NSLOT>;
-  auto kern = varlen_fwd_kernel<D, NQ, BN, NS, NSLOT>;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS>;
+  auto kern = varlen_fwd_kernel<D, NQ, BN, NS, NKS, NVS>;
   const size_t smem = S_::bytes(a.batch, a.pairs_max);
   if (smem > 227 * 1024) {
-    // the deep K/V ring does not fit next to this batch's schedule: fewer slots
-    if (NSLOT > 3) return launch_varlen_t<D, NQ, BN, NS, (NSLOT > 3 ? NSLOT - 1 : 3)>(
-        a, maps, stream, num_sms);
+    // the deep rings do not fit next to this batch's schedule: fewer slots
+    if (NKS > 2)
+      return launch_varlen_t<D, NQ, BN, NS, (NKS > 2 ? NKS - 1 : 2), NVS>(a, maps, stream,
+                                                                          num_sms);
+    if (NVS > 2)
+      return launch_varlen_t<D, NQ, BN, NS, NKS, (NVS > 2 ? NVS - 1 : 2)>(a, maps, stream,
+                                                                          num_sms);
     return cudaErrorNotSupported;
   }
   static int configured[64] = {0};
@@ -829,15 +845,15 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
     case 64:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<64, 2, 128, 1, 8>(a, maps, stream, num_sms);
+      return launch_varlen_t<64, 2, 128, 1, 4, 4>(a, maps, stream, num_sms);
     case 128:
       a.R = (max_seqlen_q + 2 * QP - 1) / (2 * QP);
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<128, 2, 128, 1, 4>(a, maps, stream, num_sms);
+      return launch_varlen_t<128, 2, 128, 1, 3, 2>(a, maps, stream, num_sms);
     case 256:
       a.R = (max_seqlen_q + QP - 1) / QP;
       a.pairs_max = batch * a.R;
-      return launch_varlen_t<256, 1, 64, 2, 4>(a, maps, stream, num_sms);
+      return launch_varlen_t<256, 1, 64, 2, 2, 2>(a, maps, stream, num_sms);
     default:
       return cudaErrorNotSupported;
   }
