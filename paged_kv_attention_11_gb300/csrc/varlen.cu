@@ -80,8 +80,8 @@ struct VarlenSmem {
   static constexpr int kVOff = kKOff + NKS * kSlotBytes;  // V ring: NVS tiles
   static constexpr int kBarOff = kVOff + NVS * kSlotBytes;
   // q_full[NQ] q_empty[NQ] k_full[NKS] k_empty[NKS] v_full[NVS] v_empty[NVS]
-  // s_full[NQ*NS] p_full[NQ*NS] o_done[NQ]
-  static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 2 * NQ * NS + NQ;
+  // s_full[NQ*NS] p_full[NQ*NS][2] o_done[NQ]
+  static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 3 * NQ * NS + NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   uint64_t* v_full = k_empty + NKS;            // [NVS]
   uint64_t* v_empty = v_full + NVS;            // [NVS]
   uint64_t* s_full = v_empty + NVS;            // [NQ*NS]
-  uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS]
-  uint64_t* o_done = p_full + NQ * NS;         // [NQ]
+  uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS][2]: the two halves of P
+  uint64_t* o_done = p_full + 2 * NQ * NS;     // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
   int* s_qlen = reinterpret_cast<int*>(smem + S_::kSchedOff);  // clamped q_len per chunk
   int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     }
     for (int i = 0; i < NQ * NS; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(p_full + 2 * i, 128);
+      mbar_init(p_full + 2 * i + 1, 128);
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -552,17 +553,28 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
         for (int x = 0; x < NQ; ++x) {
           // O_x (+)= P_x(t) V(t): A = P in the TMEM columns of S buffer (x, t % NS)
           const int sb = x * NS + t % NS;
-          mbar_wait_converged(p_full + sb, (t / NS) & 1, a.err, dead);
           if (x == 0) mbar_wait_converged(v_full + sv, (t / NVS) & 1, a.err, dead);
-          tc::fence_after_sync();
           const uint32_t blo = v_lo0 + sv * (S_::kSlotBytes >> 4);
-          // K=16 steps: 8 P columns and two 8-key atoms of V apart
+          // K=16 steps: 8 P columns and two 8-key atoms of V apart.  P comes
+          // in two halves of the keys, each with its own barrier (a shared
+          // one could complete both phases before this wait and leave a
+          // parity wait ambiguous).
           constexpr uint32_t kVStep = (2 * S_::kAtomStride) >> 4;
 #pragma unroll
-          for (int g = 0; g < BN / 64; ++g)
-            tc::mma_ts_x4<kVStep>(tmem + kOCol + x * D, tmem + sb * BN + g * 32,
-                                  blo + g * 4 * kVStep, kHiKV, kIdescO,
-                                  (cv.j > 0 || g > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+            mbar_wait_converged(p_full + 2 * sb + h, (t / NS) & 1, a.err, dead);
+            tc::fence_after_sync();
+            if (BN == 128) {
+              tc::mma_ts_x4<kVStep>(tmem + kOCol + x * D, tmem + sb * BN + h * 32,
+                                    blo + h * 4 * kVStep, kHiKV, kIdescO,
+                                    (cv.j > 0 || h > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int ks = h * (BN / 32); ks < (h + 1) * (BN / 32); ++ks)
+                tc::mma_ts_w(tmem + kOCol + x * D, tmem + sb * BN + ks * 8, blo + ks * kVStep,
+                             kHiKV, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
           tc::commit_w(o_done + x);
           if (x == NQ - 1) tc::commit_w(v_empty + sv);  // last use of V(t)
           if (ha) qk_x(ca, ta, x);
@@ -660,33 +672,6 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
         const float mu = m == -INFINITY ? 0.f : m;
         l *= alpha;
 
-        // P = 2^(s*scale_log2 - m) as bf16 pairs over the S columns; a
-        // quarter of the pairs on the FMA pipes
-        const uint64_t negm = f2(-mu, -mu);
-        uint64_t sum2[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          const uint64_t xx =
-              f2_fma(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, negm);
-          uint64_t pp;
-          if ((c & 7) == 7) {
-            pp = poly_exp2x2(xx);
-          } else {
-            float x0, x1;
-            f2_split(xx, x0, x1);
-            pp = f2(fast_exp2(x0), fast_exp2(x1));
-          }
-          sum2[c & 3] = (c < 4) ? pp : f2_add(sum2[c & 3], pp);
-          float p0, p1;
-          f2_split(pp, p0, p1);
-          s[c] = pack_bf16(p0, p1);  // P pair c over the consumed S column c
-        }
-        float l0, l1;
-        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), l0, l1);
-        l += l0 + l1;
-#pragma unroll
-        for (int c = 0; c < BN / 64; ++c)
-          tc::st_32x32b_x32(s_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&s[c * 32]));
         if (NS > 1 && j >= 1) {
           // With two S buffers nothing else orders PV(t-1) before this
           // point.  Wait for it on every tile: O may then be rescaled, and
@@ -697,27 +682,65 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
           mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
           tc::fence_after_sync();
         }
-        if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
-          const uint64_t al2 = f2(alpha, alpha);
+        // P = 2^(s*scale_log2 - m) as bf16 pairs over the S columns, in two
+        // halves of the keys, each released to the PV MMA as soon as it is
+        // written (the first half's PV runs under the second half's
+        // exponentials); an eighth of the pairs on the FMA pipes
+        const uint64_t negm = f2(-mu, -mu);
+        uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tc::ld_32x32b_x32(o_addr + c * 32, o);
-            tc::wait_ld();
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float o0, o1;
-              f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), al2),
-                       o0, o1);
-              o[2 * e] = __float_as_uint(o0);
-              o[2 * e + 1] = __float_as_uint(o1);
+          for (int c = h * (BN / 4); c < (h + 1) * (BN / 4); ++c) {
+            const uint64_t xx =
+                f2_fma(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, negm);
+            uint64_t pp;
+            if ((c & 7) == 7) {
+              pp = poly_exp2x2(xx);
+            } else {
+              float x0, x1;
+              f2_split(xx, x0, x1);
+              pp = f2(fast_exp2(x0), fast_exp2(x1));
             }
-            tc::st_32x32b_x32(o_addr + c * 32, o);
+            sum2[c & 3] = (c < 4) ? pp : f2_add(sum2[c & 3], pp);
+            float p0, p1;
+            f2_split(pp, p0, p1);
+            s[c] = pack_bf16(p0, p1);  // P pair c over the consumed S column c
           }
+          if (BN == 128)
+            tc::st_32x32b_x32(s_addr + h * 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(&s[h * 32]));
+          else
+            tc::st_32x32b_x16(s_addr + h * 16, &s[h * 16]);
+          if (h == 0) {
+            // O must be rescaled before the first half's PV; done here, once
+            // the first half of the S row is dead, to keep registers free
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
+              const uint64_t al2 = f2(alpha, alpha);
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tc::ld_32x32b_x32(o_addr + c * 32, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  float o0, o1;
+                  f2_split(f2_mul(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), al2),
+                           o0, o1);
+                  o[2 * e] = __float_as_uint(o0);
+                  o[2 * e + 1] = __float_as_uint(o1);
+                }
+                tc::st_32x32b_x32(o_addr + c * 32, o);
+              }
+            }
+          }
+          tc::wait_st();
+          tc::fence_before_sync();
+          mbar_arrive(p_full + 2 * sb + h);
         }
-        tc::wait_st();
-        tc::fence_before_sync();
-        mbar_arrive(p_full + sb);
+        float l0, l1;
+        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), l0, l1);
+        l += l0 + l1;
       }
       // epilogue: O / l -> bf16 rows (after the item's last PV)
       mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
