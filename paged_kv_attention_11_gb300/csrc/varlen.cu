@@ -471,7 +471,6 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     Box b1 = h1 ? box_req(c1) : none;
     int t = 0, s = 0, ph = 0;  // tiles loaded; ring slot and its phase
     while (h0) {
-      if (isK && c0.j == 0 && lane == 0) load_q(c0);
       if (lane == 0) {
         if (t >= nring) mbar_wait(rempty + s, ph ^ 1, a.err, dead);
         mbar_arrive_expect_tx(rfull + s, S_::kSlotBytes);
@@ -481,6 +480,21 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
       if (lane < nbox)  // one box: this lane's page slice of the tile, all columns
         tma_load_5d(rbase + s * S_::kSlotBytes + lane * R * D * 2, tm, rfull + s, 0, 0, 0,
                     b0.row / 8, z);
+      if (isK && c0.j == 0 && lane == 0) {
+        // a new item: its Q tiles (after the K tile, which does not wait for
+        // the previous item's last QK), and an L2 prefetch of the Q tiles of
+        // the item after it
+        load_q(c0);
+        const int inext = my_item(c0.k + 1);
+        if (inext < T) {
+          const Item nx = item_at(inext);
+#pragma unroll
+          for (int x = 0; x < NQ; ++x)
+#pragma unroll
+            for (int ch = 0; ch < D / 64; ++ch)
+              tma_prefetch_l2_4d(&tmQ, ch * 64, 0, nx.g, nx.q0 + nx.p_begin + x * QP);
+        }
+      }
       ++t;
       if (++s == nring) {
         s = 0;
