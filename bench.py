@@ -208,17 +208,46 @@ class DeviceStep:
 def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True):
     """Run warmup + steps; returns per-step per-phase device ms (events).
 
-    With ``graphs`` every phase is captured once into a CUDA graph (the API
-    calls are capture-safe: no allocation, no host sync) and replayed, so
-    host-side argument marshalling never shows up inside the device-time
-    events.  Every timed step starts after an L2 flush on the same stream.
+    With ``graphs`` the whole step is captured once into one CUDA graph (the
+    API calls are capture-safe: no allocation, no host sync), with timing
+    events recorded as graph nodes before, between and after the phases, and
+    replayed once per timed step.  The events then time the device work of
+    the step and of each phase, not the host's graph launch (about 6 us per
+    launch on the GB300, measured).  Without external-event capture support
+    in torch, each phase gets its own graph and the events sit around the
+    replays.  Every timed step starts after an L2 flush on the same stream.
     """
     import torch
     for _ in range(warmup):
         for f in fn_phases:
             f(stream)
     torch.cuda.synchronize()
+    n = len(fn_phases)
     if graphs:
+        try:
+            gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
+        except TypeError:
+            gev = None
+        if gev is not None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                gev[0].record(stream)
+                for i, f in enumerate(fn_phases):
+                    f(stream)
+                    gev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    g.replay()
+            torch.cuda.synchronize()
+            out = []
+            for _ in range(steps):
+                flush()
+                with torch.cuda.stream(stream):
+                    g.replay()
+                torch.cuda.synchronize()
+                out.append([gev[i].elapsed_time(gev[i + 1]) for i in range(n)])
+            return out
         gs = []
         for f in fn_phases:
             g = torch.cuda.CUDAGraph()
@@ -236,7 +265,7 @@ def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True):
                     f(stream)
         torch.cuda.synchronize()
     recs = []
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fn_phases) + 1)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
               for _ in range(steps)]
     with torch.cuda.stream(stream):
         for k in range(steps):
@@ -248,7 +277,7 @@ def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True):
                 evs[i + 1].record(stream)
             recs.append(evs)
     torch.cuda.synchronize()
-    return [[recs[k][i].elapsed_time(recs[k][i + 1]) for i in range(len(fn_phases))]
+    return [[recs[k][i].elapsed_time(recs[k][i + 1]) for i in range(n)]
             for k in range(steps)]
 
 
