@@ -88,7 +88,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   }
 }
 
-// mbar_wait by every lane of a warp, which leaves it converged again.
+// mbar_wait by every lane of a warp, which leaves it converged again (the
+// tcgen05 issue that follows is several times slower from a diverged warp).
 __device__ __forceinline__ bool mbar_wait_converged(uint64_t* bar, uint32_t parity,
                                                     int32_t* err, bool& dead) {
   const bool ok = mbar_wait(bar, parity, err, dead);

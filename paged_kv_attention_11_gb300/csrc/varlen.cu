@@ -80,8 +80,8 @@ struct VarlenSmem {
   static constexpr int kVOff = kKOff + NKS * kSlotBytes;  // V ring: NVS tiles
   static constexpr int kBarOff = kVOff + NVS * kSlotBytes;
   // q_full[NQ] q_empty[NQ] k_full[NKS] k_empty[NKS] v_full[NVS] v_empty[NVS]
-  // s_full[NQ*NS] p_full[NQ*NS][2] o_done[NQ]
-  static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 3 * NQ * NS + NQ;
+  // s_full[NQ*NS] p_full[NQ*NS] o_done[NQ]
+  static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 2 * NQ * NS + NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   uint64_t* v_full = k_empty + NKS;            // [NVS]
   uint64_t* v_empty = v_full + NVS;            // [NVS]
   uint64_t* s_full = v_empty + NVS;            // [NQ*NS]
-  uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS][2]: the two halves of P
-  uint64_t* o_done = p_full + 2 * NQ * NS;     // [NQ]
+  uint64_t* p_full = s_full + NQ * NS;         // [NQ*NS]
+  uint64_t* o_done = p_full + NQ * NS;         // [NQ]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S_::kTmemOff);
   int* s_qlen = reinterpret_cast<int*>(smem + S_::kSchedOff);  // clamped q_len per chunk
   int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
@@ -273,8 +273,7 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     }
     for (int i = 0; i < NQ * NS; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + 2 * i, 128);
-      mbar_init(p_full + 2 * i + 1, 128);
+      mbar_init(p_full + i, 1);  // one arrive per warpgroup, after a named barrier
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -569,15 +568,12 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
           const int sb = x * NS + t % NS;
           if (x == 0) mbar_wait_converged(v_full + sv, (t / NVS) & 1, a.err, dead);
           const uint32_t blo = v_lo0 + sv * (S_::kSlotBytes >> 4);
-          // K=16 steps: 8 P columns and two 8-key atoms of V apart.  P comes
-          // in two halves of the keys, each with its own barrier (a shared
-          // one could complete both phases before this wait and leave a
-          // parity wait ambiguous).
+          // K=16 steps: 8 P columns and two 8-key atoms of V apart
           constexpr uint32_t kVStep = (2 * S_::kAtomStride) >> 4;
+          mbar_wait_converged(p_full + sb, (t / NS) & 1, a.err, dead);
+          tc::fence_after_sync();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            mbar_wait_converged(p_full + 2 * sb + h, (t / NS) & 1, a.err, dead);
-            tc::fence_after_sync();
             if (BN == 128) {
               tc::mma_ts_x4<kVStep>(tmem + kOCol + x * D, tmem + sb * BN + h * 32,
                                     blo + h * 4 * kVStep, kHiKV, kIdescO,
@@ -589,7 +585,9 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
                              kHiKV, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          tc::commit_w(o_done + x);
+          // O_x is read back only at the item's end (and, with two S
+          // buffers, before a rescale): commit o_done only then
+          if (NS > 1 || cv.j == cv.it.n - 1) tc::commit_w(o_done + x);
           if (x == NQ - 1) tc::commit_w(v_empty + sv);  // last use of V(t)
           if (ha) qk_x(ca, ta, x);
         }
@@ -621,6 +619,7 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
     int t = 0;
+    int mi = 0;  // items with keys done by this warpgroup
     for (int kk_ = 0, i = my_item(0); i < T; ++kk_, i = my_item(kk_)) {
       const Item it = item_at(i);
       const int p = it.p_begin + x * QP + (r >> a.log2G);  // chunk row of this thread
@@ -696,10 +695,8 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
           mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
           tc::fence_after_sync();
         }
-        // P = 2^(s*scale_log2 - m) as bf16 pairs over the S columns, in two
-        // halves of the keys, each released to the PV MMA as soon as it is
-        // written (the first half's PV runs under the second half's
-        // exponentials); an eighth of the pairs on the FMA pipes
+        // P = 2^(s*scale_log2 - m) as bf16 pairs over the S columns, stored
+        // in two halves of the keys; an eighth of the pairs on the FMA pipes
         const uint64_t negm = f2(-mu, -mu);
         uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -748,16 +745,20 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
               }
             }
           }
-          tc::wait_st();
-          tc::fence_before_sync();
-          mbar_arrive(p_full + 2 * sb + h);
         }
+        tc::wait_st();
+        tc::fence_before_sync();
+        // the whole warpgroup's P (and O) stores are done: one arrive
+        named_bar_sync(1 + x, 128);
+        if (r == 0) mbar_arrive(p_full + sb);
         float l0, l1;
         f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), l0, l1);
         l += l0 + l1;
       }
-      // epilogue: O / l -> bf16 rows (after the item's last PV)
-      mbar_wait(o_done + x, (t - 1) & 1, a.err, dead);
+      // epilogue: O / l -> bf16 rows (after the item's last PV).  o_done
+      // completes once per tile with two S buffers, once per item with one.
+      mbar_wait(o_done + x, (NS > 1 ? (t - 1) : mi) & 1, a.err, dead);
+      ++mi;
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(orow);
