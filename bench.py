@@ -205,17 +205,21 @@ class DeviceStep:
                                    stream=stream)
 
 
-def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True):
+def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True, phase_events=True):
     """Run warmup + steps; returns per-step per-phase device ms (events).
 
     With ``graphs`` the whole step is captured once into one CUDA graph (the
     API calls are capture-safe: no allocation, no host sync), with timing
-    events recorded as graph nodes before, between and after the phases, and
-    replayed once per timed step.  The events then time the device work of
-    the step and of each phase, not the host's graph launch (about 6 us per
-    launch on the GB300, measured).  Without external-event capture support
-    in torch, each phase gets its own graph and the events sit around the
-    replays.  Every timed step starts after an L2 flush on the same stream.
+    events recorded as graph nodes, and replayed once per timed step, so the
+    events time device work, not the host's graph launch.  With
+    ``phase_events`` there is an event between consecutive phases (per-phase
+    times; an event node between two kernels also stops the next kernel's
+    prologue from overlapping the previous one through programmatic
+    dependent launch); without, only around the step, and the single
+    returned "phase" is the whole step as an engine would run it.  Without
+    external-event capture support in torch, each phase gets its own graph
+    and the events sit around the replays.  Every timed step starts after an
+    L2 flush on the same stream.
     """
     import torch
     for _ in range(warmup):
@@ -234,7 +238,10 @@ def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True):
                 gev[0].record(stream)
                 for i, f in enumerate(fn_phases):
                     f(stream)
-                    gev[i + 1].record(stream)
+                    if phase_events or i == n - 1:
+                        gev[i + 1 if phase_events else 1].record(stream)
+            if not phase_events:
+                n = 1
             torch.cuda.synchronize()
             with torch.cuda.stream(stream):
                 for _ in range(warmup):
@@ -327,11 +334,16 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(bus) as clocks:
-        per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush)
+        per_step = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush,
+                              phase_events=False)
     torch.cuda.synchronize()
     barrier()
+    # per-kernel breakdown for the roofline: the same steps with an event
+    # between the two kernels
+    per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush)
+    torch.cuda.synchronize()
     assert int(ds.err.item()) == 0, f"device error flag {int(ds.err.item())}"
-    step_ms = float(np.mean([sum(p) for p in per]))
+    step_ms = float(np.mean([sum(p) for p in per_step]))
     dec_ms = float(np.mean([p[1] for p in per]))
     app_ms = float(np.mean([p[0] for p in per]))
     if ws > 1:
@@ -364,6 +376,7 @@ def run_ours(args):
         "decode_only": {"gb_s": round(dec_gbs, 2), "us": round(dec_ms * 1e3, 2),
                         "pct_of_8TBs": round(100 * dec_gbs / NOMINAL_HBM_GBS, 2)},
         "append_us": round(app_ms * 1e3, 2),
+        "step_us_with_event_between_kernels": round((app_ms + dec_ms) * 1e3, 2),
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (split-KV with fused last-arriver merge)",
                      "achieved": round(dec_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm_peak, 4), "peak_source": peak_src,
@@ -420,6 +433,8 @@ def run_mixed(args, device, stream, flush, rank):
     try:
         step = wl.mixed_step()
         ds = DeviceStep(step, wl.BASE_SEED + 3 + 1000 * rank, device)
+        per_step = time_steps([ds.append, ds.varlen, ds.decode], args.steps, args.warmup,
+                              stream, flush, phase_events=False)
         per = time_steps([ds.append, ds.varlen, ds.decode], args.steps, args.warmup, stream,
                          flush)
         torch.cuda.synchronize()
@@ -427,7 +442,7 @@ def run_mixed(args, device, stream, flush, rank):
             return {"unavailable": f"device error flag {int(ds.err.item())}"}
     except Exception as e:  # varlen not available yet, etc.
         return {"unavailable": f"{type(e).__name__}: {e}"}
-    ms = float(np.mean([sum(p) for p in per]))
+    ms = float(np.mean([sum(p) for p in per_step]))
     ph = np.mean(np.array(per), axis=0)
     tokens = step.n_new_tokens
     fl = varlen_flops(step)
