@@ -40,7 +40,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_split_kernel launch on
 # the qwen3_decode workload (ncu --set full capture on a GB300, 316.77 + 4.15 MB);
 # valid for that workload and this decode kernel only.
-DECODE_TRAFFIC_BYTES = 320_922_624
+DECODE_TRAFFIC_BYTES = 0  # not yet captured for the current decode kernel
 
 
 # ------------------------------------------------------------------ helpers
@@ -380,7 +380,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (split-KV with fused last-arriver merge)",
                      "achieved": round(dec_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm_peak, 4), "peak_source": peak_src,
-                     "algorithmic_bytes": dbytes, "traffic": DECODE_TRAFFIC_BYTES},
+                     "algorithmic_bytes": dbytes, "traffic": DECODE_TRAFFIC_BYTES or None},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,  # append + decode (split-KV with fused merge) per step
         "clocks": clocks.summary(),

@@ -762,7 +762,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
 #define PKV_DEC_NW 4
 #endif
 #ifndef PKV_DEC_NSTAGE
-#define PKV_DEC_NSTAGE 16
+#define PKV_DEC_NSTAGE 24  // 192 KB of K/V in flight per SM; 16 when the batch's plan needs room
 #endif
 #ifndef PKV_DEC_CTAS
 #define PKV_DEC_CTAS 1
@@ -804,13 +804,13 @@ size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t 
          align256((size_t)pieces * G * D * 4);
 }
 
-template <int D>
-static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
+template <int D, int NSTAGE>
+static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
-  using P_ = DecodePlan<D, C::NW, C::NSTAGE>;
+  using P_ = DecodePlan<D, C::NW, NSTAGE>;
   constexpr bool kOneBox = (D == 128) && (PKV_DEC_ONEBOX != 0);
-  auto kern = decode_split_kernel<D, C::NW, C::NSTAGE, kOneBox>;
+  auto kern = decode_split_kernel<D, C::NW, NSTAGE, kOneBox>;
   (void)max_seq_len;
   CUtensorMap tmK, tmV;
   const bool enc_ok =
@@ -855,6 +855,19 @@ static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a, tmK, tmV);
+}
+
+// The deep ring when the batch's shared-memory plan leaves room for it, a
+// 16-stage one otherwise (large batches: the per-sequence schedule arrays).
+template <int D>
+static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
+                                   int max_seq_len, cudaStream_t stream, int num_sms) {
+  using C = DecodeCfg<D>;
+  if (C::NSTAGE > 16 &&
+      DecodePlan<D, C::NW, (C::NSTAGE > 16 ? C::NSTAGE : 16)>(a.G, a.batch).total > 227 * 1024)
+    return launch_decode_s<D, (C::NSTAGE < 16 ? C::NSTAGE : 16)>(a, k_cache, v_cache,
+                                                                 max_seq_len, stream, num_sms);
+  return launch_decode_s<D, C::NSTAGE>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
 }
 
 cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
