@@ -38,9 +38,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_split_kernel launch on
-# the qwen3_decode workload (ncu --set full capture on a GB300, 316.77 + 4.15 MB);
-# valid for that workload and this decode kernel only.
-DECODE_TRAFFIC_BYTES = 0  # not yet captured for the current decode kernel
+# the qwen3_decode workload (ncu --set full capture on a GB300, 316.78 + 4.15 MB,
+# 24-stage ring); valid for that workload and this decode kernel only.
+DECODE_TRAFFIC_BYTES = 320_930_048
 
 
 # ------------------------------------------------------------------ helpers
