@@ -158,11 +158,24 @@ class DeviceStep:
         g.manual_seed(seed)
         shape = (step.num_pages, step.H_kv, step.P, step.D)
         bf = torch.bfloat16
-        self.k_cache = torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(bf)
-        if step.k_head_scale is not None:
-            s = torch.from_numpy(step.k_head_scale).to(device).view(1, -1, 1, 1)
-            self.k_cache = (self.k_cache.float() * s).to(bf)
-        self.v_cache = torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(bf)
+        if step.num_pages * step.H_kv * step.P * step.D * 2 > (4 << 30):
+            # a multi-layer pool: only this layer's referenced pages are drawn
+            self.k_cache = torch.empty(shape, device=device, dtype=bf)
+            self.v_cache = torch.empty(shape, device=device, dtype=bf)
+            used = torch.from_numpy(step.used_pages.astype(np.int64)).to(device)
+            for c in range(0, used.numel(), 8192):
+                idx = used[c:c + 8192]
+                sub = (idx.numel(),) + shape[1:]
+                self.k_cache[idx] = torch.randn(sub, generator=g, device=device).to(bf)
+                self.v_cache[idx] = torch.randn(sub, generator=g, device=device).to(bf)
+        else:
+            self.k_cache = torch.randn(shape, generator=g, device=device,
+                                       dtype=torch.float32).to(bf)
+            if step.k_head_scale is not None:
+                s = torch.from_numpy(step.k_head_scale).to(device).view(1, -1, 1, 1)
+                self.k_cache = (self.k_cache.float() * s).to(bf)
+            self.v_cache = torch.randn(shape, generator=g, device=device,
+                                       dtype=torch.float32).to(bf)
         n_new = step.n_new_tokens
         self.k_new = torch.randn((n_new, step.H_kv, step.D), generator=g, device=device).to(bf)
         self.v_new = torch.randn((n_new, step.H_kv, step.D), generator=g, device=device).to(bf)
@@ -361,6 +374,8 @@ def run_ours(args):
 
     # ---- secondary: mixed continuous-batching step (tokens/s) -------------
     mixed = None if args.only == "decode" else run_mixed(args, device, stream, flush, rank)
+    sliding = None if args.only else run_sliding(args, device, stream, flush, rank)
+    grpo = None if args.only else run_grpo(args, device, stream, flush, rank)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
@@ -385,6 +400,8 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,  # append + decode (split-KV with fused merge) per step
         "clocks": clocks.summary(),
         "mixed_step": mixed,
+        "sliding_step": sliding,
+        "grpo_step": grpo,
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.skip_cpu else cpu_baseline(step, ds, rank)
@@ -457,7 +474,71 @@ def run_mixed(args, device, stream, flush, rank):
                                 "peak": tf_peak, "unit": "TFLOP/s",
                                 "frac": round(fl / (ph[1] * 1e-3) / 1e12 / tf_peak, 4),
                                 "peak_source": src, "algorithmic_flops": fl},
-            "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2)}
+            "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2),
+            "append_gb_s": round(append_bytes(step, tokens) / (ph[0] * 1e-3) / 1e9, 2),
+            "append_bytes": int(append_bytes(step, tokens))}
+
+
+def run_sliding(args, device, stream, flush, rank):
+    """Sliding-window step (window 512, 8/1 heads, head_dim 256, page 64):
+    layer 0 appends its rows, then prefill + decode; layer 1 reads the same
+    pool with its own queries (shared KV), without an append."""
+    try:
+        step = wl.sliding()
+        ds = DeviceStep(step, wl.BASE_SEED + 4 + 1000 * rank, device)
+        l0 = time_steps([ds.append, ds.varlen, ds.decode], args.steps, args.warmup, stream,
+                        flush)
+        l1 = time_steps([ds.varlen, ds.decode], args.steps, args.warmup, stream, flush)
+        import torch
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            return {"unavailable": f"device error flag {int(ds.err.item())}"}
+    except Exception as e:
+        return {"unavailable": f"{type(e).__name__}: {e}"}
+    p0 = np.mean(np.array(l0), axis=0)
+    p1 = np.mean(np.array(l1), axis=0)
+    fl = varlen_flops(step)
+    db = decode_bytes(step)
+    return {"workload": "sliding: window 512, H 8/1/256, page 64; 32 decode rows (cached "
+                        "~U[1024,8192]) + 4 prefill chunks of 2048; 2 layers on one pool",
+            "layer0_us": {"append": round(p0[0] * 1e3, 2), "varlen": round(p0[1] * 1e3, 2),
+                          "decode": round(p0[2] * 1e3, 2)},
+            "layer1_us": {"varlen": round(p1[0] * 1e3, 2), "decode": round(p1[1] * 1e3, 2)},
+            "varlen_tflops": round(fl / (p0[1] * 1e-3) / 1e12, 2),
+            "decode_gb_s": round(db / (p0[2] * 1e-3) / 1e9, 2),
+            "decode_bytes": int(db), "varlen_flops": fl,
+            "note": "decode K/V (16.8 MB) fits in L2; L2 flushed before every timed step"}
+
+
+def run_grpo(args, device, stream, flush, rank):
+    """GRPO rollout decode step, one layer of 36 in one pool (the last layer's
+    page range): append 256 rows, decode 256 sequences whose 256-token prefix
+    pages are shared by 4 generations."""
+    try:
+        step = wl.grpo_layer(layers=36, layer=35)
+        ds = DeviceStep(step, wl.BASE_SEED + 5 + 1000 * rank, device)
+        per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush,
+                         phase_events=False)
+        import torch
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            return {"unavailable": f"device error flag {int(ds.err.item())}"}
+        del ds
+        torch.cuda.empty_cache()
+    except Exception as e:
+        return {"unavailable": f"{type(e).__name__}: {e}"}
+    ms = float(np.mean([sum(p) for p in per]))
+    logical = decode_bytes(step) + append_bytes(step, step.Bd)
+    return {"workload": "grpo: 64 prompts x 4 generations, prefix 256 shared, completion "
+                        "~U[0,3840], H 32/8/128, page 16, 36 layers in one pool "
+                        f"({step.num_pages} pages)",
+            "layer_step_us": round(ms * 1e3, 2),
+            "step_ms_36_layers": round(36 * ms, 3),
+            "decode_tokens_per_s": round(step.Bd / (36 * ms * 1e-3), 1),
+            "logical_gb_s": round(logical / (ms * 1e-3) / 1e9, 2),
+            "logical_bytes_per_layer": int(logical),
+            "note": "one layer timed (append + decode), scaled by 36; logical bytes count "
+                    "each generation's shared prefix pages"}
 
 
 # ---------------------------------------------------------- CPU baselines
