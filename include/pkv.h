@@ -25,11 +25,12 @@
  *   row p % page_size.  A slot is page * page_size + row.
  * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
  * - Supported shapes: head_dim in {64, 128, 256}; page_size a multiple of
- *   16 (16 and 64 are the tested sizes); num_q_heads a multiple of
- *   num_kv_heads with a group of at most 8 for decode and dividing 128 for
- *   varlen; decode batch <= 4096 and varlen batch <= 1024 (both also bounded
- *   by the shared memory their schedules need).  Anything else returns
- *   PKV_ERR_UNSUPPORTED.
+ *   16 (decode tests use 16 and 64, varlen tests 16 to 256), and for varlen
+ *   a divisor or a multiple of its key tile (128 keys for head_dim 64 and
+ *   128, 64 for 256); num_q_heads a multiple of num_kv_heads with a group of
+ *   at most 8 for decode and dividing 128 for varlen; decode batch <= 4096
+ *   and varlen batch <= 1024 (their schedules live in shared memory).
+ *   Anything else returns PKV_ERR_UNSUPPORTED.
  * - Host-detectable argument errors return PKV_ERR_INVALID before anything
  *   is enqueued.  CUDA launch errors return PKV_ERR_CUDA (message from
  *   pkv_last_cuda_error()).
@@ -159,9 +160,8 @@ pkv_status paged_attn_decode(void* out, const void* q,
  *   window         > 0 (causal only): also require q_pos - k_pos < window
  *
  * Runs QK^T and PV on the tcgen05 tensor cores with TMEM accumulators in
- * one persistent launch.  Limits: batch <= 1024 chunks; the per-chunk
- * schedule (about 4 bytes per 128*2/G query rows of max_seqlen_q) must fit
- * in shared memory, else PKV_ERR_UNSUPPORTED.
+ * one persistent launch (one CTA per SM).  Limits: batch <= 1024 chunks;
+ * page_size as above, else PKV_ERR_UNSUPPORTED.
  */
 pkv_status paged_attn_varlen(void* out, const void* q,
                              const void* k_cache, const void* v_cache,
