@@ -17,27 +17,30 @@
 //    the kv head, so a K/V tile staged once in shared memory feeds the
 //    whole GQA group and, with NQ = 2, two Q tiles.
 //  * Every CTA derives the same schedule from cu_seq_lens in its prologue:
-//    (chunk, item) pairs sorted by their number of KV tiles, most first,
-//    dealt to the CTAs in a snake so that every CTA gets a similar total.
+//    (chunk, item) pairs sorted by their number of KV tiles, most first (up
+//    to 256 pairs; beyond that in chunk order), dealt to the CTAs in a snake
+//    so that every CTA gets a similar total.
 //  * The CTA's items form one stream of KV tiles; no role drains at an
 //    item boundary.  Two producer warps load with TMA (128-byte swizzle, one
 //    box per page slice, lane-parallel issue): one the K tiles (and the Q
 //    tiles when the stream enters an item), one the V tiles, each through
 //    its own ring.
-//  * Warp 1 allocates 512 TMEM columns and issues tcgen05.mma (cta_group::1,
-//    kind::f16, bf16 in, fp32 accumulate):
+//  * The MMA warp (warp 4*NQ+1) allocates 512 TMEM columns and issues
+//    tcgen05.mma (cta_group::1, kind::f16, bf16 in, fp32 accumulate) as a
+//    converged warp, one elected lane per operation:
 //        S_x(t)  = Q_x K(t)^T        smem x smem -> TMEM  (M=128, N=BN)
 //        O_x    += P_x(t) V(t)       TMEM x smem -> TMEM  (M=128, N=D)
 //    P_x(t) is written by the softmax into the TMEM columns of S_x(t), as
 //    bf16 pairs, and read from there by the PV MMA.  Per tile t and Q tile
-//    x the issue order is PV_x(t), QK_x(t+NS): the tensor pipe runs in
-//    issue order, so S_x(t+NS) may reuse the columns P_x(t) was read from.
+//    x the issue order is PV_x(t), QK_x(t+NS): the tensor pipe runs one
+//    thread's MMAs in issue order, so S_x(t+NS) may reuse the columns P_x(t)
+//    was read from.
 //    With NQ = 2 (NS = 1) the two Q tiles' softmaxes alternate with the
 //    tensor core; with NQ = 1 (NS = 2, head_dim 256) S is double-buffered
 //    so that QK of the next tile runs under the softmax of this one.
 //  * One softmax warpgroup per Q tile (one thread per row): tcgen05.ld the
 //    S row, mask (boundary tiles only), online softmax in the exp2 domain
-//    (packed f32x2 arithmetic; a quarter of the exponentials on the FMA
+//    (packed f32x2 arithmetic; an eighth of the exponentials on the FMA
 //    pipes, the rest on the SFU), P -> TMEM, rescale O in TMEM only when the
 //    running max grew by more than 2^8 (the stale max is exact math: O and
 //    l share it), epilogue O / l -> bf16.
