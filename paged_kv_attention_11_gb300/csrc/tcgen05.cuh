@@ -18,17 +18,6 @@
 namespace pkv {
 namespace tc {
 
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 // The two 32-bit halves of a 128-byte-swizzle descriptor: the low half
 // carries the start address (>> 4) and the leading byte offset, the high
 // half the stride byte offset, the version bit and the swizzle mode, so a
@@ -70,65 +59,10 @@ __device__ __forceinline__ void fence_before_sync() {
 __device__ __forceinline__ void fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // --------------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc]; accumulate iff `acc`.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// Same MMA with the descriptors given as 32-bit halves.
-__device__ __forceinline__ void mma_ss_h(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                         uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                         uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "mov.b64 da, {%1, %2};\n\t"
-      "mov.b64 db, {%3, %4};\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc given as halves]: A is M=128 lanes x
-// K columns of packed 16-bit pairs.
-__device__ __forceinline__ void mma_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                         uint32_t b_hi, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "mov.b64 db, {%2, %3};\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 // Warp-converged forms: every lane of the warp executes them with the same
 // operands and one elected lane issues, so the operands can stay in
 // uniform registers.
-__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                         uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                         uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
-      "mov.b64 da, {%1, %2};\n\t"
-      "mov.b64 db, {%3, %4};\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
-      : "memory");
-}
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                          uint32_t b_hi, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -196,14 +130,6 @@ __device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, 1;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc), "n"(B_STEP), "n"(2 * B_STEP),
       "n"(3 * B_STEP)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
       : "memory");
 }
 
