@@ -134,6 +134,14 @@ def append_bytes(step: wl.Step, n_rows: int) -> int:
     return n_rows * step.H_kv * step.D * 2 * 2 * 2 + n_rows * 8
 
 
+def append_rope_bytes(step: wl.Step, n_rows: int) -> int:
+    """Fused norm + rotary + append: q read and written in place, k and v
+    read and written, one cos/sin table row (D float32) per token, slot and
+    position per token, and the two [D] bf16 norm weights."""
+    per_tok = (step.H_q * step.D * 2 * 2 + step.H_kv * step.D * 2 * 2 * 2 + step.D * 4 + 8 + 4)
+    return n_rows * per_tok + 2 * step.D * 2
+
+
 def varlen_flops(step: wl.Step) -> float:
     """4*D*H_q flops per unmasked (query, key) pair (QK^T and PV)."""
     pairs = 0
@@ -198,6 +206,35 @@ class DeviceStep:
         need = pkv.decode_workspace_size(max(step.Bd, 1), step.H_q, step.H_kv, step.D)
         self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def enable_rope(self, theta: float = 1e6, eps: float = 1e-6, max_position: int = 16384):
+        """Set up the fused norm + rotary append: one contiguous q for all
+        new tokens (prefill rows, then decode rows; the varlen and decode
+        calls then read its two slices), positions, the cos/sin table and
+        the two norm weights."""
+        import torch
+        s = self.step
+        dev = self.k_cache.device
+        parts = [t for t in (self.q_pre, self.q_dec) if t is not None]
+        self.q_all = torch.cat(parts).contiguous()
+        if s.Bp:
+            self.q_pre = self.q_all[:s.total_q]
+        if s.Bd:
+            self.q_dec = self.q_all[s.total_q:]
+        self.positions = torch.from_numpy(s.all_positions).to(dev)
+        self.cos_sin = torch.empty((max_position, s.D), dtype=torch.float32, device=dev)
+        self.pkv.rope_table(self.cos_sin, theta)
+        g = torch.Generator(device=dev)
+        g.manual_seed(77)
+        self.q_w = (1 + 0.1 * torch.randn(s.D, generator=g, device=dev)).to(torch.bfloat16)
+        self.k_w = (1 + 0.1 * torch.randn(s.D, generator=g, device=dev)).to(torch.bfloat16)
+        self.rope_eps = eps
+
+    def append_rope(self, stream):
+        self.pkv.paged_kv_append_rope(self.q_all, self.k_new, self.v_new, self.k_cache,
+                                      self.v_cache, self.slots, self.positions, self.cos_sin,
+                                      self.q_w, self.k_w, self.rope_eps, err_flag=self.err,
+                                      stream=stream)
 
     def append(self, stream):
         self.pkv.paged_kv_append(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
@@ -463,7 +500,35 @@ def run_mixed(args, device, stream, flush, rank):
     ph = np.mean(np.array(per), axis=0)
     tokens = step.n_new_tokens
     fl = varlen_flops(step)
-    _, tf_peak, _, src = peaks()
+    hbm_peak, tf_peak, _, src = peaks()
+    # the same step with q/k RMSNorm and the rotary embedding fused into the
+    # append (the attention layer's whole input transform)
+    try:
+        ds.enable_rope()
+        rope_step = time_steps([ds.append_rope, ds.varlen, ds.decode], args.steps, args.warmup,
+                               stream, flush, phase_events=False)
+        rope_per = time_steps([ds.append_rope, ds.varlen, ds.decode], args.steps, args.warmup,
+                              stream, flush)
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(ds.err.item())}")
+        rms = float(np.mean([sum(p) for p in rope_step]))
+        rph = np.mean(np.array(rope_per), axis=0)
+        rb = append_rope_bytes(step, tokens)
+        with_rope = {
+            "value": round(tokens / (rms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(rms, 5),
+            "phase_us": {"append_rope": round(rph[0] * 1e3, 2), "varlen": round(rph[1] * 1e3, 2),
+                         "decode": round(rph[2] * 1e3, 2)},
+            "append_rope_roofline": {
+                "bound": "hbm", "achieved": round(rb / (rph[0] * 1e-3) / 1e9, 2),
+                "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(rb / (rph[0] * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": src,
+                "algorithmic_bytes": int(rb)},
+            "note": "q and k RMSNorm + rotary (theta 1e6) over all new tokens fused into the "
+                    "append; q transformed in place"}
+    except Exception as e:
+        with_rope = {"unavailable": f"{type(e).__name__}: {e}"}
     return {"metric": "mixed-step tokens/sec", "value": round(tokens / (ms * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(ms, 5), "tokens_per_step": int(tokens),
             "workload": "mixed_step: 8 prefill chunks (len ~U[128,1024] on prefix ~U[0,512]) + "
@@ -476,7 +541,8 @@ def run_mixed(args, device, stream, flush, rank):
                                 "peak_source": src, "algorithmic_flops": fl},
             "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2),
             "append_gb_s": round(append_bytes(step, tokens) / (ph[0] * 1e-3) / 1e9, 2),
-            "append_bytes": int(append_bytes(step, tokens))}
+            "append_bytes": int(append_bytes(step, tokens)),
+            "with_rope": with_rope}
 
 
 def run_sliding(args, device, stream, flush, rank):

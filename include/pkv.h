@@ -63,6 +63,8 @@ typedef enum {
 #define PKV_DEVERR_LEN     4  /* a length exceeded max_blocks_per_seq*page_size or the
                                  declared maximum: clamped */
 #define PKV_DEVERR_TIMEOUT 8  /* an internal pipeline wait gave up (never expected) */
+#define PKV_DEVERR_POS     16 /* a position outside [0, max_position) of the rotary
+                                 table: that token was skipped */
 
 /*
  * paged_kv_append - scatter this step's new K/V rows into the page pools.
@@ -204,6 +206,70 @@ pkv_status paged_attn_decode_static(void* out, const void* q,
                                     int32_t head_dim, int32_t page_size, int64_t num_pages,
                                     int32_t max_seq_len, float scale, int32_t window,
                                     int32_t* err_flag, void* stream);
+
+/*
+ * pkv_rope_table - fill the rotary (cos, sin) table that
+ * paged_kv_append_rope reads.  Source: scripts/benchmarks commit log,
+ * Gemma-4 engine commit ("Dual attention regimes": (cos, sin) pairs
+ * precomputed per position and per attention regime, rope_theta 1e6 for
+ * full attention).
+ *
+ *   cos_sin       [max_position, head_dim] float32 (written), 16-byte
+ *                 aligned.  Row p, column i < head_dim/2 holds
+ *                 cos(p * theta^(-2i/head_dim)); column head_dim/2 + i the
+ *                 sine of the same angle.
+ *   theta         the rotary base (> 0 and finite)
+ *
+ * Each entry is computed in double precision on the device and rounded
+ * once to float.  Call it once per (max_position, head_dim, theta); the
+ * table is the caller's.  head_dim must be even; max_position == 0 is a
+ * no-op.
+ */
+pkv_status pkv_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim,
+                          double theta, void* stream);
+
+/*
+ * paged_kv_append_rope - paged_kv_append with the attention's input
+ * transform fused in: per-head RMSNorm of q and k, then the rotary
+ * embedding, for the same tokens whose K/V rows are appended.  Sources:
+ * scripts/benchmarks commit log -- Llama-3.2 support commit (Qwen3's
+ * per-head QK RMSNorm over head_dim of [B, S, H, D]), Gemma-4 shared-KV
+ * commit (the cache keeps post-rotary K and V as projected).
+ *
+ *   q              [num_tokens, num_q_heads, head_dim] bf16, transformed in
+ *                  place; NULL: no q (num_q_heads is then ignored)
+ *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] bf16 (read)
+ *   k_cache,v_cache,slot_mapping, page_size, num_pages: as paged_kv_append
+ *   positions      [num_tokens] int32: the token's position in its sequence
+ *                  (the row of cos_sin)
+ *   cos_sin        [max_position, head_dim] float32, as pkv_rope_table
+ *                  writes it (16-byte aligned)
+ *   q_norm_weight, k_norm_weight
+ *                  [head_dim] bf16 RMSNorm weights, 16-byte aligned; NULL
+ *                  means no norm on that side
+ *   norm_eps       the RMSNorm epsilon (>= 0, finite)
+ *
+ * For each token t and head, with x the row as float:
+ *   x <- x * w / sqrt(mean(x^2) + norm_eps)        (when a weight is given)
+ *   for i < head_dim/2, with c, s = cos_sin[positions[t]][i], [head_dim/2 + i]:
+ *     x'[i] = x[i] c - x[i + head_dim/2] s,  x'[i + head_dim/2] = x[i + head_dim/2] c + x[i] s
+ * computed in float with one rounding to bf16 (nearest-even).  q rows are
+ * written back; k rows go to slot_mapping[t] and v rows are copied there
+ * bit-exactly.  A negative slot skips the append of that token (its q rows
+ * are still transformed).  A position outside [0, max_position) skips the
+ * token whole and raises PKV_DEVERR_POS.  head_dim in {64, 128, 256};
+ * num_tokens * (num_q_heads + num_kv_heads) * head_dim / 8 < 2^30.
+ * q must not overlap k_new, v_new or the pools.
+ */
+pkv_status paged_kv_append_rope(void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache,
+                                const int64_t* slot_mapping, const int32_t* positions,
+                                const float* cos_sin, int32_t max_position,
+                                const void* q_norm_weight, const void* k_norm_weight,
+                                float norm_eps, int32_t num_tokens,
+                                int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t page_size, int64_t num_pages,
+                                int32_t* err_flag, void* stream);
 
 /* Human-readable name of a pkv_status value (static string). */
 const char* pkv_status_string(int32_t status);

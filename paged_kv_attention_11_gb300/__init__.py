@@ -6,6 +6,9 @@ Three calls, same names as the C ABI (include/pkv.h):
 * ``paged_attn_decode`` one query per sequence over its paged prefix
 * ``paged_attn_varlen`` packed variable-length (prefill) attention
 
+plus ``paged_kv_append_rope`` (the append with q/k RMSNorm and the rotary
+embedding fused in) and ``rope_table`` (its cos/sin table).
+
 This module only marshals arguments (device pointers, sizes, the current
 CUDA stream) into the library; every step of the computation runs in the
 library's CUDA kernels.  There is no fallback: if libpkv.so is missing the
@@ -15,6 +18,7 @@ from ._binding import (  # noqa: F401
     PKVError,
     DEVERR_LEN,
     DEVERR_PAGE,
+    DEVERR_POS,
     DEVERR_SLOT,
     DEVERR_TIMEOUT,
     decode_workspace_size,
@@ -24,4 +28,6 @@ from ._binding import (  # noqa: F401
     paged_attn_decode_static,
     paged_attn_varlen,
     paged_kv_append,
+    paged_kv_append_rope,
+    rope_table,
 )

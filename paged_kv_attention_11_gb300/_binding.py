@@ -15,6 +15,7 @@ DEVERR_SLOT = 1
 DEVERR_PAGE = 2
 DEVERR_LEN = 4
 DEVERR_TIMEOUT = 8
+DEVERR_POS = 16
 
 _c_i32, _c_i64, _c_p, _c_f = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
 _SIGS = {
@@ -30,6 +31,9 @@ _SIGS = {
     "paged_attn_decode_static": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32,
                                  _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_p,
                                  _c_p],
+    "pkv_rope_table": [_c_p, _c_i32, _c_i32, ctypes.c_double, _c_p],
+    "paged_kv_append_rope": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p,
+                             _c_f, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_p, _c_p],
     "pkv_status_string": [_c_i32],
     "pkv_last_cuda_error": [],
 }
@@ -174,3 +178,41 @@ def paged_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
         float(scale), int(window), _ptr(err_flag), _stream(stream)))
     return out
+
+
+def rope_table(cos_sin: torch.Tensor, theta: float, stream=None) -> torch.Tensor:
+    """Fill cos_sin [max_position, head_dim] float32 with the rotary table:
+    column i < head_dim/2 is cos(p * theta^(-2i/head_dim)), column
+    head_dim/2 + i the sine."""
+    if cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous() or cos_sin.dim() != 2:
+        raise ValueError("cos_sin must be a contiguous [max_position, head_dim] float32 tensor")
+    _check("pkv_rope_table", lib().pkv_rope_table(
+        _ptr(cos_sin), cos_sin.shape[0], cos_sin.shape[1], float(theta), _stream(stream)))
+    return cos_sin
+
+
+def paged_kv_append_rope(q: Optional[torch.Tensor], k_new: torch.Tensor, v_new: torch.Tensor,
+                         k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         slot_mapping: torch.Tensor, positions: torch.Tensor,
+                         cos_sin: torch.Tensor, q_norm_weight: Optional[torch.Tensor] = None,
+                         k_norm_weight: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                         err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q [T, H_q, D] (in place) or None; k_new/v_new [T, H_kv, D]; caches
+    [num_pages, H_kv, P, D]; slots [T] int64; positions [T] int32; cos_sin
+    [max_position, D] float32; norm weights [D] bf16 or None."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    for n, t in (("q", q), ("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+        if t is not None:
+            _bf16(t, n)
+    if slot_mapping.dtype != torch.int64 or positions.dtype != torch.int32:
+        raise ValueError("slot_mapping must be int64 and positions int32")
+    if cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous():
+        raise ValueError("cos_sin must be a contiguous float32 tensor")
+    num_pages, H_kv, P, D = k_cache.shape
+    H_q = q.shape[1] if q is not None else 0
+    _check("paged_kv_append_rope", lib().paged_kv_append_rope(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+        _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], _ptr(q_norm_weight),
+        _ptr(k_norm_weight), float(eps), k_new.shape[0], H_q, H_kv, D, P, num_pages,
+        _ptr(err_flag), _stream(stream)))

@@ -172,4 +172,66 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
+pkv_status pkv_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim,
+                          double theta, void* stream) {
+  if (max_position < 0 || head_dim <= 0 || head_dim % 2 != 0) return PKV_ERR_INVALID;
+  if (!(theta > 0.0) || theta > 1e300) return PKV_ERR_INVALID;  // NaN, <= 0 or infinite
+  if (max_position == 0) return PKV_OK;
+  if (!cos_sin || !aligned16(cos_sin)) return PKV_ERR_INVALID;
+  int sms = 0;
+  if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  cudaError_t e = pkv::launch_rope_table(cos_sin, max_position, head_dim, theta,
+                                         static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+pkv_status paged_kv_append_rope(void* q, const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, const int64_t* slot_mapping,
+                                const int32_t* positions, const float* cos_sin,
+                                int32_t max_position, const void* q_norm_weight,
+                                const void* k_norm_weight, float norm_eps, int32_t num_tokens,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t page_size, int64_t num_pages, int32_t* err_flag,
+                                void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+      num_pages <= 0 || max_position <= 0 || (q && num_q_heads <= 0))
+    return PKV_ERR_INVALID;
+  if (!(norm_eps >= 0.f) || norm_eps > 3e38f) return PKV_ERR_INVALID;  // NaN, < 0, inf
+  if (!supported_head_dim(head_dim)) return PKV_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)num_tokens * ((q ? num_q_heads : 0) + (int64_t)num_kv_heads);
+  if (rows * (head_dim / 8) >= (int64_t(1) << 30)) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !positions || !cos_sin)
+    return PKV_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(cos_sin) || (q && !aligned16(q)) || (q_norm_weight && !aligned16(q_norm_weight)) ||
+      (k_norm_weight && !aligned16(k_norm_weight)))
+    return PKV_ERR_INVALID;
+  int sms = 0;
+  if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  pkv::RopeAppendArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.slot_mapping = slot_mapping;
+  a.positions = positions;
+  a.cos_sin = cos_sin;
+  a.q_w = q ? q_norm_weight : nullptr;
+  a.k_w = k_norm_weight;
+  a.eps = norm_eps;
+  a.max_pos = max_position;
+  a.T = num_tokens;
+  a.H_q = q ? num_q_heads : 0;
+  a.H_kv = num_kv_heads;
+  a.P = page_size;
+  a.num_slots = num_pages * (int64_t)page_size;
+  a.err = err_flag;
+  cudaError_t e =
+      pkv::launch_kv_append_rope(a, head_dim, static_cast<cudaStream_t>(stream), sms);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 }  // extern "C"

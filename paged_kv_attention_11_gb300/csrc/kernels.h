@@ -19,6 +19,30 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
                              int32_t D, int32_t P, int64_t num_pages, int32_t* err,
                              cudaStream_t stream, int num_sms);
 
+// Arguments of the fused norm + rotary + append kernel (rope_append.cu).
+struct RopeAppendArgs {
+  void* q;                      // [T, H_q, D] bf16, transformed in place; null: no q
+  const void* k_new;            // [T, H_kv, D] bf16
+  const void* v_new;            // [T, H_kv, D] bf16
+  void* k_cache;                // [num_pages, H_kv, P, D] bf16
+  void* v_cache;
+  const int64_t* slot_mapping;  // [T]
+  const int32_t* positions;     // [T]
+  const float* cos_sin;         // [max_pos, D] f32: cos in [0, D/2), sin in [D/2, D)
+  const void* q_w;              // [D] bf16 RMSNorm weight of q, or null (no norm)
+  const void* k_w;              // [D] bf16 RMSNorm weight of k, or null
+  float eps;
+  int32_t max_pos, T, H_q, H_kv, P;
+  int64_t num_slots;
+  int32_t* err;
+};
+
+cudaError_t launch_rope_table(float* cos_sin, int32_t max_pos, int32_t D, double theta,
+                              cudaStream_t stream, int num_sms);
+
+cudaError_t launch_kv_append_rope(const RopeAppendArgs& a, int32_t D, cudaStream_t stream,
+                                  int num_sms);
+
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms);
 
 cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

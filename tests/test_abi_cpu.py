@@ -99,6 +99,33 @@ def test_host_validation_rejects_before_cuda(lib):
                                0.1, 0, None, 0, None, None) == 0
 
 
+def test_rope_entry_points_validate_on_host(lib):
+    L = _bind(lib)
+    P = 0x1000  # fake, never dereferenced: validation fails first
+    nan = float("nan")
+
+    def app(q=P, T=4, H_q=8, H_kv=2, D=128, max_pos=64, eps=1e-6, cs=P, slots=P):
+        return L.paged_kv_append_rope(q, P, P, P, P, slots, P, cs, max_pos, None, None, eps, T,
+                                      H_q, H_kv, D, 16, 64, None, None)
+    assert app(T=-1) == 1
+    assert app(max_pos=0) == 1
+    assert app(eps=nan) == 1 and app(eps=-1.0) == 1
+    assert app(H_q=0) == 1                 # q given without heads
+    assert app(H_kv=0) == 1
+    assert app(D=96) == 2                  # head_dim outside {64, 128, 256}
+    assert app(cs=P + 4) == 1              # misaligned table
+    assert app(slots=None) == 1            # missing slot mapping
+    assert app(T=1 << 28) == 2             # more vectors than one launch indexes
+    assert app(T=0, q=None, cs=None, slots=None) == 0   # no tokens: no-op
+    # the table: odd head_dim, non-positive / NaN / infinite theta, misaligned
+    assert L.pkv_rope_table(P, 16, 127, 1e6, None) == 1
+    assert L.pkv_rope_table(P, 16, 128, 0.0, None) == 1
+    assert L.pkv_rope_table(P, 16, 128, nan, None) == 1
+    assert L.pkv_rope_table(P, 16, 128, float("inf"), None) == 1
+    assert L.pkv_rope_table(P + 8, 16, 128, 1e6, None) == 1
+    assert L.pkv_rope_table(None, 0, 128, 1e6, None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import paged_kv_attention_11_gb300._binding as b
     monkeypatch.setattr(b, "_LIB_PATH", str(tmp_path / "missing.so"))

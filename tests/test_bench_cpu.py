@@ -66,3 +66,19 @@ def test_reference_arm_runs_on_host():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_append_rope_bytes_counts_every_tensor_once():
+    # recount from the tensors the fused call touches, itemised
+    step = wl.mixed_step()
+    n = step.n_new_tokens
+    bf16, f32 = 2, 4
+    tensors = {
+        "q read": n * step.H_q * step.D * bf16, "q write": n * step.H_q * step.D * bf16,
+        "k_new": n * step.H_kv * step.D * bf16, "v_new": n * step.H_kv * step.D * bf16,
+        "k pool rows": n * step.H_kv * step.D * bf16, "v pool rows": n * step.H_kv * step.D * bf16,
+        "cos/sin rows": n * step.D * f32, "slots": n * 8, "positions": n * 4,
+        "norm weights": 2 * step.D * bf16,
+    }
+    assert bench.append_rope_bytes(step, n) == sum(tensors.values())
+    assert len(step.all_positions) == n

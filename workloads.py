@@ -131,6 +131,15 @@ class Step:
         return (np.concatenate(out) if out else np.zeros(0)).astype(np.int64)
 
     @property
+    def all_positions(self) -> np.ndarray:
+        """Position of every new token in its sequence, in append order
+        (prefill tokens prefix + i, then each decode row's cached length)."""
+        parts = [self.pre_prefix[c] + np.arange(self.pre_qlen[c]) for c in range(self.Bp)]
+        if self.Bd:
+            parts.append(np.asarray(self.dec_cached))
+        return (np.concatenate(parts) if parts else np.zeros(0)).astype(np.int32)
+
+    @property
     def n_new_tokens(self) -> int:
         return self.total_q + self.Bd
 
