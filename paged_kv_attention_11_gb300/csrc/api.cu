@@ -226,6 +226,9 @@ pkv_status paged_kv_append_rope(void* q, const void* k_new, const void* v_new, v
   a.H_q = q ? num_q_heads : 0;
   a.H_kv = num_kv_heads;
   a.P = page_size;
+  a.P_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == page_size) a.P_shift = sh;
   a.num_slots = num_pages * (int64_t)page_size;
   a.err = err_flag;
   cudaError_t e =

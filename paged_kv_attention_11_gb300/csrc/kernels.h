@@ -33,6 +33,7 @@ struct RopeAppendArgs {
   const void* k_w;              // [D] bf16 RMSNorm weight of k, or null
   float eps;
   int32_t max_pos, T, H_q, H_kv, P;
+  int32_t P_shift;              // log2(P) when P is a power of two, else -1
   int64_t num_slots;
   int32_t* err;
 };

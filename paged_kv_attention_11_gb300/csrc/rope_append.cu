@@ -60,121 +60,131 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cs,
   }
 }
 
-// One vector of a q/k row: where it comes from and its raw contents.
-struct RopeVec {
-  int32_t t, hr, l, pos;
-  bool in, live, isq;
-  int64_t src;
-  uint4 x, v;
-};
+// Work unit: kRopeSteps * (256 / D) consecutive rows of one token's q/k
+// rows (q heads first, then kv heads), processed by one warp.  Lane `lane`
+// always owns the same 16-byte slice l = lane % (D/8) of a row, so the
+// token's position and slot, the lane's cos/sin values and its slice of
+// both norm weights are loaded once per unit and reused for every row.
+// Each step covers 32 / (D/8) rows; the unit's kRopeSteps steps load their
+// rows (and, for kv rows, the v rows) before any is finished.
+#ifndef PKV_ROPE_STEPS
+#define PKV_ROPE_STEPS 4
+#endif
+#ifndef PKV_ROPE_MINBLOCKS
+#define PKV_ROPE_MINBLOCKS 2
+#endif
+constexpr int kRopeSteps = PKV_ROPE_STEPS;
+constexpr int kRopeBlocksPerSm = PKV_ROPE_MINBLOCKS;
 
 template <int D>
-__device__ __forceinline__ RopeVec rope_load(const RopeAppendArgs& a, int32_t i, int32_t total,
-                                             int32_t Hq, int32_t rows_per_tok) {
-  constexpr int LPR = D / 8;
-  RopeVec r;
-  r.in = i < total;
-  const int32_t row = r.in ? i / LPR : 0;
-  r.l = i & (LPR - 1);
-  r.t = row / rows_per_tok;
-  r.hr = row - r.t * rows_per_tok;
-  r.isq = r.hr < Hq;
-  r.pos = r.in ? __ldg(a.positions + r.t) : 0;
-  r.live = r.in && r.pos >= 0 && r.pos < a.max_pos;
-  r.src = r.isq ? ((int64_t)r.t * Hq + r.hr) * LPR + r.l
-                : ((int64_t)r.t * a.H_kv + (r.hr - Hq)) * LPR + r.l;
-  r.x = make_uint4(0u, 0u, 0u, 0u);
-  r.v = r.x;
-  if (r.live) {
-    if (r.isq) {
-      r.x = static_cast<const uint4*>(a.q)[r.src];
-    } else {
-      r.x = __ldg(static_cast<const uint4*>(a.k_new) + r.src);
-      r.v = __ldg(static_cast<const uint4*>(a.v_new) + r.src);
-    }
-  }
-  return r;
-}
-
-// Norm, rotate and store one vector.  Every lane of the warp calls it (the
-// shuffles need them all), whatever its vector's state.
-template <int D>
-__device__ __forceinline__ void rope_finish(const RopeAppendArgs& a, const RopeVec& r,
-                                            int32_t Hq) {
-  constexpr int LPR = D / 8;     // lanes per row
-  constexpr int HALF = LPR / 2;  // lane distance between rotary partners
-  float x[8];
-  unpack8(r.x, x);
-  // per-head RMSNorm: sum of squares over the row's LPR lanes
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
-#pragma unroll
-  for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-  const uint4* w = static_cast<const uint4*>(r.isq ? a.q_w : a.k_w);
-  if (w != nullptr) {
-    const float rn = rsqrtf(ss * (1.f / (float)D) + a.eps);
-    float wf[8];
-    unpack8(__ldg(w + r.l), wf);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = x[k] * rn * wf[k];
-  }
-  // rotary: lanes [0, HALF) hold dims i < D/2, lanes [HALF, LPR) dims i + D/2
-  float y[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) y[k] = __shfl_xor_sync(0xFFFFFFFFu, x[k], HALF);
-  const bool lo = r.l < HALF;
-  const int i0 = (lo ? r.l : r.l - HALF) * 8;  // first pair index of this vector
-  const float4* cs = reinterpret_cast<const float4*>(a.cos_sin + (int64_t)(r.live ? r.pos : 0) * D);
-  const float4 c0 = __ldg(cs + i0 / 4), c1 = __ldg(cs + i0 / 4 + 1);
-  const float4 s0 = __ldg(cs + (D / 2 + i0) / 4), s1 = __ldg(cs + (D / 2 + i0) / 4 + 1);
-  const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  float o[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    o[k] = lo ? fmaf(x[k], c[k], -y[k] * s[k]) : fmaf(x[k], c[k], y[k] * s[k]);
-
-  if (!r.in) return;
-  if (!r.live) {
-    if (r.hr == 0 && r.l == 0) raise_err(a.err, PKV_DEVERR_POS);
-    return;
-  }
-  if (r.isq) {
-    static_cast<uint4*>(a.q)[r.src] = pack8(o);
-    return;
-  }
-  const int64_t slot = __ldg(a.slot_mapping + r.t);
-  if (slot < 0) return;  // padding row: skip the append
-  if (slot >= a.num_slots) {
-    if (r.hr == Hq && r.l == 0) raise_err(a.err, PKV_DEVERR_SLOT);
-    return;
-  }
-  const int64_t page = slot / a.P;
-  const int64_t prow = slot - page * a.P;
-  const int64_t dst = ((page * a.H_kv + (r.hr - Hq)) * a.P + prow) * LPR + r.l;
-  static_cast<uint4*>(a.k_cache)[dst] = pack8(o);
-  static_cast<uint4*>(a.v_cache)[dst] = r.v;
-}
-
-template <int D>
-__global__ void __launch_bounds__(256, 4) kv_append_rope_kernel(const RopeAppendArgs a) {
-  constexpr int LPR = D / 8;
+__global__ void __launch_bounds__(256, kRopeBlocksPerSm) kv_append_rope_kernel(
+    const RopeAppendArgs a) {
+  constexpr int LPR = D / 8;           // lanes per row
+  constexpr int HALF = LPR / 2;        // lane distance between rotary partners
+  constexpr int RPS = 32 / LPR;        // rows per warp step
+  constexpr int U = kRopeSteps;        // steps per unit
+  constexpr int R = U * RPS;           // rows per unit
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
+  const int l = lane & (LPR - 1);      // the lane's slice of a row
+  const int sub = lane / LPR;          // the lane's row within a step
+  const bool lo = l < HALF;
+  const int i0 = (l & (HALF - 1)) * 8;  // first rotary pair of the slice
   const int32_t Hq = a.q != nullptr ? a.H_q : 0;
-  const int32_t rows_per_tok = Hq + a.H_kv;
-  const int32_t total = a.T * rows_per_tok * LPR;  // host-checked: < 2^30
-  const int32_t nthreads = (int32_t)(gridDim.x * blockDim.x);
-  // Whole warps iterate together (the shuffles need every lane); two
-  // vectors per thread per step, both loaded before either is finished.
-  for (int32_t base = (int32_t)(blockIdx.x * blockDim.x + (threadIdx.x & ~31u)); base < total;
-       base += 2 * nthreads) {
-    const RopeVec r0 = rope_load<D>(a, base + lane, total, Hq, rows_per_tok);
-    const RopeVec r1 = rope_load<D>(a, base + nthreads + lane, total, Hq, rows_per_tok);
-    rope_finish<D>(a, r0, Hq);
-    rope_finish<D>(a, r1, Hq);
+  const int32_t rows = Hq + a.H_kv;
+  const int32_t units_per_tok = (rows + R - 1) / R;
+  const int64_t units = (int64_t)a.T * units_per_tok;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint4* q = static_cast<uint4*>(a.q);
+  const uint4* k_new = static_cast<const uint4*>(a.k_new);
+  const uint4* v_new = static_cast<const uint4*>(a.v_new);
+  // the lane's slices of the two norm weights, kept packed (bf16)
+  const uint4 qw = a.q_w ? __ldg(static_cast<const uint4*>(a.q_w) + l) : make_uint4(0u, 0u, 0u, 0u);
+  const uint4 kw = a.k_w ? __ldg(static_cast<const uint4*>(a.k_w) + l) : make_uint4(0u, 0u, 0u, 0u);
+
+  for (int64_t unit = (((int64_t)blockIdx.x * blockDim.x) >> 5) + (threadIdx.x >> 5);
+       unit < units; unit += nwarps) {  // warp-uniform
+    const int32_t t = (int32_t)(unit / units_per_tok);
+    const int32_t row0 = (int32_t)(unit - (int64_t)t * units_per_tok) * R;
+    const int32_t pos = __ldg(a.positions + t);
+    const bool live = pos >= 0 && pos < a.max_pos;
+    // the rows: loads first
+    uint4 x[U], v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t hr = row0 + u * RPS + sub;
+      x[u] = make_uint4(0u, 0u, 0u, 0u);
+      v[u] = x[u];
+      if (live && hr < rows) {
+        if (hr < Hq) {
+          x[u] = q[((int64_t)t * Hq + hr) * LPR + l];
+        } else {
+          const int64_t src = ((int64_t)t * a.H_kv + (hr - Hq)) * LPR + l;
+          x[u] = __ldg(k_new + src);
+          v[u] = __ldg(v_new + src);
+        }
+      }
+    }
+    if (!live) {  // warp-uniform: the whole unit belongs to token t
+      if (row0 == 0 && lane == 0) raise_err(a.err, PKV_DEVERR_POS);
+      continue;
+    }
+    const float4* cs = reinterpret_cast<const float4*>(a.cos_sin + (int64_t)pos * D);
+    float c[8], s[8];
+    {
+      const float4 c0 = __ldg(cs + i0 / 4), c1 = __ldg(cs + i0 / 4 + 1);
+      const float4 s0 = __ldg(cs + (D / 2 + i0) / 4), s1 = __ldg(cs + (D / 2 + i0) / 4 + 1);
+      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+      c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+      s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+    }
+    const bool has_kv = row0 + R > Hq;
+    int64_t slot = -1;
+    if (has_kv) slot = __ldg(a.slot_mapping + t);
+    if (has_kv && slot >= a.num_slots && lane == 0 && row0 <= Hq) raise_err(a.err, PKV_DEVERR_SLOT);
+    const bool store_kv = slot >= 0 && slot < a.num_slots;
+    int64_t page = 0, prow = 0;
+    if (store_kv) {
+      page = a.P_shift >= 0 ? (slot >> a.P_shift) : slot / a.P;
+      prow = slot - page * a.P;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int32_t hr = row0 + u * RPS + sub;
+      const bool isq = hr < Hq;
+      float f[8];
+      unpack8(x[u], f);
+      // per-head RMSNorm: sum of squares over the row's LPR lanes
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss = fmaf(f[k], f[k], ss);
+#pragma unroll
+      for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+      if (isq ? a.q_w != nullptr : a.k_w != nullptr) {
+        const float rn = rsqrtf(ss * (1.f / (float)D) + a.eps);
+        float wf[8];
+        unpack8(isq ? qw : kw, wf);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = f[k] * rn * wf[k];
+      }
+      // rotary: lanes [0, HALF) of a row hold dims i < D/2, the rest i + D/2
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float y = __shfl_xor_sync(0xFFFFFFFFu, f[k], HALF);
+        o[k] = lo ? fmaf(f[k], c[k], -y * s[k]) : fmaf(f[k], c[k], y * s[k]);
+      }
+      if (hr >= rows) continue;
+      if (isq) {
+        static_cast<uint4*>(a.q)[((int64_t)t * Hq + hr) * LPR + l] = pack8(o);
+      } else if (store_kv) {
+        const int64_t dst = ((page * a.H_kv + (hr - Hq)) * a.P + prow) * LPR + l;
+        static_cast<uint4*>(a.k_cache)[dst] = pack8(o);
+        static_cast<uint4*>(a.v_cache)[dst] = v[u];
+      }
+    }
   }
 }
 
@@ -191,10 +201,12 @@ cudaError_t launch_rope_table(float* cos_sin, int32_t max_pos, int32_t D, double
 
 cudaError_t launch_kv_append_rope(const RopeAppendArgs& a, int32_t D, cudaStream_t stream,
                                   int num_sms) {
-  const int64_t total = (int64_t)a.T * ((a.q != nullptr ? a.H_q : 0) + a.H_kv) * (D / 8);
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 511) / 512;  // two vectors per thread
-  const int64_t cap = (int64_t)num_sms * 4;
+  const int64_t rows = (a.q != nullptr ? a.H_q : 0) + a.H_kv;
+  const int64_t R = (int64_t)kRopeSteps * (256 / D);
+  const int64_t units = (int64_t)a.T * ((rows + R - 1) / R);  // one warp each
+  if (units == 0) return cudaSuccess;
+  int64_t blocks = (units + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * kRopeBlocksPerSm;  // the resident blocks
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
