@@ -6,14 +6,8 @@
 // back in place, k goes to its page slot, and v is copied to the same slot
 // unchanged (the cache stores post-rotary K: Gemma-4 shared-KV commit).
 //
-// HBM-bound elementwise work.  One thread owns one 16-byte vector (8 bf16)
-// of a q/k row, so a row of head_dim values spans D/8 consecutive lanes of
-// one warp: the sum of squares is a shuffle reduction over those lanes and
-// the rotary partner of a lane's 8 values sits HALF = D/16 lanes away
-// (one xor-shuffle per value).  The thread that owns a k vector also moves
-// the matching v vector.  All arithmetic is fp32 with one rounding to bf16
-// at the end.  The cos/sin table row of a token is read by all its heads and
-// stays in L1/L2.
+// HBM-bound elementwise work (the layout of the work is described at the
+// kernel).  All arithmetic is fp32 with one rounding to bf16 at the end.
 //
 // pkv_rope_table's kernel fills that table in double precision (CUDA's
 // pow and sincos), rounding each entry once to float.
@@ -60,69 +54,99 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cs,
   }
 }
 
-// Work unit: kRopeSteps * (256 / D) consecutive rows of one token's q/k
-// rows (q heads first, then kv heads), processed by one warp.  Lane `lane`
-// always owns the same 16-byte slice l = lane % (D/8) of a row, so the
-// token's position and slot, the lane's cos/sin values and its slice of
-// both norm weights are loaded once per unit and reused for every row.
-// Each step covers 32 / (D/8) rows; the unit's kRopeSteps steps load their
-// rows (and, for kv rows, the v rows) before any is finished.
+// Work unit: R = kRopeSteps * (512 / D) consecutive q/k rows of one token
+// (q heads first, then kv heads), processed by one warp.  A lane owns pair
+// slice j of every row it touches: dims [8j, 8j+8) and [D/2+8j, D/2+8j+8),
+// two 16-byte vectors, so both members of each of its rotary pairs are in
+// its own registers.  A row spans D/16 lanes (the RMSNorm sum of squares is
+// a shuffle reduction over them) and a warp step covers 512/D rows.  The
+// token's position and slot, the lane's cos/sin values and its slices of
+// both norm weights are loaded once per unit; the unit's rows (and, for kv
+// rows, the v rows) are loaded before any is finished.  Arithmetic on pairs
+// of floats uses the f32x2 forms.
 #ifndef PKV_ROPE_STEPS
-#define PKV_ROPE_STEPS 4
+#define PKV_ROPE_STEPS 1
 #endif
 #ifndef PKV_ROPE_MINBLOCKS
-#define PKV_ROPE_MINBLOCKS 2
+#define PKV_ROPE_MINBLOCKS 3
 #endif
 constexpr int kRopeSteps = PKV_ROPE_STEPS;
 constexpr int kRopeBlocksPerSm = PKV_ROPE_MINBLOCKS;
 
+namespace {
+// the 4 bf16 pairs of a 16-byte vector as 4 float pairs
+__device__ __forceinline__ void unpack_pairs(const uint4 v, uint64_t (&p)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    p[k] = f2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint4 pack_pairs(const uint64_t (&p)[4]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float lo, hi;
+    f2_split(p[k], lo, hi);
+    w[k] = pack_bf16(lo, hi);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+}  // namespace
+
 template <int D>
 __global__ void __launch_bounds__(256, kRopeBlocksPerSm) kv_append_rope_kernel(
     const RopeAppendArgs a) {
-  constexpr int LPR = D / 8;           // lanes per row
-  constexpr int HALF = LPR / 2;        // lane distance between rotary partners
-  constexpr int RPS = 32 / LPR;        // rows per warp step
-  constexpr int U = kRopeSteps;        // steps per unit
-  constexpr int R = U * RPS;           // rows per unit
+  constexpr int LPR = D / 16;     // lanes per row
+  constexpr int RPS = 32 / LPR;   // rows per warp step
+  constexpr int U = kRopeSteps;   // steps per unit
+  constexpr int R = U * RPS;      // rows per unit
+  constexpr int VR = D / 8;       // 16-byte vectors per row
+  constexpr int HV = D / 16;      // ... per half row
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const int l = lane & (LPR - 1);      // the lane's slice of a row
-  const int sub = lane / LPR;          // the lane's row within a step
-  const bool lo = l < HALF;
-  const int i0 = (l & (HALF - 1)) * 8;  // first rotary pair of the slice
+  const int j = lane & (LPR - 1);  // the lane's pair slice
+  const int sub = lane / LPR;      // the lane's row within a step
   const int32_t Hq = a.q != nullptr ? a.H_q : 0;
   const int32_t rows = Hq + a.H_kv;
   const int32_t units_per_tok = (rows + R - 1) / R;
-  const int64_t units = (int64_t)a.T * units_per_tok;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const uint4* q = static_cast<uint4*>(a.q);
+  const int32_t units = a.T * units_per_tok;  // host-checked to fit
+  const int32_t nwarps = (int32_t)((gridDim.x * blockDim.x) >> 5);
+  uint4* q = static_cast<uint4*>(a.q);
   const uint4* k_new = static_cast<const uint4*>(a.k_new);
   const uint4* v_new = static_cast<const uint4*>(a.v_new);
+  uint4* k_cache = static_cast<uint4*>(a.k_cache);
+  uint4* v_cache = static_cast<uint4*>(a.v_cache);
   // the lane's slices of the two norm weights, kept packed (bf16)
-  const uint4 qw = a.q_w ? __ldg(static_cast<const uint4*>(a.q_w) + l) : make_uint4(0u, 0u, 0u, 0u);
-  const uint4 kw = a.k_w ? __ldg(static_cast<const uint4*>(a.k_w) + l) : make_uint4(0u, 0u, 0u, 0u);
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  const uint4* qwp = static_cast<const uint4*>(a.q_w);
+  const uint4* kwp = static_cast<const uint4*>(a.k_w);
+  const uint4 qwl = qwp ? __ldg(qwp + j) : z, qwh = qwp ? __ldg(qwp + HV + j) : z;
+  const uint4 kwl = kwp ? __ldg(kwp + j) : z, kwh = kwp ? __ldg(kwp + HV + j) : z;
 
-  for (int64_t unit = (((int64_t)blockIdx.x * blockDim.x) >> 5) + (threadIdx.x >> 5);
-       unit < units; unit += nwarps) {  // warp-uniform
-    const int32_t t = (int32_t)(unit / units_per_tok);
-    const int32_t row0 = (int32_t)(unit - (int64_t)t * units_per_tok) * R;
+  for (int32_t unit = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); unit < units;
+       unit += nwarps) {  // warp-uniform
+    const int32_t t = unit / units_per_tok;
+    const int32_t row0 = (unit - t * units_per_tok) * R;
     const int32_t pos = __ldg(a.positions + t);
     const bool live = pos >= 0 && pos < a.max_pos;
     // the rows: loads first
-    uint4 x[U], v[U];
+    uint4 xl[U], xh[U], vl[U], vh[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int32_t hr = row0 + u * RPS + sub;
-      x[u] = make_uint4(0u, 0u, 0u, 0u);
-      v[u] = x[u];
+      xl[u] = xh[u] = vl[u] = vh[u] = z;
       if (live && hr < rows) {
         if (hr < Hq) {
-          x[u] = q[((int64_t)t * Hq + hr) * LPR + l];
+          const int64_t b = ((int64_t)t * Hq + hr) * VR + j;
+          xl[u] = q[b];
+          xh[u] = q[b + HV];
         } else {
-          const int64_t src = ((int64_t)t * a.H_kv + (hr - Hq)) * LPR + l;
-          x[u] = __ldg(k_new + src);
-          v[u] = __ldg(v_new + src);
+          const int64_t b = ((int64_t)t * a.H_kv + (hr - Hq)) * VR + j;
+          xl[u] = __ldg(k_new + b);
+          xh[u] = __ldg(k_new + b + HV);
+          vl[u] = __ldg(v_new + b);
+          vh[u] = __ldg(v_new + b + HV);
         }
       }
     }
@@ -130,20 +154,21 @@ __global__ void __launch_bounds__(256, kRopeBlocksPerSm) kv_append_rope_kernel(
       if (row0 == 0 && lane == 0) raise_err(a.err, PKV_DEVERR_POS);
       continue;
     }
-    const float4* cs = reinterpret_cast<const float4*>(a.cos_sin + (int64_t)pos * D);
-    float c[8], s[8];
+    uint64_t c[4], sp[4], sn[4];  // cos, sin and -sin of the lane's 8 pairs
     {
-      const float4 c0 = __ldg(cs + i0 / 4), c1 = __ldg(cs + i0 / 4 + 1);
-      const float4 s0 = __ldg(cs + (D / 2 + i0) / 4), s1 = __ldg(cs + (D / 2 + i0) / 4 + 1);
-      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
-      c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-      s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+      const float4* cs = reinterpret_cast<const float4*>(a.cos_sin + (int64_t)pos * D);
+      const float4 c0 = __ldg(cs + 2 * j), c1 = __ldg(cs + 2 * j + 1);
+      const float4 s0 = __ldg(cs + D / 8 + 2 * j), s1 = __ldg(cs + D / 8 + 2 * j + 1);
+      c[0] = f2(c0.x, c0.y); c[1] = f2(c0.z, c0.w); c[2] = f2(c1.x, c1.y); c[3] = f2(c1.z, c1.w);
+      sp[0] = f2(s0.x, s0.y); sp[1] = f2(s0.z, s0.w); sp[2] = f2(s1.x, s1.y); sp[3] = f2(s1.z, s1.w);
+      sn[0] = f2(-s0.x, -s0.y); sn[1] = f2(-s0.z, -s0.w);
+      sn[2] = f2(-s1.x, -s1.y); sn[3] = f2(-s1.z, -s1.w);
     }
     const bool has_kv = row0 + R > Hq;
     int64_t slot = -1;
     if (has_kv) slot = __ldg(a.slot_mapping + t);
-    if (has_kv && slot >= a.num_slots && lane == 0 && row0 <= Hq) raise_err(a.err, PKV_DEVERR_SLOT);
+    if (has_kv && slot >= a.num_slots && lane == 0 && row0 <= Hq)
+      raise_err(a.err, PKV_DEVERR_SLOT);
     const bool store_kv = slot >= 0 && slot < a.num_slots;
     int64_t page = 0, prow = 0;
     if (store_kv) {
@@ -154,35 +179,50 @@ __global__ void __launch_bounds__(256, kRopeBlocksPerSm) kv_append_rope_kernel(
     for (int u = 0; u < U; ++u) {
       const int32_t hr = row0 + u * RPS + sub;
       const bool isq = hr < Hq;
-      float f[8];
-      unpack8(x[u], f);
+      uint64_t fl[4], fh[4];
+      unpack_pairs(xl[u], fl);
+      unpack_pairs(xh[u], fh);
       // per-head RMSNorm: sum of squares over the row's LPR lanes
-      float ss = 0.f;
+      uint64_t acc = f2_mul(fl[0], fl[0]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ss = fmaf(f[k], f[k], ss);
+      for (int k = 1; k < 4; ++k) acc = f2_fma(fl[k], fl[k], acc);
 #pragma unroll
-      for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-      if (isq ? a.q_w != nullptr : a.k_w != nullptr) {
+      for (int k = 0; k < 4; ++k) acc = f2_fma(fh[k], fh[k], acc);
+      float s0, s1;
+      f2_split(acc, s0, s1);
+      float ss = s0 + s1;
+#pragma unroll
+      for (int off = LPR / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+      if (isq ? qwp != nullptr : kwp != nullptr) {
         const float rn = rsqrtf(ss * (1.f / (float)D) + a.eps);
-        float wf[8];
-        unpack8(isq ? qw : kw, wf);
+        const uint64_t rn2 = f2(rn, rn);
+        uint64_t wl[4], wh[4];
+        unpack_pairs(isq ? qwl : kwl, wl);
+        unpack_pairs(isq ? qwh : kwh, wh);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = f[k] * rn * wf[k];
+        for (int k = 0; k < 4; ++k) {
+          fl[k] = f2_mul(fl[k], f2_mul(rn2, wl[k]));
+          fh[k] = f2_mul(fh[k], f2_mul(rn2, wh[k]));
+        }
       }
-      // rotary: lanes [0, HALF) of a row hold dims i < D/2, the rest i + D/2
-      float o[8];
+      // rotary: (lo, hi) -> (lo c - hi s, hi c + lo s)
+      uint64_t ol[4], oh[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float y = __shfl_xor_sync(0xFFFFFFFFu, f[k], HALF);
-        o[k] = lo ? fmaf(f[k], c[k], -y * s[k]) : fmaf(f[k], c[k], y * s[k]);
+      for (int k = 0; k < 4; ++k) {
+        ol[k] = f2_fma(fl[k], c[k], f2_mul(fh[k], sn[k]));
+        oh[k] = f2_fma(fh[k], c[k], f2_mul(fl[k], sp[k]));
       }
       if (hr >= rows) continue;
       if (isq) {
-        static_cast<uint4*>(a.q)[((int64_t)t * Hq + hr) * LPR + l] = pack8(o);
+        const int64_t b = ((int64_t)t * Hq + hr) * VR + j;
+        q[b] = pack_pairs(ol);
+        q[b + HV] = pack_pairs(oh);
       } else if (store_kv) {
-        const int64_t dst = ((page * a.H_kv + (hr - Hq)) * a.P + prow) * LPR + l;
-        static_cast<uint4*>(a.k_cache)[dst] = pack8(o);
-        static_cast<uint4*>(a.v_cache)[dst] = v[u];
+        const int64_t b = ((page * a.H_kv + (hr - Hq)) * a.P + prow) * VR + j;
+        k_cache[b] = pack_pairs(ol);
+        k_cache[b + HV] = pack_pairs(oh);
+        v_cache[b] = vl[u];
+        v_cache[b + HV] = vh[u];
       }
     }
   }
@@ -202,7 +242,7 @@ cudaError_t launch_rope_table(float* cos_sin, int32_t max_pos, int32_t D, double
 cudaError_t launch_kv_append_rope(const RopeAppendArgs& a, int32_t D, cudaStream_t stream,
                                   int num_sms) {
   const int64_t rows = (a.q != nullptr ? a.H_q : 0) + a.H_kv;
-  const int64_t R = (int64_t)kRopeSteps * (256 / D);
+  const int64_t R = (int64_t)kRopeSteps * (512 / D);
   const int64_t units = (int64_t)a.T * ((rows + R - 1) / R);  // one warp each
   if (units == 0) return cudaSuccess;
   int64_t blocks = (units + 7) / 8;
