@@ -16,27 +16,6 @@
 
 namespace pkv {
 
-namespace {
-
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    f[2 * k] = __uint_as_float(w[k] << 16);
-    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  uint4 v;
-  v.x = pack_bf16(f[0], f[1]);
-  v.y = pack_bf16(f[2], f[3]);
-  v.z = pack_bf16(f[4], f[5]);
-  v.w = pack_bf16(f[6], f[7]);
-  return v;
-}
-
-}  // namespace
 
 __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cs, int32_t max_pos,
                                                          int32_t D, double theta) {
