@@ -51,6 +51,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(vals, device):
+    """Each value's maximum over all ranks (the slowest replica sets the
+    job's time); the values themselves at world size 1."""
+    ws, _, _ = dist_env()
+    if ws <= 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_gb_s(ws: int, bytes_per_rank: int, step_ms: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed in one step over
+    the (max-over-ranks) step time."""
+    return ws * bytes_per_rank / (step_ms * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -396,14 +415,10 @@ def run_ours(args):
     step_ms = float(np.mean([sum(p) for p in per_step]))
     dec_ms = float(np.mean([p[1] for p in per]))
     app_ms = float(np.mean([p[0] for p in per]))
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms, dec_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms = float(t[0]), float(t[1])
+    step_ms, dec_ms = max_over_ranks([step_ms, dec_ms], device)
     dbytes = decode_bytes(step)
     abytes = append_bytes(step, step.n_new_tokens)
-    value = ws * (dbytes + abytes) / (step_ms * 1e-3) / 1e9
+    value = job_gb_s(ws, dbytes + abytes, step_ms)
     dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------
