@@ -176,7 +176,7 @@ def test_append_rope_bad_slot_flags_and_skips(pkv):
 def test_mixed_step_with_fused_rope_end_to_end(pkv):
     """The mixed continuous-batching step (8 prefill chunks + 120 decode rows,
     H 32/8/128, page 16) with the input transform fused into the append:
-    all 4728 new tokens' q and k normalised and rotated (theta 1e6), then
+    all 5645 new tokens' q and k normalised and rotated (theta 1e6), then
     varlen prefill and decode read the rotated q and the pool."""
     import torch
     step = wl.mixed_step()
