@@ -141,3 +141,33 @@ def test_product_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.replace("oracles", ""), f
+
+
+def _declared_signatures():
+    """name -> list of parameter C types, from include/pkv.h."""
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    sigs = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;",
+                         src, flags=re.M):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        sigs[m.group(1)] = params
+    return sigs
+
+
+def _ctype_of(param: str):
+    if "*" in param:
+        return ctypes.c_void_p
+    base = param.rsplit(" ", 1)[0].replace("const ", "").strip()
+    return {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "float": ctypes.c_float,
+            "double": ctypes.c_double, "size_t": ctypes.c_size_t}[base]
+
+
+def test_binding_signatures_match_the_header():
+    # every ctypes prototype in the binding has the header's arity and types
+    import paged_kv_attention_11_gb300._binding as b
+    sigs = _declared_signatures()
+    assert set(b._SIGS) == set(sigs), set(b._SIGS) ^ set(sigs)
+    for name, args in b._SIGS.items():
+        want = [_ctype_of(p) for p in sigs[name]]
+        assert args == want, (name, args, want)
