@@ -82,3 +82,9 @@ def test_append_rope_bytes_counts_every_tensor_once():
     }
     assert bench.append_rope_bytes(step, n) == sum(tensors.values())
     assert len(step.all_positions) == n
+
+
+def test_multicore_oracle_baseline_runs():
+    # spawned workers, two of them, one timed step
+    out = bench.cpu_baseline_multicore(steps=1, max_workers=2)
+    assert out["cores"] == 2 and out["kind"] == "oracle" and out["value"] > 0
