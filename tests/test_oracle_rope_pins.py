@@ -196,3 +196,16 @@ def test_q_rows_of_invalid_positions_untouched():
     assert np.array_equal(out[[0, 3]], q[[0, 3]])
     assert np.array_equal(out[[1, 2]], oracle.norm_rope_rows(q[[1, 2]], pos[[1, 2]], 1e6,
                                                              None, 1e-6))
+
+
+def test_norm_precedes_rotation():
+    # The order is only visible through a non-uniform weight (a rotation
+    # keeps the mean square).  x = e0, w = [2, 1, 1, 1], eps 0, D 4:
+    # norm first gives [4, 0, 0, 0] (rms of e0 is 1/2), then pair (0, 2)
+    # turns by pos -> [4 cos p, 0, 4 sin p, 0]; rotating first would give
+    # [4 cos p, 0, 2 sin p, 0].
+    x = wl.f32_to_bf16_bits(np.array([[[1.0, 0.0, 0.0, 0.0]]], np.float32))
+    w = wl.f32_to_bf16_bits(np.array([2.0, 1.0, 1.0, 1.0], np.float32))
+    got = f64(oracle.norm_rope_rows(x, np.array([3]), 1e4, w, 0.0))[0, 0]
+    want = np.array([4 * math.cos(3.0), 0.0, 4 * math.sin(3.0), 0.0])
+    np.testing.assert_allclose(got, want, rtol=2.0 ** -8, atol=0)
