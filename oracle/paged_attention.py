@@ -19,7 +19,7 @@ Sources, by page and section:
   sliding mask is causal AND q_pos - kv_pos < window (strict less-than);
   full attention is plain causal.
 
-Readings where the pages are silent (each documented in the design doc):
+Readings where the pages are silent:
 
 * A decode step attends the new token: append first, then the query at
   position len-1 attends keys 0..len-1.

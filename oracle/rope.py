@@ -16,7 +16,7 @@ Sources, by page and section:
   README's Gemma-4 paragraph: the rotary (cos, sin) tables are precomputed
   per position and per regime, rope_theta = 1e6 for full attention.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings where the pages are silent:
 
 * Rotary convention: rotate-half.  For i < D/2, dims i and i + D/2 form a
   pair rotated counter-clockwise by the angle pos * theta^(-2i/D), i.e.
