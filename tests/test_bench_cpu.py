@@ -88,3 +88,14 @@ def test_multicore_oracle_baseline_runs():
     # spawned workers, two of them, one timed step
     out = bench.cpu_baseline_multicore(steps=1, max_workers=2)
     assert out["cores"] == 2 and out["kind"] == "oracle" and out["value"] > 0
+
+
+def test_positions_agree_with_slots():
+    # the position of each new token, looked up through its block table,
+    # must land on the slot the append writes
+    for step in (wl.mixed_step(), wl.tiny(), wl.sliding()):
+        pos = step.all_positions.astype(np.int64)
+        tables = ([step.pre_block_table[c] for c in range(step.Bp) for _ in range(int(step.pre_qlen[c]))]
+                  + [step.dec_block_table[b] for b in range(step.Bd)])
+        slots = np.array([int(t[p // step.P]) * step.P + p % step.P for t, p in zip(tables, pos)])
+        assert np.array_equal(slots, step.all_slots)
