@@ -41,6 +41,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # the qwen3_decode workload (ncu --set full capture on a GB300, 316.78 + 4.15 MB,
 # 24-stage ring); valid for that workload and this decode kernel only.
 DECODE_TRAFFIC_BYTES = 320_930_048
+# the same for one varlen_fwd_kernel<128,2,128,1,3,2> launch on the mixed step
+# (78.50 + 9.11 MB) and one kv_append_rope_kernel<128> launch on the mixed
+# step with both norms (70.27 + 13.77 MB; 3 blocks per SM, 1 step per unit)
+VARLEN_MIXED_TRAFFIC_BYTES = 87_604_224
+APPEND_ROPE_MIXED_TRAFFIC_BYTES = 84_039_936
 
 
 # ------------------------------------------------------------------ helpers
@@ -544,7 +549,7 @@ def run_mixed(args, device, stream, flush, rank):
                 "bound": "hbm", "achieved": round(rb / (rph[0] * 1e-3) / 1e9, 2),
                 "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(rb / (rph[0] * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": src,
-                "algorithmic_bytes": int(rb)},
+                "algorithmic_bytes": int(rb), "traffic": APPEND_ROPE_MIXED_TRAFFIC_BYTES},
             "note": "q and k RMSNorm + rotary (theta 1e6) over all new tokens fused into the "
                     "append; q transformed in place"}
     except Exception as e:
@@ -558,7 +563,8 @@ def run_mixed(args, device, stream, flush, rank):
             "varlen_roofline": {"bound": "tensor", "achieved": round(fl / (ph[1] * 1e-3) / 1e12, 2),
                                 "peak": tf_peak, "unit": "TFLOP/s",
                                 "frac": round(fl / (ph[1] * 1e-3) / 1e12 / tf_peak, 4),
-                                "peak_source": src, "algorithmic_flops": fl},
+                                "peak_source": src, "algorithmic_flops": fl,
+                                "traffic": VARLEN_MIXED_TRAFFIC_BYTES},
             "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2),
             "append_gb_s": round(append_bytes(step, tokens) / (ph[0] * 1e-3) / 1e9, 2),
             "append_bytes": int(append_bytes(step, tokens)),
