@@ -37,15 +37,35 @@ METRIC = "paged decode-attn achieved HBM GB/s (% of 8 TB/s); mixed-step tokens/s
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode_split_kernel launch on
-# the qwen3_decode workload (ncu --set full capture on a GB300, 316.78 + 4.15 MB,
-# 24-stage ring); valid for that workload and this decode kernel only.
-DECODE_TRAFFIC_BYTES = 320_930_048
-# the same for one varlen_fwd_kernel<128,2,128,1,3,2> launch on the mixed step
-# (78.50 + 9.11 MB) and one kv_append_rope_kernel<128> launch on the mixed
-# step with both norms (70.27 + 13.77 MB; 3 blocks per SM, 1 step per unit)
-VARLEN_MIXED_TRAFFIC_BYTES = 87_604_224
-APPEND_ROPE_MIXED_TRAFFIC_BYTES = 84_039_936
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
+# from an ncu capture on a GB300, with the SHA-256 prefix of the kernel's
+# source file at capture time.  A value is reported only while the source
+# still has that hash; once the kernel changes the field is null until a new
+# capture replaces the entry.
+#   decode_qwen3: decode_split_kernel<128,4,24,1> on the qwen3_decode step
+#                 (316.78 + 4.15 MB; profiles/decode_split_kernel_qwen3_decode.md)
+#   varlen_mixed: varlen_fwd_kernel<128,2,128,1,3,2> on the mixed step
+#                 (78.50 + 9.11 MB; profiles/varlen_fwd_kernel_mixed_step.md)
+#   append_rope_mixed: kv_append_rope_kernel<128> on the mixed step, both
+#                 norms (70.27 + 13.77 MB; profiles/kv_append_rope_kernel_mixed_step.md)
+TRAFFIC = {
+    "decode_qwen3": (320_930_048, "decode.cu", "24056982da403059"),
+    "varlen_mixed": (87_604_224, "varlen.cu", "8c512d957a881826"),
+    "append_rope_mixed": (84_039_936, "rope_append.cu", "e68e8d036bcc4835"),
+}
+
+
+def traffic_bytes(key: str):
+    """The captured traffic of TRAFFIC[key], or None when the kernel source
+    has changed since the capture."""
+    import hashlib
+    nbytes, src, sha = TRAFFIC[key]
+    path = os.path.join(ROOT, "paged_kv_attention_11_gb300", "csrc", src)
+    try:
+        cur = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if cur == sha else None
 
 
 # ------------------------------------------------------------------ helpers
@@ -452,7 +472,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (split-KV with fused last-arriver merge)",
                      "achieved": round(dec_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm_peak, 4), "peak_source": peak_src,
-                     "algorithmic_bytes": dbytes, "traffic": DECODE_TRAFFIC_BYTES or None},
+                     "algorithmic_bytes": dbytes, "traffic": traffic_bytes("decode_qwen3")},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,  # append + decode (split-KV with fused merge) per step
         "clocks": clocks.summary(),
@@ -549,7 +569,8 @@ def run_mixed(args, device, stream, flush, rank):
                 "bound": "hbm", "achieved": round(rb / (rph[0] * 1e-3) / 1e9, 2),
                 "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(rb / (rph[0] * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": src,
-                "algorithmic_bytes": int(rb), "traffic": APPEND_ROPE_MIXED_TRAFFIC_BYTES},
+                "algorithmic_bytes": int(rb),
+                "traffic": traffic_bytes("append_rope_mixed")},
             "note": "q and k RMSNorm + rotary (theta 1e6) over all new tokens fused into the "
                     "append; q transformed in place"}
     except Exception as e:
@@ -564,7 +585,7 @@ def run_mixed(args, device, stream, flush, rank):
                                 "peak": tf_peak, "unit": "TFLOP/s",
                                 "frac": round(fl / (ph[1] * 1e-3) / 1e12 / tf_peak, 4),
                                 "peak_source": src, "algorithmic_flops": fl,
-                                "traffic": VARLEN_MIXED_TRAFFIC_BYTES},
+                                "traffic": traffic_bytes("varlen_mixed")},
             "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2),
             "append_gb_s": round(append_bytes(step, tokens) / (ph[0] * 1e-3) / 1e9, 2),
             "append_bytes": int(append_bytes(step, tokens)),

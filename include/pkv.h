@@ -193,13 +193,17 @@ pkv_status paged_attn_varlen(void* out, const void* q,
  * paged_attn_decode_workspace_size() exceeds 8 MiB is rejected with
  * PKV_ERR_UNSUPPORTED (message in pkv_last_cuda_error()).
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any
- * stream capture.  Every call clears the array's arrival counters on
- * `stream` before its kernel runs.  All calls share the one array: calls
- * whose work may overlap on the GPU (different streams or host threads)
- * race and must be serialised by the caller.  No allocation and no free
- * is made.
+ * CUDA places the array on a device when the library's module holding it
+ * is loaded there: under the default lazy module loading that is the
+ * first call of this entry point on the device, which also looks up the
+ * array's device address (once per device and CUDA context, with that
+ * device current).  Make that first call before handing the remaining free
+ * HBM to a page pool, and before any stream capture.  All host-side checks
+ * run first: a rejected call enqueues nothing.  Every accepted call clears
+ * the array's arrival counters on `stream` before its kernel runs.  All
+ * calls share the one array: calls whose work may overlap on the GPU
+ * (different streams or host threads) race and must be serialised by the
+ * caller.  No allocation and no free is made.
  */
 pkv_status paged_attn_decode_static(void* out, const void* q,
                                     const void* k_cache, const void* v_cache,

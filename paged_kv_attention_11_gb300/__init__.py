@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     DEVERR_POS,
     DEVERR_SLOT,
     DEVERR_TIMEOUT,
+    decode_workspace,
     decode_workspace_size,
     lib,
     lib_path,

@@ -112,21 +112,52 @@ def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_
     return int(lib().paged_attn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim))
 
 
+# Decode workspaces kept by the binding for callers that pass none: one per
+# (device, stream, head shape), zero-filled once and grown when a larger batch
+# needs more.  The kernel leaves a workspace zero-filled after every call, so
+# calls in one stream's order may share it; calls on different streams get
+# different ones.
+_WORKSPACES = {}
+
+
+def decode_workspace(device: torch.device, stream_handle: int, batch: int, num_q_heads: int,
+                     num_kv_heads: int, head_dim: int) -> torch.Tensor:
+    """The binding's cached decode workspace for this stream and shape: it
+    allocates (and zero-fills) only when none is cached yet or the cached
+    one is too small, so a CUDA-graph capture must be preceded by one call
+    of the same shape on the capturing stream (or pass ``workspace``)."""
+    need = max(decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim), 256)
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           int(stream_handle), num_q_heads, num_kv_heads, head_dim)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        # the zero fill runs on torch's current stream: order the kernel's
+        # stream after it
+        cur = torch.cuda.current_stream(device)
+        if int(stream_handle) != cur.cuda_stream:
+            torch.cuda.ExternalStream(int(stream_handle), device=device).wait_stream(cur)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                       v_cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
                       max_seq_len: int, scale: float, window: int = 0,
                       workspace: Optional[torch.Tensor] = None,
                       err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """out/q [B, H_q, D]; block_table [B, max_blocks] int32; seq_lens [B] int32."""
+    """out/q [B, H_q, D]; block_table [B, max_blocks] int32; seq_lens [B] int32.
+    Without ``workspace`` the binding's cached one for this stream is used
+    (``decode_workspace``): it allocates only on the first call of a stream
+    and shape, or when the batch outgrows it."""
     for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
         _bf16(t, n)
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise ValueError("block_table and seq_lens must be int32")
     B, H_q, D = q.shape
     num_pages, H_kv, P, _ = k_cache.shape
-    need = decode_workspace_size(B, H_q, H_kv, D)
     if workspace is None:
-        workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=q.device)
+        workspace = decode_workspace(q.device, _stream(stream), B, H_q, H_kv, D)
     _check("paged_attn_decode", lib().paged_attn_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),

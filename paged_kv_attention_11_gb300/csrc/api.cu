@@ -46,6 +46,27 @@ bool supported_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
 
 namespace pkv {
 void set_last_error(const std::string& msg) { g_last_cuda_error = msg; }
+
+pkv_status decode_check_args(const void* out, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_table,
+                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t page_size, int64_t num_pages, int32_t max_seq_len,
+                             float scale) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+      num_pages <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
+    return PKV_ERR_INVALID;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+  if (!(scale == scale)) return PKV_ERR_INVALID;  // NaN
+  if (!supported_head_dim(head_dim) || page_size % 16 != 0 || num_q_heads / num_kv_heads > 8 ||
+      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 4096)
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return PKV_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID;
+  return PKV_OK;
+}
 }  // namespace pkv
 
 extern "C" {
@@ -98,20 +119,12 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
                              int64_t num_pages, int32_t max_seq_len, float scale, int32_t window,
                              void* workspace, size_t workspace_bytes, int32_t* err_flag,
                              void* stream) {
-  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
-      num_pages <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
-    return PKV_ERR_INVALID;
-  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
-  if (!(scale == scale)) return PKV_ERR_INVALID;  // NaN
-  if (!supported_head_dim(head_dim) || page_size % 16 != 0 || num_q_heads / num_kv_heads > 8 ||
-      num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 4096)
-    return PKV_ERR_UNSUPPORTED;
-  if (batch == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens || !workspace)
-    return PKV_ERR_INVALID;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return PKV_ERR_INVALID;
+  const pkv_status chk =
+      pkv::decode_check_args(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                             batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                             max_seq_len, scale);
+  if (chk != PKV_OK || batch == 0) return chk;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_INVALID;
   int sms = 0;
   if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
   if (workspace_bytes <

@@ -9,10 +9,22 @@
 
 #include <string>
 
+#include "../../include/pkv.h"
+
 namespace pkv {
 
 // Message returned by pkv_last_cuda_error() on this host thread.
 void set_last_error(const std::string& msg);
+
+// Host-side argument checks of paged_attn_decode, everything but the
+// workspace (PKV_OK, PKV_ERR_INVALID or PKV_ERR_UNSUPPORTED; nothing is
+// enqueued).
+pkv_status decode_check_args(const void* out, const void* q, const void* k_cache,
+                             const void* v_cache,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                             int64_t num_pages, int32_t max_seq_len, float scale);
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t num_tokens, int32_t H_kv,

@@ -47,6 +47,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "exp2_math.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
 
@@ -97,45 +98,6 @@ struct VarlenSmem {
     return 1024 + (need > 116 * 1024 ? need : 116 * 1024);
   }
 };
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// 2^x for a pair, on the FMA/ALU pipes, for x <= 8 (the softmax's
-// stale-max bound): x = n + f with n = round(x) (added to the exponent
-// field) and f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise
-// relative error on that interval (max relative error 2.2e-4, below bf16
-// resolution of P).  x is clamped at -125 (a masked, -inf score gives
-// 2^-125 * 2^f instead of 0: below 2^-100 of the row sum, which holds at
-// least one term >= 2^-8).
-__device__ __forceinline__ uint64_t poly_exp2x2(uint64_t x) {
-  float x0, x1;
-  f2_split(x, x0, x1);
-  const uint64_t xc = f2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const uint64_t kMagic = f2(12582912.f, 12582912.f);  // 1.5 * 2^23: rounds to an integer
-  const uint64_t tt = f2_add(xc, kMagic);
-  const uint64_t f = f2_sub(xc, f2_sub(tt, kMagic));
-  uint64_t p = f2_fma(f2(0.05286737531423569f, 0.05286737531423569f), f,
-                      f2(0.24215202033519745f, 0.24215202033519745f));
-  p = f2_fma(p, f, f2(0.6935867667198181f, 0.6935867667198181f));
-  p = f2_fma(p, f, f2(0.9999627470970154f, 0.9999627470970154f));
-  float t0, t1, p0, p1;
-  f2_split(tt, t0, t1);
-  f2_split(p, p0, p1);
-  const int n0 = __float_as_int(t0) - 0x4B400000;
-  const int n1 = __float_as_int(t1) - 0x4B400000;
-  return f2(__int_as_float(__float_as_int(p0) + (n0 << 23)),
-            __int_as_float(__float_as_int(p1) + (n1 << 23)));
-}
 
 // Item geometry shared by every role of the CTA.
 struct Item {

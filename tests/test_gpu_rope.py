@@ -218,14 +218,14 @@ def test_mixed_step_with_fused_rope_end_to_end(pkv):
                               torch.as_tensor(slots % P, device="cuda"), :]
     check_rows(gk.cpu().numpy().view(np.uint16), vals.k_new, pos, theta, kw, eps, "k rows")
     assert np.array_equal(bf16_dev_to_bits(vc), hv), "V pool differs"
-    # attention over the GPU's own rotated rows (so the comparison isolates
-    # the attention kernels): the oracle reads the pool and q as the GPU
-    # left them
-    gk_pool = bf16_dev_to_bits(kc)
-    want_pre = oracle.paged_varlen(gq[:step.total_q], gk_pool, hv, step.cu_seq_lens_q,
+    # attention end to end from the same host inputs: the oracle's own
+    # transformed q (q_norm_rope) and pool (kv_append_rope) drive its
+    # varlen and decode, and the GPU's outputs are compared with those
+    hq = oracle.q_norm_rope(q_all, pos, theta, qw, eps, max_pos)
+    want_pre = oracle.paged_varlen(hq[:step.total_q], hk, hv, step.cu_seq_lens_q,
                                    step.cu_seq_lens_k, step.pre_block_table, step.scale,
                                    True, step.window)
     assert_close_attn(bf16_dev_to_f64(out_pre), want_pre, "varlen after fused rope")
-    want_dec = oracle.paged_decode(gq[step.total_q:], gk_pool, hv, step.dec_block_table,
+    want_dec = oracle.paged_decode(hq[step.total_q:], hk, hv, step.dec_block_table,
                                    step.dec_seq_lens, step.scale, step.window)
     assert_close_attn(bf16_dev_to_f64(out_dec), want_dec, "decode after fused rope")

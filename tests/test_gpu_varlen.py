@@ -103,18 +103,26 @@ def test_varlen_empty_chunks_and_single_rows(pkv):
 
 
 def test_varlen_q1_equals_decode(pkv):
-    """A chunk of one query is the decode step of the same sequence."""
+    """A chunk of one query is the decode step of the same sequence: both
+    kernels match the oracle's varlen result and its decode result (the two
+    oracle results are the same rows), and each other."""
     import torch
     prefix = [63, 500, 2000]
     step = _prefill_step(11, 32, 8, 128, 16, prefix, [1, 1, 1])
     vals = wl.fill_values(step, 11)
-    got, _, (kc, vc) = _varlen(pkv, step, vals)
+    got, want, (kc, vc) = _varlen(pkv, step, vals)
+    assert_close_attn(got, want, "q1 varlen vs oracle")
     out = torch.empty_like(to_dev_bf16(vals.q_pre[0]))
     lens = (step.pre_prefix + step.pre_qlen).astype(np.int32)
     pkv.paged_attn_decode(out, to_dev_bf16(vals.q_pre[0]), kc, vc, to_dev(step.pre_block_table),
                           to_dev(lens), int(lens.max()), step.scale, 0)
     torch.cuda.synchronize()
-    assert_close_attn(got, bf16_dev_to_f64(out), "q1 vs decode")
+    hk, hv = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, step.all_slots)
+    want_dec = oracle.paged_decode(vals.q_pre[0], hk, hv, step.pre_block_table, lens, step.scale)
+    assert np.array_equal(want_dec, want), "oracle: decode and q_len=1 varlen rows differ"
+    got_dec = bf16_dev_to_f64(out)
+    assert_close_attn(got_dec, want_dec, "q1 decode vs oracle")
+    assert_close_attn(got, got_dec, "q1 varlen vs decode")
 
 
 def test_varlen_sharp_scores_rescale_path(pkv):
