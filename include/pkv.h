@@ -83,6 +83,8 @@ typedef enum {
  *
  * Rows are copied bit-exactly.  Slots must be distinct within one call
  * (duplicates race; the winner is unspecified).  num_tokens == 0 is a no-op.
+ * num_tokens * num_kv_heads * head_dim / 8 must be below 2^31 (else
+ * PKV_ERR_UNSUPPORTED).
  */
 pkv_status paged_kv_append(const void* k_new, const void* v_new,
                            void* k_cache, void* v_cache,

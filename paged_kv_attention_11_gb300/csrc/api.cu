@@ -96,6 +96,8 @@ pkv_status paged_kv_append(const void* k_new, const void* v_new, void* k_cache, 
     return PKV_ERR_INVALID;
   int sms = 0;
   if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  if ((int64_t)num_tokens * num_kv_heads * (head_dim / 8) >= (int64_t(1) << 31))
+    return PKV_ERR_UNSUPPORTED;
   cudaError_t e = pkv::launch_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
                                         num_kv_heads, head_dim, page_size, num_pages, err_flag,
                                         static_cast<cudaStream_t>(stream), sms);

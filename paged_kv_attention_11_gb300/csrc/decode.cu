@@ -45,6 +45,10 @@ constexpr int kTile = 16;  // keys per pipeline stage
 constexpr int kGP = 8;     // GQA group padded to the mma N dimension
 constexpr int kNRec = 4;   // piece records in flight
 constexpr int kMergeLse = 128;  // (piece, head) log-sum-exps staged in smem for a merge
+// Shortest chunk a segment is cut into (tiles).  Small batches (a few long
+// windowed segments) then still spread over every SM instead of one segment
+// per CTA; large batches cut at half a CTA's share, far above this floor.
+constexpr int kMinChunkTiles = 4;
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -198,7 +202,8 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
 
   // ---- work items (every CTA computes the same list, in smem) ----
   // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
-  // than S_max = max(32, W / (2N)) tiles is cut into nch_b equal chunks.
+  // than S_max = max(kMinChunkTiles, W / (2N)) tiles is cut into nch_b
+  // equal chunks.
   {
     int local = 0;
     for (int b = tid; b < B; b += NT) {
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       for (int w = 0; w < NT / 32; ++w) tot += scan_tmp[w];
       const int64_t W = tot * a.H_kv;
       const int64_t half_share = (W + 2 * (int64_t)gridDim.x - 1) / (2 * (int64_t)gridDim.x);
-      s_misc[0] = (int)(half_share > 32 ? half_share : 32);  // S_max
+      s_misc[0] = (int)(half_share > kMinChunkTiles ? half_share : kMinChunkTiles);  // S_max
     }
     __syncthreads();
   }
