@@ -298,6 +298,19 @@ class DeviceStep:
                                    s.window, workspace=self.ws, err_flag=self.err,
                                    stream=stream)
 
+    def decode_shared_prefix(self, stream):
+        """The same decode through the shared-prefix (cascade) entry point."""
+        import torch
+        s = self.step
+        if not hasattr(self, "ws_pfx"):
+            need = self.pkv.shared_prefix_workspace_size(s.Bd, s.H_q, s.H_kv, s.D)
+            self.ws_pfx = torch.zeros(need, dtype=torch.uint8, device=self.k_cache.device)
+            self.prefix_lens = torch.from_numpy(s.prefix_lens).to(self.k_cache.device)
+        self.pkv.paged_attn_decode_shared_prefix(
+            self.out_dec, self.q_dec, self.k_cache, self.v_cache, self.dec_bt, self.dec_lens,
+            s.group_size, self.prefix_lens, s.max_seq_len_dec(), s.scale,
+            workspace=self.ws_pfx, err_flag=self.err, stream=stream)
+
 
 def time_steps(fn_phases, steps, warmup, stream, flush, graphs=True, phase_events=True):
     """Run warmup + steps; returns per-step per-phase device ms (events).
@@ -453,6 +466,7 @@ def run_ours(args):
     mixed = None if args.only == "decode" else run_mixed(args, device, stream, flush, rank)
     sliding = None if args.only else run_sliding(args, device, stream, flush, rank)
     grpo = None if args.only else run_grpo(args, device, stream, flush, rank)
+    full512 = None if args.only else run_full512(args, device, stream, flush, rank)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
@@ -479,6 +493,7 @@ def run_ours(args):
         "mixed_step": mixed,
         "sliding_step": sliding,
         "grpo_step": grpo,
+        "head_dim_512_step": full512,
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.skip_cpu else cpu_baseline(step, ds, rank)
@@ -632,6 +647,8 @@ def run_grpo(args, device, stream, flush, rank):
         ds = DeviceStep(step, wl.BASE_SEED + 5 + 1000 * rank, device)
         per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush,
                          phase_events=False)
+        per_c = time_steps([ds.append, ds.decode_shared_prefix], args.steps, args.warmup, stream,
+                           flush, phase_events=False)
         import torch
         torch.cuda.synchronize()
         if int(ds.err.item()) != 0:
@@ -641,7 +658,9 @@ def run_grpo(args, device, stream, flush, rank):
     except Exception as e:
         return {"unavailable": f"{type(e).__name__}: {e}"}
     ms = float(np.mean([sum(p) for p in per]))
+    ms_c = float(np.mean([sum(p) for p in per_c]))
     logical = decode_bytes(step) + append_bytes(step, step.Bd)
+    unique = grpo_unique_bytes(step) + append_bytes(step, step.Bd)
     return {"workload": "grpo: 64 prompts x 4 generations, prefix 256 shared, completion "
                         "~U[0,3840], H 32/8/128, page 16, 36 layers in one pool "
                         f"({step.num_pages} pages)",
@@ -650,8 +669,59 @@ def run_grpo(args, device, stream, flush, rank):
             "decode_tokens_per_s": round(step.Bd / (36 * ms * 1e-3), 1),
             "logical_gb_s": round(logical / (ms * 1e-3) / 1e9, 2),
             "logical_bytes_per_layer": int(logical),
+            "shared_prefix": {
+                "layer_step_us": round(ms_c * 1e3, 2),
+                "step_ms_36_layers": round(36 * ms_c, 3),
+                "decode_tokens_per_s": round(step.Bd / (36 * ms_c * 1e-3), 1),
+                "unique_gb_s": round(unique / (ms_c * 1e-3) / 1e9, 2),
+                "unique_bytes_per_layer": int(unique),
+                "note": "append + paged_attn_decode_shared_prefix (prefix pass reads each "
+                        "prompt's pages once, then the suffix decode with the merge); "
+                        "unique bytes count each prompt's prefix once"},
             "note": "one layer timed (append + decode), scaled by 36; logical bytes count "
                     "each generation's shared prefix pages"}
+
+
+def grpo_unique_bytes(step: wl.Step) -> int:
+    """Algorithmic bytes of the cascade decode: each group's shared prefix
+    K/V once per group, each member's suffix once, q, out, page ids."""
+    L = step.dec_seq_lens.astype(np.int64)
+    kvrow = step.H_kv * step.D * 2 * 2
+    pl = np.repeat(step.prefix_lens.astype(np.int64), step.group_size)[:step.Bd]
+    share = L > pl
+    kv = int(np.sum(np.where(share, L - pl, L))) * kvrow
+    kv += int(sum(int(step.prefix_lens[j]) for j in range(len(step.prefix_lens))
+                  if np.any(share[j * step.group_size:(j + 1) * step.group_size]))) * kvrow
+    qo = step.Bd * step.H_q * step.D * 2 * 2
+    bt = int(np.sum(-(-L // step.P))) * 4 + step.Bd * 4
+    return kv + qo + bt
+
+
+def run_full512(args, device, stream, flush, rank):
+    """Full-attention decode with 512-wide heads (8 q heads on 1 kv head,
+    page 16, 64 rows over 1k-8k tokens): append + decode."""
+    try:
+        step = wl.full_d512()
+        ds = DeviceStep(step, wl.BASE_SEED + 6 + 1000 * rank, device)
+        per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush)
+        import torch
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            return {"unavailable": f"device error flag {int(ds.err.item())}"}
+        del ds
+        torch.cuda.empty_cache()
+    except Exception as e:
+        return {"unavailable": f"{type(e).__name__}: {e}"}
+    ph = np.mean(np.array(per), axis=0)
+    db = decode_bytes(step)
+    hbm_peak, _, _, src = peaks()
+    gbs = db / (ph[1] * 1e-3) / 1e9
+    return {"workload": "full_d512: H 8/1/512, page 16, 64 decode rows cached ~U[1024,8192]",
+            "decode_us": round(ph[1] * 1e3, 2), "append_us": round(ph[0] * 1e3, 2),
+            "decode_roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
+                                "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                "peak_source": src, "algorithmic_bytes": int(db),
+                                "traffic": None}}
 
 
 # ---------------------------------------------------------- CPU baselines

@@ -24,7 +24,8 @@
  *   of a sequence with block-table row T lives in page T[p / page_size],
  *   row p % page_size.  A slot is page * page_size + row.
  * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
- * - Supported shapes of the attention calls: head_dim in {64, 128, 256};
+ * - Supported shapes of the attention calls: head_dim in {64, 128, 256}
+ *   (paged_attn_decode and paged_attn_decode_static also 512);
  *   page_size a multiple of 16 (decode tests use 16 and 64, varlen tests 16
  *   to 256), and for varlen a divisor or a multiple of its key tile (128
  *   keys for head_dim 64 and 128, 64 for 256); num_q_heads a multiple of
@@ -142,6 +143,52 @@ pkv_status paged_attn_decode(void* out, const void* q,
                              int32_t max_seq_len, float scale, int32_t window,
                              void* workspace, size_t workspace_bytes,
                              int32_t* err_flag, void* stream);
+
+/*
+ * paged_attn_decode_shared_prefix - paged_attn_decode for batches whose
+ * sequences come in groups that share their leading pages (cascade
+ * decode).  Source: the grpo_equivalence page (num_generations = 4
+ * completions decoded per prompt) and the flex paged-KV engine's page
+ * table of the scripts/benchmarks commit log (block tables may point at the
+ * same physical pages).
+ *
+ * Sequences b = j*group_size .. j*group_size + group_size - 1 (the last
+ * group may be shorter) form group j.  prefix_lens [ceil(batch /
+ * group_size)] int32 (device): the group's shared prefix in keys, a
+ * multiple of page_size; the first prefix_lens[j] / page_size block-table
+ * entries of every member of group j must be the same pages (the caller's
+ * contract; not checked).  0 means no sharing.  A length that is negative,
+ * not a multiple of page_size or longer than a block-table row is treated
+ * as 0 and flagged PKV_DEVERR_LEN.
+ *
+ * The result is paged_attn_decode's (every query attends all of its keys,
+ * full causal attention: there is no window argument), computed in two
+ * launches on `stream`: a prefix pass reads each group's prefix pages once
+ * per kv head for the query rows of all members whose length exceeds the
+ * prefix, then the split-KV decode reads only those members' suffixes and
+ * merges them with the prefix partials (log-sum-exp weights).  Members no
+ * longer than their prefix are decoded whole.
+ *
+ *   workspace  paged_attn_decode_shared_prefix_workspace_size() bytes,
+ *              256-byte aligned, zero-filled before its first use, with the
+ *              reuse rules of paged_attn_decode's workspace.
+ * Limits: head_dim in {64, 128, 256}; group_size * num_q_heads /
+ * num_kv_heads query rows per group and kv head at most 32 (head_dim 64),
+ * 16 (128) or 8 (256); else PKV_ERR_UNSUPPORTED.
+ */
+size_t paged_attn_decode_shared_prefix_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim);
+pkv_status paged_attn_decode_shared_prefix(void* out, const void* q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table,
+                                           int32_t max_blocks_per_seq,
+                                           const int32_t* seq_lens, int32_t batch,
+                                           int32_t group_size, const int32_t* prefix_lens,
+                                           int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t page_size,
+                                           int64_t num_pages, int32_t max_seq_len, float scale,
+                                           void* workspace, size_t workspace_bytes,
+                                           int32_t* err_flag, void* stream);
 
 /*
  * paged_attn_varlen - packed variable-length attention over the paged cache

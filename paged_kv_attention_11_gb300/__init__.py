@@ -6,8 +6,10 @@ Three calls, same names as the C ABI (include/pkv.h):
 * ``paged_attn_decode`` one query per sequence over its paged prefix
 * ``paged_attn_varlen`` packed variable-length (prefill) attention
 
-plus ``paged_kv_append_rope`` (the append with q/k RMSNorm and the rotary
-embedding fused in) and ``rope_table`` (its cos/sin table).
+plus ``paged_attn_decode_shared_prefix`` (decode that reads a prefix shared
+by a group of sequences once per group), ``paged_kv_append_rope`` (the
+append with q/k RMSNorm and the rotary embedding fused in) and
+``rope_table`` (its cos/sin table).
 
 This module only marshals arguments (device pointers, sizes, the current
 CUDA stream) into the library; every step of the computation runs in the
@@ -26,9 +28,11 @@ from ._binding import (  # noqa: F401
     lib,
     lib_path,
     paged_attn_decode,
+    paged_attn_decode_shared_prefix,
     paged_attn_decode_static,
     paged_attn_varlen,
     paged_kv_append,
     paged_kv_append_rope,
     rope_table,
+    shared_prefix_workspace_size,
 )

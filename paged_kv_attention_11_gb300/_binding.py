@@ -31,6 +31,10 @@ _SIGS = {
     "paged_attn_decode_static": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32,
                                  _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_p,
                                  _c_p],
+    "paged_attn_decode_shared_prefix_workspace_size": [_c_i32, _c_i32, _c_i32, _c_i32],
+    "paged_attn_decode_shared_prefix": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32,
+                                        _c_i32, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64,
+                                        _c_i32, _c_f, _c_p, ctypes.c_size_t, _c_p, _c_p],
     "pkv_rope_table": [_c_p, _c_i32, _c_i32, ctypes.c_double, _c_p],
     "paged_kv_append_rope": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p,
                              _c_f, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_p, _c_p],
@@ -38,6 +42,7 @@ _SIGS = {
     "pkv_last_cuda_error": [],
 }
 _RES = {"paged_attn_decode_workspace_size": ctypes.c_size_t,
+        "paged_attn_decode_shared_prefix_workspace_size": ctypes.c_size_t,
         "pkv_status_string": ctypes.c_char_p, "pkv_last_cuda_error": ctypes.c_char_p}
 
 
@@ -120,15 +125,22 @@ def decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_
 _WORKSPACES = {}
 
 
+def shared_prefix_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int,
+                                 head_dim: int) -> int:
+    return int(lib().paged_attn_decode_shared_prefix_workspace_size(batch, num_q_heads,
+                                                                   num_kv_heads, head_dim))
+
+
 def decode_workspace(device: torch.device, stream_handle: int, batch: int, num_q_heads: int,
-                     num_kv_heads: int, head_dim: int) -> torch.Tensor:
+                     num_kv_heads: int, head_dim: int, shared_prefix: bool = False) -> torch.Tensor:
     """The binding's cached decode workspace for this stream and shape: it
     allocates (and zero-fills) only when none is cached yet or the cached
     one is too small, so a CUDA-graph capture must be preceded by one call
     of the same shape on the capturing stream (or pass ``workspace``)."""
-    need = max(decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim), 256)
+    size = shared_prefix_workspace_size if shared_prefix else decode_workspace_size
+    need = max(size(batch, num_q_heads, num_kv_heads, head_dim), 256)
     key = (device.index if device.index is not None else torch.cuda.current_device(),
-           int(stream_handle), num_q_heads, num_kv_heads, head_dim)
+           int(stream_handle), num_q_heads, num_kv_heads, head_dim, shared_prefix)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < need:
         ws = torch.zeros(need, dtype=torch.uint8, device=device)
@@ -163,6 +175,37 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
         float(scale), int(window), _ptr(workspace), workspace.numel(), _ptr(err_flag),
         _stream(stream)))
+    return out
+
+
+def paged_attn_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                    v_cache: torch.Tensor, block_table: torch.Tensor,
+                                    seq_lens: torch.Tensor, group_size: int,
+                                    prefix_lens: torch.Tensor, max_seq_len: int, scale: float,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    err_flag: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """Decode for groups of ``group_size`` consecutive sequences that share
+    their first ``prefix_lens[j]`` keys (pages aliased in their block
+    tables): out/q [B, H_q, D]; prefix_lens [ceil(B / group_size)] int32.
+    Same result as paged_attn_decode; the shared pages are read once per
+    group.  Workspace handling as paged_attn_decode."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    for n, t in (("block_table", block_table), ("seq_lens", seq_lens),
+                 ("prefix_lens", prefix_lens)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    B, H_q, D = q.shape
+    num_pages, H_kv, P, _ = k_cache.shape
+    if workspace is None:
+        workspace = decode_workspace(q.device, _stream(stream), B, H_q, H_kv, D,
+                                     shared_prefix=True)
+    _check("paged_attn_decode_shared_prefix", lib().paged_attn_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, int(group_size), _ptr(prefix_lens), H_q, H_kv,
+        D, P, num_pages, int(max_seq_len), float(scale), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)))
     return out
 
 

@@ -41,6 +41,8 @@ int num_sms_current(int* out) {
 }
 
 bool supported_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
+// decode also runs the 512-wide heads of full-attention layers
+bool decode_head_dim(int D) { return supported_head_dim(D) || D == 512; }
 
 }  // namespace
 
@@ -58,7 +60,7 @@ pkv_status decode_check_args(const void* out, const void* q, const void* k_cache
     return PKV_ERR_INVALID;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
   if (!(scale == scale)) return PKV_ERR_INVALID;  // NaN
-  if (!supported_head_dim(head_dim) || page_size % 16 != 0 || num_q_heads / num_kv_heads > 8 ||
+  if (!decode_head_dim(head_dim) || page_size % 16 != 0 || num_q_heads / num_kv_heads > 8 ||
       num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 4096)
     return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
@@ -107,7 +109,7 @@ pkv_status paged_kv_append(const void* k_new, const void* v_new, void* k_cache, 
 size_t paged_attn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                         int32_t head_dim) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
-      !supported_head_dim(head_dim))
+      !decode_head_dim(head_dim))
     return 0;
   int sms = 0;
   if (num_sms_current(&sms) != 0) return 0;
@@ -136,6 +138,64 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
       out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
       num_kv_heads, head_dim, page_size, num_pages, max_seq_len, scale, window, workspace,
       workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), sms);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+size_t paged_attn_decode_shared_prefix_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim) {
+  if (!supported_head_dim(head_dim)) return 0;
+  const size_t dec =
+      paged_attn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim);
+  if (dec == 0) return 0;
+  const size_t rows = (size_t)batch * num_q_heads;
+  return align256(dec) + align256(rows * 4) + align256(rows * head_dim * 4);
+}
+
+pkv_status paged_attn_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+    int32_t batch, int32_t group_size, const int32_t* prefix_lens, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, int64_t num_pages,
+    int32_t max_seq_len, float scale, void* workspace, size_t workspace_bytes,
+    int32_t* err_flag, void* stream) {
+  const pkv_status chk =
+      pkv::decode_check_args(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                             batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                             max_seq_len, scale);
+  if (chk != PKV_OK) return chk;
+  if (group_size < 1) return PKV_ERR_INVALID;
+  if (!supported_head_dim(head_dim) ||
+      group_size * (num_q_heads / num_kv_heads) > pkv::prefix_max_rows(head_dim))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!prefix_lens || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_INVALID;
+  int sms = 0;
+  if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  const size_t dec = align256(
+      pkv::decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, sms));
+  const size_t rows = (size_t)batch * num_q_heads;
+  if (workspace_bytes < dec + align256(rows * 4) + align256(rows * head_dim * 4))
+    return PKV_ERR_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* pre_lse = reinterpret_cast<float*>(ws + dec);
+  float* pre_o = reinterpret_cast<float*>(ws + dec + align256(rows * 4));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_prefix_pass(q, k_cache, v_cache, block_table, max_blocks_per_seq,
+                                          seq_lens, prefix_lens, batch, group_size, num_q_heads,
+                                          num_kv_heads, head_dim, page_size, num_pages, scale,
+                                          pre_o, pre_lse, err_flag, st, sms);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_fail(e);
+  pkv::DecodeCascade cas = {prefix_lens, group_size, pre_o, pre_lse};
+  e = pkv::launch_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                         batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                         max_seq_len, scale, 0, workspace, dec, err_flag, st, sms, &cas);
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }

@@ -37,12 +37,11 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tile16.cuh"
 #include "tmap.h"
 
 namespace pkv {
 
-constexpr int kTile = 16;  // keys per pipeline stage
-constexpr int kGP = 8;     // GQA group padded to the mma N dimension
 constexpr int kNRec = 4;   // piece records in flight
 constexpr int kMergeLse = 128;  // (piece, head) log-sum-exps staged in smem for a merge
 // Shortest chunk a segment is cut into (tiles).  Small batches (a few long
@@ -65,12 +64,21 @@ struct DecodeArgs {
   int32_t* queue;      // [2]: next item, CTAs done; zero between calls
   float* part_lse;     // [(S + N) * G]
   float* part_o;       // [(S + N) * G * D]
+  // shared-prefix (cascade) decode: null prefix_lens = plain decode.  A
+  // sequence of group b / group_size whose length exceeds the group's shared
+  // prefix attends only its suffix here, and its result is merged with the
+  // prefix pass's partial (pre_o, pre_lse at row b * H_q + head).
+  const int32_t* prefix_lens;
+  int32_t group_size;
+  const float* pre_o;
+  const float* pre_lse;
   int32_t* err;
 };
 
-// Keys [lo, L) of sequence b are attended; returns the tile range.
+// Keys [lo, L) of sequence b are attended here; returns the tile range and
+// whether a prefix partial covers keys [0, lo).
 __device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, int& lo,
-                                           int& t_lo, int& t_hi, bool flag) {
+                                           int& t_lo, int& t_hi, bool flag, int* pfx = nullptr) {
   int len = __ldg(a.seq_lens + b);
   const int cap = a.max_blocks * a.P;
   if (len < 0 || len > cap) {
@@ -79,6 +87,15 @@ __device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, i
   }
   L = len;
   lo = (a.window > 0 && len > a.window) ? len - a.window : 0;
+  int has_pfx = 0;
+  if (a.prefix_lens != nullptr) {
+    const int pl = shared_prefix_len(a.prefix_lens, b / a.group_size, a.P, cap);
+    if (pl > 0 && len > pl) {
+      lo = pl;
+      has_pfx = 1;
+    }
+  }
+  if (pfx) *pfx = has_pfx;
   t_lo = lo / kTile;
   t_hi = (len + kTile - 1) / kTile;
 }
@@ -92,46 +109,46 @@ struct PieceRec {
   int nch;           // chunks of the segment (1: the item is the whole segment)
   int slot0;         // partial slot of chunk 0 of the segment
   int chunk;         // this item's chunk
-  int pad;
+  int pfx;           // 1: a prefix partial joins the merge (cascade)
+};
+
+// Head dims of 512 and more keep the query rows in shared memory (read with
+// ldmatrix per tile) instead of registers, which then hold only O, and hand
+// consumer states to the epilogue through one combine buffer instead of two.
+template <int D>
+struct DecodeLayout {
+  static constexpr bool kQSmem = D >= 512;
+  static constexpr int kNComb = kQSmem ? 1 : 2;
+  // query rows in a record slot: kQSmem: kGP rows padded by 16 bytes (rows
+  // G..kGP-1 zero), so that the 8 rows of an ldmatrix hit distinct banks
+  static constexpr int kQRowBytes = kQSmem ? D * 2 + 16 : D * 2;
 };
 
 // Shared-memory plan (byte offsets from the 1024-aligned base); depends on
 // the runtime GQA group and batch.
 template <int D, int NW, int NSTAGE>
 struct DecodePlan {
+  using Lay = DecodeLayout<D>;
   static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
   static constexpr int kCombStride = D + 4;             // padded row (floats)
-  int rec, qbuf, comb, ml, bars, ok, misc, scan, cum, total;
+  int rec, qbuf, qslot, comb, ml, bars, ok, misc, scan, sort, cum, total;
   __host__ __device__ DecodePlan(int G, int batch) {
     int o = NSTAGE * kStageBytes;
     rec = o;   o += kNRec * (int)sizeof(PieceRec);
-    qbuf = o;  o += kNRec * G * D * 2;
-    comb = o;  o += 2 * NW * G * kCombStride * 4;
-    ml = o;    o += 2 * NW * G * 2 * 4;
-    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 4) * 8;
+    qslot = (Lay::kQSmem ? kGP : G) * Lay::kQRowBytes;
+    qbuf = o;  o += kNRec * qslot;
+    comb = o;  o += Lay::kNComb * NW * G * kCombStride * 4;
+    ml = o;    o += Lay::kNComb * NW * G * 2 * 4;
+    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 2 * Lay::kNComb) * 8;
     ok = o;    o += NSTAGE * 4;
     misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
     scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
+    sort = o;  o += 256 * 4;  // bucket counts of the queue-order sort
     cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
     total = 1024 + o;
   }
 };
-
-// Shared-memory address of 16-byte chunk c (0..D/8-1) of key row `key` in a
-// staged tile.  Default staging: D/64 boxes of [16 rows x 128 B] (one box
-// per 64-column slice).  ONEBOX (head_dim 128): one box of 32 rows x 128 B,
-// row = 2*key + c/8.  Both are 128-byte swizzled: 16-byte unit u of a row r
-// sits at unit u ^ (r % 8).
-template <int D, bool ONEBOX>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int c) {
-  if (ONEBOX) {
-    const int rp = 2 * key + (c >> 3);
-    return base + rp * 128 + (((c & 7) ^ (rp & 7)) << 4);
-  } else {
-    return base + (c >> 3) * (kTile * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4);
-  }
-}
 
 template <int D, int NW, int NSTAGE, bool ONEBOX>
 __global__ void __launch_bounds__((NW + 2) * 32, 1)
@@ -140,6 +157,9 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
   using P_ = DecodePlan<D, NW, NSTAGE>;
+  using Lay = DecodeLayout<D>;
+  constexpr bool QS = Lay::kQSmem;
+  constexpr int NCB = Lay::kNComb;
   constexpr int NT = (NW + 2) * 32;
   constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
   constexpr int kBoxBytes = kTile * 128;
@@ -159,8 +179,8 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   uint64_t* empty = full + NSTAGE;
   uint64_t* rec_full = empty + NSTAGE;
   uint64_t* rec_empty = rec_full + kNRec;
-  uint64_t* comb_full = rec_empty + kNRec;  // [2]
-  uint64_t* comb_empty = comb_full + 2;     // [2]
+  uint64_t* comb_full = rec_empty + kNRec;  // [NCB]
+  uint64_t* comb_empty = comb_full + NCB;   // [NCB]
   int* stage_ok = reinterpret_cast<int*>(smem + plan.ok);
   float* merge_m = reinterpret_cast<float*>(smem + plan.misc);
   float* merge_inv = merge_m + kGP;
@@ -177,28 +197,57 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   const int lane = tid & 31;
   const int B = a.batch;
 
-  if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
+  // one barrier per thread (the block has more threads than barriers)
+  static_assert(2 * NSTAGE + 2 * kNRec + 2 * NCB <= NT, "barrier init");
+  {
+    const int i = tid;
+    if (i < NSTAGE) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+    } else if (i < 2 * NSTAGE) {
+      mbar_init(full + i, 1);  // empty[i - NSTAGE]
+    } else if (i < 2 * NSTAGE + kNRec) {
+      mbar_init(rec_full + (i - 2 * NSTAGE), 32);
+    } else if (i < 2 * NSTAGE + 2 * kNRec) {
+      mbar_init(rec_full + (i - 2 * NSTAGE), NW * 32 + 32);  // rec_empty
+    } else if (i < 2 * NSTAGE + 2 * kNRec + NCB) {
+      mbar_init(comb_full + (i - 2 * NSTAGE - 2 * kNRec), NW * 32);
+    } else if (i < 2 * NSTAGE + 2 * kNRec + 2 * NCB) {
+      mbar_init(comb_full + (i - 2 * NSTAGE - 2 * kNRec), 32);  // comb_empty
     }
-    for (int i = 0; i < kNRec; ++i) {
-      mbar_init(rec_full + i, 32);
-      mbar_init(rec_empty + i, NW * 32 + 32);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(comb_full + i, NW * 32);
-      mbar_init(comb_empty + i, 32);
-    }
-    fence_mbar_init();
+    if (i < 2 * NSTAGE + 2 * kNRec + 2 * NCB) fence_mbar_init();
+  }
+  if (tid == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+  }
+  if (QS) {
+    // rows G..kGP-1 of every query slot stay zero (the padded heads of the
+    // mma N dimension); rows < G are written per item
+    for (int i = tid; i < kNRec * (kGP - G) * (Lay::kQRowBytes / 16); i += NT) {
+      const int per = (kGP - G) * (Lay::kQRowBytes / 16);
+      const int sl = i / per, j = i - sl * per;
+      reinterpret_cast<uint4*>(qbuf + sl * plan.qslot + G * Lay::kQRowBytes)[j] =
+          make_uint4(0, 0, 0, 0);
+    }
   }
   pdl_wait();  // inputs may come from the previous kernel in the stream
   // the producer's first queue grab is issued now; its latency hides behind
   // the prologue
   int first_grab = 0;
   if (warp == NW && lane == 0) first_grab = atomicAdd(a.queue, 1);
+  {
+    // the query rows and block tables, spread over the grid, into L2: the
+    // producers' first items then find them there
+    const int64_t qlines = ((int64_t)B * a.H_q * D * 2 + 127) / 128;
+    const int64_t blines = ((int64_t)B * a.max_blocks * 4 + 127) / 128;
+    const char* qp = reinterpret_cast<const char*>(a.q);
+    const char* bp = reinterpret_cast<const char*>(a.block_table);
+    for (int64_t l = (int64_t)blockIdx.x * NT + tid; l < qlines + blines;
+         l += (int64_t)gridDim.x * NT) {
+      const char* p = l < qlines ? qp + l * 128 : bp + (l - qlines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+  }
 
   // ---- work items (every CTA computes the same list, in smem) ----
   // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
@@ -241,20 +290,57 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
   }
   __syncthreads();
-  // queue order: sequences by chunk length, longest first (ties by index);
-  // beyond 512 sequences the natural order is kept
-  if (B <= 512) {
-    for (int b = tid; b < B; b += NT) {
-      const int cb = s_sp[b];
-      int rank = 0;
-      for (int c = 0; c < B; ++c) {
-        const int cc = s_sp[c];
-        rank += (cc > cb || (cc == cb && c < b)) ? 1 : 0;
-      }
-      s_order[rank] = b;
+  // queue order: sequences by chunk length, longest first, ties by index.
+  // One warp runs a stable bucket sort: lengths fall into up to 256 buckets
+  // (exact when the longest chunk is under 256 tiles, else by its top bits),
+  // bucket sizes are counted and scanned, then each group of 32 sequences
+  // is placed in index order within its bucket.  Deterministic, so every
+  // CTA derives the same queue.
+  if (warp == 0) {
+    int* hist = reinterpret_cast<int*>(smem + plan.sort);  // [256]
+    int mx = 0;
+    for (int b = lane; b < B; b += 32) mx = max(mx, s_sp[b]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int shift = 0;
+    while ((mx >> shift) > 255) ++shift;
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int b = lane; b < B; b += 32) atomicAdd(hist + (255 - (s_sp[b] >> shift)), 1);
+    __syncwarp();
+    int v[8], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = hist[lane * 8 + k];
+      sum += v[k];
     }
-  } else {
-    for (int b = tid; b < B; b += NT) s_order[b] = b;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      hist[lane * 8 + k] = run;  // first position of bucket lane*8+k
+      run += v[k];
+    }
+    __syncwarp();
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      const bool act = b < B;
+      const int bin = act ? 255 - (s_sp[b] >> shift) : -1 - lane;  // idle lanes match nothing
+      const unsigned same = __match_any_sync(0xffffffffu, bin);
+      const int base = act ? hist[bin] : 0;
+      __syncwarp();
+      if (act) {
+        s_order[base + __popc(same & ((1u << lane) - 1u))] = b;
+        if (lane == __ffs(same) - 1) hist[bin] = base + __popc(same);
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
   for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
@@ -314,7 +400,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
     struct Item {
       bool more;
-      int b, g, L, lo, first_tile, n, nch, slot0, chunk;
+      int b, g, L, lo, first_tile, n, nch, slot0, chunk, pfx;
     };
     auto grab = [&]() -> int {
       int i = 0;
@@ -325,7 +411,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     auto item_at = [&](int i) -> Item {
       Item it;
       it.more = i < T;
-      it.b = it.g = it.L = it.lo = it.first_tile = it.nch = it.slot0 = it.chunk = 0;
+      it.b = it.g = it.L = it.lo = it.first_tile = it.nch = it.slot0 = it.chunk = it.pfx = 0;
       it.n = -1;
       if (!it.more) return it;
       int lo = 0, hi = B;  // s_sp[lo] <= i < s_sp[lo+1]
@@ -335,8 +421,8 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       }
       const int b = s_order[lo];
       const int j = i - s_sp[lo];
-      int L, klo, t_lo, t_hi;
-      seq_extent(a, b, L, klo, t_lo, t_hi, false);
+      int L, klo, t_lo, t_hi, pfx;
+      seq_extent(a, b, L, klo, t_lo, t_hi, false, &pfx);
       const int t = t_hi - t_lo;
       const int nch = nch_of(t);
       const int csz = (t + nch - 1) / nch;
@@ -350,6 +436,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       it.nch = nch;
       it.slot0 = s_nat[b] + g * nch;
       it.chunk = chunk;
+      it.pfx = pfx;
       return it;
     };
     auto prefetch = [&](const Item& p, uint4 (&qr)[QV], int& pages) {
@@ -378,11 +465,18 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       const int slot = k % kNRec;
       if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
       if (cur.more) {
-        uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * G * D * 2);
+        uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * plan.qslot);
 #pragma unroll
         for (int i = 0; i < QV; ++i) {
           const int v = lane + 32 * i;
-          if (v < qvec) qdst[v] = qcur[i];
+          if (v < qvec) {
+            if (QS) {  // padded rows: vector v of head v / (D/8)
+              const int h = v / (D / 8);
+              qdst[v + h] = qcur[i];
+            } else {
+              qdst[v] = qcur[i];
+            }
+          }
         }
       }
       if (lane == 0) {
@@ -396,6 +490,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         r.nch = cur.nch;
         r.slot0 = cur.slot0;
         r.chunk = cur.chunk;
+        r.pfx = cur.pfx;
       }
       __syncwarp();
       mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
@@ -479,21 +574,29 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       const int slot = k % kNRec;
       if (!mbar_wait(rec_full + slot, (k / kNRec) & 1, a.err, dead)) break;
       const PieceRec rec = recs[slot];
-      // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan
-      uint32_t qb[KS][2];
-      {
+      // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan.
+      // Registers (head dims up to 256), or per tile from shared memory.
+      uint32_t qb[QS ? 1 : KS][2];
+      if (!QS) {
         const bool hv = rec.n >= 0 && quad < G;
-        const uint8_t* qrow = qbuf + slot * G * D * 2 + (hv ? quad : 0) * D * 2;
+        const uint8_t* qrow = qbuf + slot * plan.qslot + (hv ? quad : 0) * D * 2;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
           qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * qlan) * 2)
                          : 0u;
           qb[ks][1] =
               hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 8 + 2 * qlan) * 2) : 0u;
         }
+        mbar_arrive(rec_empty + slot);  // record and query rows copied to registers
       }
-      mbar_arrive(rec_empty + slot);  // record and query rows copied to registers
-      if (rec.n < 0) break;
+      // ldmatrix row address of this lane in the smem query slot: row
+      // lane % 8 (a head), 8 dims at (lane / 8) * 8 of each 32-dim step
+      const uint32_t q_lane_addr = smem_u32(qbuf + slot * plan.qslot) +
+                                   (lane & 7) * Lay::kQRowBytes + (lane >> 3) * 16;
+      if (rec.n < 0) {
+        if (QS) mbar_arrive(rec_empty + slot);
+        break;
+      }
 
       float o[KS][4];
 #pragma unroll
@@ -517,13 +620,27 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+          if (QS) {
+            // two k-steps per ldmatrix of the query rows
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-            if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            for (int ks = 0; ks < KS; ks += 2) {
+              uint32_t b00, b01, b10, b11;
+              ldsm_x4(q_lane_addr + ks * 32, b00, b01, b10, b11);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sa, a0, a1, a2, a3, b00, b01);
+              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sb, a0, a1, a2, a3, b10, b11);
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
+              const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(addr, a0, a1, a2, a3);
+              if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
           }
         }
         // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
@@ -577,6 +694,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         if (lane == 0) mbar_arrive(empty + s);
       }
       it_base += n;
+      if (QS) mbar_arrive(rec_empty + slot);  // done reading the query rows
 
       // ---- hand (m, l, O) of this warp to the epilogue warp ----
 #pragma unroll
@@ -584,8 +702,8 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         lA += __shfl_xor_sync(0xffffffffu, lA, off);
         lB += __shfl_xor_sync(0xffffffffu, lB, off);
       }
-      const int cb = k & 1;
-      if (k >= 2) mbar_wait(comb_empty + cb, ((k >> 1) - 1) & 1, a.err, dead);
+      const int cb = k % NCB;
+      if (k >= NCB) mbar_wait(comb_empty + cb, ((k / NCB) - 1) & 1, a.err, dead);
       float* co = comb_o + ((cb * NW + r0) * G) * CS;
       float* cml = comb_ml + ((cb * NW + r0) * G) * 2;
       const int hA = 2 * qlan, hB = hA + 1;
@@ -622,10 +740,10 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       const PieceRec rec = recs[slot];
       mbar_arrive(rec_empty + slot);
       if (rec.n < 0) break;
-      const int cb = k & 1;
-      mbar_wait(comb_full + cb, (k >> 1) & 1, a.err, dead);
+      const int cb = k % NCB;
+      mbar_wait(comb_full + cb, (k / NCB) & 1, a.err, dead);
       const int b = rec.b, g = rec.g;
-      const bool whole = rec.nch == 1;
+      const bool whole = rec.nch == 1 && rec.pfx == 0;
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
       const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
@@ -691,15 +809,19 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         __syncwarp();
         if (*merge_flag) {
           __threadfence();
-          const int np = rec.nch;
+          // the segment's chunks, plus the prefix partial as chunk nch
+          const int np = rec.nch + rec.pfx;
+          const int64_t pre_row = (int64_t)b * a.H_q + g * G;
+          auto lse_glob = [&](int c, int h) -> float {
+            return c < rec.nch ? __ldcg(a.part_lse + ((int64_t)rec.slot0 + c) * G + h)
+                               : __ldcg(a.pre_lse + pre_row + h);
+          };
           // (1) every (chunk, head) log2-sum-exp in one round of loads, the
           //     per-head max and weight sum from shared memory
-          for (int i = lane; i < np * G && i < kMergeLse; i += 32)
-            merge_lse[i] = __ldcg(a.part_lse + ((int64_t)rec.slot0 + i / G) * G + (i % G));
+          for (int i = lane; i < np * G && i < kMergeLse; i += 32) merge_lse[i] = lse_glob(i / G, i % G);
           __syncwarp();
           auto lse_at = [&](int c, int h) -> float {
-            return c * G + h < kMergeLse ? merge_lse[c * G + h]
-                                         : __ldcg(a.part_lse + ((int64_t)rec.slot0 + c) * G + h);
+            return c * G + h < kMergeLse ? merge_lse[c * G + h] : lse_glob(c, h);
           };
           if (lane < G) {
             const int h = lane;
@@ -712,44 +834,70 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
             merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
           }
           __syncwarp();
-          // (2) weighted sum of the chunks' outputs, 4 dims per lane; the
-          //     loads of 4 chunks are issued before any is used
-          for (int j = lane; j < G * (D / 4); j += 32) {
-            const int h = j / (D / 4), d4 = j - h * (D / 4);
-            const float M = merge_m[h];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
-              for (int c0 = 0; c0 < np; c0 += 4) {
-                float4 v[4];
-                float w[4];
+          // (2) weighted sum of the chunks' outputs, 4 dims (a slice) per
+          //     lane and load: each lane keeps kMU slices x kMC chunks of
+          //     loads in flight, so a merge costs a few L2 round trips
+          //     instead of one per (slice, chunk group).  Every output sums
+          //     its chunks in chunk order.
+          constexpr int kMU = 4, kMC = 4;
+          const int nslice = G * (D / 4);
+          for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
+            float4 acc[kMU];
+            int hh[kMU];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int c = c0 + u;
-                  w[u] = 0.f;
-                  v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                  if (c < np) {
-                    const int64_t pc = ((int64_t)rec.slot0 + c) * G + h;
-                    v[u] = __ldcg(reinterpret_cast<const float4*>(a.part_o + pc * D) + d4);
-                    w[u] = exp2f(lse_at(c, h) - M);
+            for (int u = 0; u < kMU; ++u) {
+              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const int j = j0 + 32 * u;
+              hh[u] = j < nslice ? j / (D / 4) : 0;
+            }
+            for (int c0 = 0; c0 < np; c0 += kMC) {
+              float4 v[kMU][kMC];
+#pragma unroll
+              for (int u = 0; u < kMU; ++u) {
+                const int j = j0 + 32 * u;
+                const int h = hh[u], d4 = j - h * (D / 4);
+#pragma unroll
+                for (int cc = 0; cc < kMC; ++cc) {
+                  const int c = c0 + cc;
+                  v[u][cc] = make_float4(0.f, 0.f, 0.f, 0.f);
+                  if (j < nslice && c < np && merge_m[h] != -INFINITY) {
+                    const float* src = c < rec.nch
+                                           ? a.part_o + (((int64_t)rec.slot0 + c) * G + h) * D
+                                           : a.pre_o + (pre_row + h) * D;
+                    v[u][cc] = __ldcg(reinterpret_cast<const float4*>(src) + d4);
                   }
                 }
+              }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  acc.x += w[u] * v[u].x;
-                  acc.y += w[u] * v[u].y;
-                  acc.z += w[u] * v[u].z;
-                  acc.w += w[u] * v[u].w;
+              for (int u = 0; u < kMU; ++u) {
+                const float M = merge_m[hh[u]];
+#pragma unroll
+                for (int cc = 0; cc < kMC; ++cc) {
+                  const int c = c0 + cc;
+                  if (c < np && M != -INFINITY) {
+                    const float w = exp2f(lse_at(c, hh[u]) - M);
+                    acc[u].x += w * v[u][cc].x;
+                    acc[u].y += w * v[u][cc].y;
+                    acc[u].z += w * v[u][cc].z;
+                    acc[u].w += w * v[u][cc].w;
+                  }
                 }
               }
             }
-            const float inv = merge_inv[h];
-            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
-                pk;
+#pragma unroll
+            for (int u = 0; u < kMU; ++u) {
+              const int j = j0 + 32 * u;
+              if (j >= nslice) continue;
+              const int h = hh[u], d4 = j - h * (D / 4);
+              const float inv = merge_inv[h];
+              __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x * inv, acc[u].y * inv);
+              __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z * inv, acc[u].w * inv);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+              pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+              *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
+                  pk;
+            }
           }
           if (lane == 0) a.seg_count[seg] = 0;
           __syncwarp();
@@ -782,12 +930,14 @@ template <> struct DecodeCfg<128> {
   static constexpr int NW = PKV_DEC_NW, NSTAGE = PKV_DEC_NSTAGE, CTAS_PER_SM = PKV_DEC_CTAS;
 };
 template <> struct DecodeCfg<256> { static constexpr int NW = 2, NSTAGE = 8, CTAS_PER_SM = 1; };
+template <> struct DecodeCfg<512> { static constexpr int NW = 2, NSTAGE = 4, CTAS_PER_SM = 1; };
 
 static int decode_ctas_per_sm(int D) {
   switch (D) {
     case 64: return DecodeCfg<64>::CTAS_PER_SM;
     case 128: return DecodeCfg<128>::CTAS_PER_SM;
-    default: return DecodeCfg<256>::CTAS_PER_SM;
+    case 256: return DecodeCfg<256>::CTAS_PER_SM;
+    default: return DecodeCfg<512>::CTAS_PER_SM;
   }
 }
 
@@ -880,8 +1030,13 @@ cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const v
                           const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
                           float scale, int32_t window, void* workspace, size_t workspace_bytes,
-                          int32_t* err, cudaStream_t stream, int num_sms) {
+                          int32_t* err, cudaStream_t stream, int num_sms,
+                          const DecodeCascade* cascade) {
   DecodeArgs a;
+  a.prefix_lens = cascade ? cascade->prefix_lens : nullptr;
+  a.group_size = cascade ? cascade->group_size : 1;
+  a.pre_o = cascade ? cascade->pre_o : nullptr;
+  a.pre_lse = cascade ? cascade->pre_lse : nullptr;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.block_table = block_table;
@@ -912,6 +1067,7 @@ cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const v
     case 64: return launch_decode_t<64>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     case 128: return launch_decode_t<128>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     case 256: return launch_decode_t<256>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 512: return launch_decode_t<512>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -58,12 +58,34 @@ cudaError_t launch_kv_append_rope(const RopeAppendArgs& a, int32_t D, cudaStream
 
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms);
 
+// Shared-prefix (cascade) inputs of the decode kernel: the groups' prefix
+// lengths and the prefix pass's partials ([batch * H_q, D] and [batch * H_q]).
+struct DecodeCascade {
+  const int32_t* prefix_lens;
+  int32_t group_size;
+  const float* pre_o;
+  const float* pre_lse;
+};
+
 cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_table, int32_t max_blocks,
                           const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
                           float scale, int32_t window, void* workspace, size_t workspace_bytes,
-                          int32_t* err, cudaStream_t stream, int num_sms);
+                          int32_t* err, cudaStream_t stream, int num_sms,
+                          const DecodeCascade* cascade = nullptr);
+
+// Prefix pass of the cascade: partial (o, log2-sum-exp) of every member row
+// over its group's shared prefix.  Query rows per (group, kv head) are
+// group_size * H_q / H_kv, at most prefix_max_rows(D).
+int prefix_max_rows(int D);
+cudaError_t launch_prefix_pass(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks,
+                               const int32_t* seq_lens, const int32_t* prefix_lens,
+                               int32_t batch, int32_t group_size, int32_t H_q, int32_t H_kv,
+                               int32_t D, int32_t P, int64_t num_pages, float scale,
+                               float* pre_o, float* pre_lse, int32_t* err, cudaStream_t stream,
+                               int num_sms);
 
 struct VarlenMaps {
   CUtensorMap q;  // 4-D view of q: {D, G, H_kv, total_q}

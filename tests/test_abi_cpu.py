@@ -171,3 +171,22 @@ def test_binding_signatures_match_the_header():
     for name, args in b._SIGS.items():
         want = [_ctype_of(p) for p in sigs[name]]
         assert args == want, (name, args, want)
+
+
+def test_shared_prefix_decode_validates_on_host(lib):
+    L = _bind(lib)
+    P = 0x1000  # fake, never dereferenced: validation fails first
+
+    def call(gs=4, pl=P, H_q=32, H_kv=8, D=128, ws=P, B=8):
+        return L.paged_attn_decode_shared_prefix(P, P, P, P, P, 4, P, B, gs, pl, H_q, H_kv, D,
+                                                 16, 64, 64, 0.1, ws, 1 << 24, None, None)
+    assert call(gs=0) == 1                 # empty groups
+    assert call(pl=None) == 1              # missing prefix lengths
+    assert call(ws=P + 64) == 1            # workspace not 256-byte aligned
+    assert call(H_q=30) == 1               # H_q not a multiple of H_kv
+    assert call(gs=8) == 2                 # 8 members x 4 heads: 32 rows > 16 at head_dim 128
+    assert call(D=512, H_q=8, H_kv=8, gs=1) == 2   # head_dim 512 has no prefix pass
+    assert call(B=0, gs=4) == 0            # empty batch: no-op
+    # head_dim 512 is a decode shape but not a varlen one
+    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 8, 2, 512, 16, 64,
+                               0.1, 1, 0, None, None) == 2

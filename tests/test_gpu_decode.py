@@ -99,7 +99,7 @@ def _decode(pkv, q, kc, vc, bt, lens, scale, window, max_len=None):
     return out, int(err.item())
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
 @pytest.mark.parametrize("H", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 2)])
 @pytest.mark.parametrize("P", [16, 64])
 def test_decode_shapes(pkv, D, H, P):
@@ -267,3 +267,24 @@ def test_decode_workspace_reuse_stays_clean(pkv):
                           f"reuse {it}")
     counters = ws[:300 * 8 * 4].view(torch.int32)
     assert int(counters.abs().sum().item()) == 0
+
+
+def test_decode_head_dim_512_workload(pkv):
+    """The full-attention regime with 512-wide heads (8 q heads on 1 kv
+    head): 64 decode rows over contexts of 1k-8k tokens, append first."""
+    step = wl.full_d512()
+    vals = wl.fill_values(step, 512)
+    got, want, (kc, vc), (hk, hv) = run_decode_step(pkv, step, vals)
+    assert np.array_equal(bf16_dev_to_bits(kc), hk), "K pool differs after append"
+    assert_close_attn(got, want, "head_dim 512")
+
+
+@pytest.mark.parametrize("window", [1, 300])
+def test_decode_head_dim_512_window_and_short(pkv, window):
+    rng = np.random.default_rng(512 + window)
+    lens = [1, 2, 16, 17, 700, 5000]
+    q, kc, vc, bt, L = _random_case(rng, len(lens), 16, 2, 512, 16, lens)
+    out, err = _decode(pkv, q, kc, vc, bt, L, 1 / np.sqrt(512), window)
+    assert err == 0
+    want = oracle.paged_decode(q, kc, vc, bt, L, 1 / np.sqrt(512), window)
+    assert_close_attn(bf16_dev_to_f64(out), want, f"D=512 window={window}")

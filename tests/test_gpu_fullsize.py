@@ -94,5 +94,17 @@ def test_grpo_rollout_full_size_sampled(pkv):
     assert np.array_equal(got_v, ov), "V pages differ after append"
     want = oracle.paged_decode(q[pick], ok, ov, cbt, lens[pick], step.scale, step.window)
     assert_close_attn(got_all[pick], want, "grpo full size")
+
+    # the same step through the shared-prefix (cascade) decode: each prompt's
+    # 16 prefix pages read once per group of 4 generations
+    out_c = torch.full((B, step.H_q, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.paged_attn_decode_shared_prefix(out_c, to_dev_bf16(q), kc, vc, to_dev(bt), to_dev(lens),
+                                        step.group_size, to_dev(step.prefix_lens),
+                                        step.max_seq_len_dec(), step.scale, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got_c = bf16_dev_to_f64(out_c)
+    assert np.all(np.isfinite(got_c)), "a sequence read a page outside its table"
+    assert_close_attn(got_c[pick], want, "grpo full size, cascade")
     del kc, vc
     torch.cuda.empty_cache()

@@ -20,6 +20,8 @@ for varlen; Gemma-4 sliding window of 512 and shared-KV layers):
            + 4 prefill chunks of 2048 (prefix 0), two layers on one pool
   grpo     64 prompts x 4 generations, 256-token prefix pages shared by the
            4 generations, completion ~U[0,3840], H 32/8/128, page 16
+  full_d512  full-attention layers with 512-wide heads: H 8/1/512, page 16,
+           64 decode (cached ~U[1024,8192]) + 4 prefill chunks of 1024
 
 Values are bf16 bit patterns (numpy uint16): fp32 draws rounded to nearest
 even before either side sees them, so both sides start from identical bits.
@@ -84,6 +86,10 @@ class Step:
     used_pages: np.ndarray = None      # pages referenced by any table
     k_head_scale: Optional[np.ndarray] = None  # [H_kv] fp32 or None
     layer_page_offset: int = 0         # for multi-layer pools (grpo)
+    # decode sequences j*group_size .. j*group_size+group_size-1 share their
+    # first prefix_lens[j] keys (the same physical pages in their tables)
+    group_size: int = 1
+    prefix_lens: Optional[np.ndarray] = None  # [ceil(Bd / group_size)] int32
 
     # ---- derived index arrays --------------------------------------------
     @property
@@ -288,6 +294,20 @@ def sliding(seed: int = BASE_SEED + 4, n_dec: int = 32, n_chunks: int = 4,
                      window=512, n_layers=2)
 
 
+def full_d512(seed: int = BASE_SEED + 6, n_dec: int = 64, n_chunks: int = 4,
+              chunk: int = 1024, num_pages: Optional[int] = None) -> Step:
+    """The full-attention regime with 512-wide heads (the Gemma-4 engine
+    commit's second attention regime: head_dim 512, rope_theta 1e6): 8 q
+    heads on 1 kv head, page 16, decode rows cached ~U[1024,8192] plus
+    prefill chunks of ``chunk`` tokens (prefix 0)."""
+    rng = np.random.default_rng(seed)
+    cached = rng.integers(1024, 8192, size=n_dec, endpoint=True)
+    need = int(sum(-(-(int(c) + 1) // 16) for c in cached)) + n_chunks * (-(-chunk // 16))
+    return make_step("full_d512", seed, H_q=8, H_kv=1, D=512, P=16,
+                     num_pages=num_pages or need + 64, dec_cached=cached,
+                     pre_prefix=[0] * n_chunks, pre_qlen=[chunk] * n_chunks)
+
+
 def grpo_layer(seed: int = BASE_SEED + 5, n_prompts: int = 64, n_gen: int = 4,
                prefix: int = 256, max_completion: int = 3840,
                layers: int = 36, layer: int = 0) -> Step:
@@ -319,7 +339,8 @@ def grpo_layer(seed: int = BASE_SEED + 5, n_prompts: int = 64, n_gen: int = 4,
     return Step(name="grpo", H_q=32, H_kv=8, D=128, P=P, num_pages=num_pages,
                 window=0, scale=float(1.0 / np.sqrt(128)), dec_cached=cached,
                 dec_block_table=_table(rows, mb), used_pages=used,
-                layer_page_offset=layer * per_layer)
+                layer_page_offset=layer * per_layer, group_size=n_gen,
+                prefix_lens=np.full(n_prompts, (prefix // P) * P, np.int32))
 
 
 WORKLOADS = {
@@ -328,4 +349,5 @@ WORKLOADS = {
     "mixed_step": mixed_step,
     "sliding": sliding,
     "grpo": grpo_layer,
+    "full_d512": full_d512,
 }
