@@ -48,6 +48,7 @@ constexpr int kMergeLse = 128;  // (piece, head) log-sum-exps staged in smem for
 // windowed segments) then still spread over every SM instead of one segment
 // per CTA; large batches cut at half a CTA's share, far above this floor.
 constexpr int kMinChunkTiles = 4;
+constexpr int kMaxSortSeq = 512;  // longest-first queue order up to this batch
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -132,7 +133,7 @@ struct DecodePlan {
   static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
   static constexpr int kCombStride = D + 4;             // padded row (floats)
-  int rec, qbuf, qslot, comb, ml, bars, ok, misc, scan, sort, cum, total;
+  int rec, qbuf, qslot, comb, ml, bars, ok, misc, scan, cum, total;
   __host__ __device__ DecodePlan(int G, int batch) {
     int o = NSTAGE * kStageBytes;
     rec = o;   o += kNRec * (int)sizeof(PieceRec);
@@ -144,7 +145,6 @@ struct DecodePlan {
     ok = o;    o += NSTAGE * 4;
     misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
     scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
-    sort = o;  o += 256 * 4;  // bucket counts of the queue-order sort
     cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
     total = 1024 + o;
   }
@@ -290,57 +290,41 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
   }
   __syncthreads();
-  // queue order: sequences by chunk length, longest first, ties by index.
-  // One warp runs a stable bucket sort: lengths fall into up to 256 buckets
-  // (exact when the longest chunk is under 256 tiles, else by its top bits),
-  // bucket sizes are counted and scanned, then each group of 32 sequences
-  // is placed in index order within its bucket.  Deterministic, so every
-  // CTA derives the same queue.
-  if (warp == 0) {
-    int* hist = reinterpret_cast<int*>(smem + plan.sort);  // [256]
-    int mx = 0;
-    for (int b = lane; b < B; b += 32) mx = max(mx, s_sp[b]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    int shift = 0;
-    while ((mx >> shift) > 255) ++shift;
-    for (int i = lane; i < 256; i += 32) hist[i] = 0;
-    __syncwarp();
-    for (int b = lane; b < B; b += 32) atomicAdd(hist + (255 - (s_sp[b] >> shift)), 1);
-    __syncwarp();
-    int v[8], sum = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[k] = hist[lane * 8 + k];
-      sum += v[k];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int run = incl - sum;
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      hist[lane * 8 + k] = run;  // first position of bucket lane*8+k
-      run += v[k];
-    }
-    __syncwarp();
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      const int b = b0 + lane;
-      const bool act = b < B;
-      const int bin = act ? 255 - (s_sp[b] >> shift) : -1 - lane;  // idle lanes match nothing
-      const unsigned same = __match_any_sync(0xffffffffu, bin);
-      const int base = act ? hist[bin] : 0;
-      __syncwarp();
-      if (act) {
-        s_order[base + __popc(same & ((1u << lane) - 1u))] = b;
-        if (lane == __ffs(same) - 1) hist[bin] = base + __popc(same);
+  // queue order: sequences by chunk length, longest first, ties by index
+  // (up to kMaxSortSeq sequences; beyond, the natural order).  The rank of b
+  // is the number of sequences that come before it: the B x B comparisons
+  // run in rows of 32 spread over all threads, ranks accumulate in s_order,
+  // and every thread then scatters its sequences to their ranks.
+  if (B <= kMaxSortSeq) {
+    for (int b = tid; b < B; b += NT) s_order[b] = 0;
+    __syncthreads();
+    const int nc = (B + 31) / 32;
+    for (int u = tid; u < B * nc; u += NT) {
+      const int b = u / nc, c0 = (u - b * nc) * 32;
+      const int kb = s_sp[b];
+      const int c1 = min(B, c0 + 32);
+      int r = 0;
+      for (int c = c0; c < c1; ++c) {
+        const int kc = s_sp[c];
+        r += (kc > kb || (kc == kb && c < b)) ? 1 : 0;
       }
-      __syncwarp();
+      if (r) atomicAdd(s_order + b, r);
     }
+    __syncthreads();
+    int rk[(kMaxSortSeq + NT - 1) / NT];
+#pragma unroll
+    for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
+      const int b = tid + k * NT;
+      rk[k] = b < B ? s_order[b] : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
+      const int b = tid + k * NT;
+      if (b < B) s_order[rk[k]] = b;
+    }
+  } else {
+    for (int b = tid; b < B; b += NT) s_order[b] = b;
   }
   __syncthreads();
   for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
