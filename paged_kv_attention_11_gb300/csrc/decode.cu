@@ -43,7 +43,7 @@
 namespace pkv {
 
 constexpr int kNRec = 4;   // piece records in flight
-constexpr int kMergeLse = 128;  // (piece, head) log-sum-exps staged in smem for a merge
+constexpr int kMergeLse = 1024;  // (piece, head) log-sum-exps staged in smem for a merge
 // Shortest chunk a segment is cut into (tiles).  Small batches (a few long
 // windowed segments) then still spread over every SM instead of one segment
 // per CTA; large batches cut at half a CTA's share, far above this floor.
@@ -73,6 +73,10 @@ struct DecodeArgs {
   int32_t group_size;
   const float* pre_o;
   const float* pre_lse;
+  // CTAs that run the decode body (the last of them to find the queue empty
+  // resets it), and the CTA count a segment's fair share is taken over
+  int32_t cta_count;
+  int32_t share_ctas;
   int32_t* err;
 };
 
@@ -150,10 +154,15 @@ struct DecodePlan {
   }
 };
 
-template <int D, int NW, int NSTAGE, bool ONEBOX>
-__global__ void __launch_bounds__((NW + 2) * 32, 1)
-    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV) {
+// The decode work of one CTA: (NW + 2) warps, threads 0 .. (NW+2)*32-1 of
+// the block.  SUBSET: the block has more threads (the mixed-step kernel
+// hosts this body on part of its warps), so the body synchronises on a
+// named barrier of its own threads instead of the whole block.  `cta` is
+// this CTA's index among the a.cta_count CTAs that run the body; smem is the
+// 1024-aligned base of the dynamic shared memory.
+template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET>
+__device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
+                                           const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
   using P_ = DecodePlan<D, NW, NSTAGE>;
@@ -168,9 +177,10 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   const int G = a.G;
   const P_ plan(G, a.batch);
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  auto block_sync = [&]() {
+    if (SUBSET) named_bar_sync(1, NT);
+    else __syncthreads();
+  };
   PieceRec* recs = reinterpret_cast<PieceRec*>(smem + plan.rec);
   uint8_t* qbuf = smem + plan.qbuf;
   float* comb_o = reinterpret_cast<float*>(smem + plan.comb);   // [2][NW][G][CS]
@@ -242,8 +252,8 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     const int64_t blines = ((int64_t)B * a.max_blocks * 4 + 127) / 128;
     const char* qp = reinterpret_cast<const char*>(a.q);
     const char* bp = reinterpret_cast<const char*>(a.block_table);
-    for (int64_t l = (int64_t)blockIdx.x * NT + tid; l < qlines + blines;
-         l += (int64_t)gridDim.x * NT) {
+    for (int64_t l = (int64_t)cta * NT + tid; l < qlines + blines;
+         l += (int64_t)a.cta_count * NT) {
       const char* p = l < qlines ? qp + l * 128 : bp + (l - qlines) * 128;
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
     }
@@ -257,12 +267,12 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     int local = 0;
     for (int b = tid; b < B; b += NT) {
       int L, lo, tl, th;
-      seq_extent(a, b, L, lo, tl, th, blockIdx.x == 0);
+      seq_extent(a, b, L, lo, tl, th, cta == 0);
       const int t = th - tl;
       s_nat[b] = t;  // tiles, for now
       local += t;
       // zero-length sequences have no work item: their zero rows are written here
-      if (t == 0 && (int)(b % gridDim.x) == (int)blockIdx.x) {
+      if (t == 0 && b % a.cta_count == cta) {
         uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.H_q * D);
         for (int i = 0; i < a.H_q * D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
@@ -270,15 +280,15 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
     if (lane == 0) scan_tmp[warp] = local;
-    __syncthreads();
+    block_sync();
     if (tid == 0) {
       int64_t tot = 0;
       for (int w = 0; w < NT / 32; ++w) tot += scan_tmp[w];
       const int64_t W = tot * a.H_kv;
-      const int64_t half_share = (W + 2 * (int64_t)gridDim.x - 1) / (2 * (int64_t)gridDim.x);
+      const int64_t half_share = (W + 2 * (int64_t)a.share_ctas - 1) / (2 * (int64_t)a.share_ctas);
       s_misc[0] = (int)(half_share > kMinChunkTiles ? half_share : kMinChunkTiles);  // S_max
     }
-    __syncthreads();
+    block_sync();
   }
   const int smax = s_misc[0];
   auto nch_of = [&](int t) { return (t + smax - 1) / smax; };
@@ -289,7 +299,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     s_nat[b] = nch * a.H_kv;
     s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
   }
-  __syncthreads();
+  block_sync();
   // queue order: sequences by chunk length, longest first, ties by index
   // (up to kMaxSortSeq sequences; beyond, the natural order).  The rank of b
   // is the number of sequences that come before it: the B x B comparisons
@@ -297,7 +307,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   // and every thread then scatters its sequences to their ranks.
   if (B <= kMaxSortSeq) {
     for (int b = tid; b < B; b += NT) s_order[b] = 0;
-    __syncthreads();
+    block_sync();
     const int nc = (B + 31) / 32;
     for (int u = tid; u < B * nc; u += NT) {
       const int b = u / nc, c0 = (u - b * nc) * 32;
@@ -310,14 +320,14 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       }
       if (r) atomicAdd(s_order + b, r);
     }
-    __syncthreads();
+    block_sync();
     int rk[(kMaxSortSeq + NT - 1) / NT];
 #pragma unroll
     for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
       const int b = tid + k * NT;
       rk[k] = b < B ? s_order[b] : 0;
     }
-    __syncthreads();
+    block_sync();
 #pragma unroll
     for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
       const int b = tid + k * NT;
@@ -326,13 +336,13 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   } else {
     for (int b = tid; b < B; b += NT) s_order[b] = b;
   }
-  __syncthreads();
+  block_sync();
   for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
   // both exclusive prefixes in one pass: each thread scans a contiguous run
   {
     const int per = (B + NT - 1) / NT;
     const int i0 = tid * per;
-    __syncthreads();
+    block_sync();
     int l1 = 0, l2 = 0;
     for (int i = i0; i < i0 + per && i < B; ++i) {
       l1 += s_nat[i];
@@ -352,7 +362,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       scan_tmp[warp] = c1;
       s_misc[4 + warp] = c2;
     }
-    __syncthreads();
+    block_sync();
     int r1 = c1 - l1, r2 = c2 - l2;
     for (int w = 0; w < warp; ++w) {
       r1 += scan_tmp[w];
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       s_nat[B] = r1;
       s_sp[B] = r2;
     }
-    __syncthreads();
+    block_sync();
   }
   pdl_launch_dependents();
   const int T = s_nat[B];  // work items in the batch
@@ -537,7 +547,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
     if (lane == 0) {
       __threadfence();
       const int done = atomicAdd(a.queue + 1, 1);
-      if (done == (int)gridDim.x - 1) {
+      if (done == a.cta_count - 1) {
         a.queue[0] = 0;
         a.queue[1] = 0;
       }
@@ -727,7 +737,14 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       const int cb = k % NCB;
       mbar_wait(comb_full + cb, (k / NCB) & 1, a.err, dead);
       const int b = rec.b, g = rec.g;
-      const bool whole = rec.nch == 1 && rec.pfx == 0;
+      // a segment in one piece is written here; so is one with a prefix
+      // partial (cascade) whose suffix is one piece: the two are joined
+      // inline, with the prefix partial's weight from its log-sum-exp
+      const bool join_pfx = rec.nch == 1 && rec.pfx == 1;
+      const bool whole = rec.nch == 1;
+      const int64_t pre_row0 = (int64_t)b * a.H_q + g * G;
+      float* w_item = merge_lse + NW * kGP;  // [kGP] weights of the joined outputs
+      float* w_pfx = w_item + kGP;           // [kGP]
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
       const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
@@ -747,35 +764,69 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
         }
         merge_m[h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
         merge_inv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
+        if (join_pfx) {
+          const float li = merge_m[h];
+          const float lp = __ldcg(a.pre_lse + pre_row0 + h);
+          const float m2 = fmaxf(li, lp);
+          const float wi = li == -INFINITY ? 0.f : exp2f(li - m2);
+          const float wp = lp == -INFINITY ? 0.f : exp2f(lp - m2);
+          const float den = wi + wp;
+          w_item[h] = den > 0.f ? wi / den : 0.f;
+          w_pfx[h] = den > 0.f ? wp / den : 0.f;
+        }
       }
       __syncwarp();
-      for (int j = lane; j < G * (D / 4); j += 32) {
-        const int h = j / (D / 4), d4 = j - h * (D / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      // 4 slices per lane per pass; the prefix partial's loads (cascade)
+      // are issued before any is used
+      for (int j0 = lane; j0 < G * (D / 4); j0 += 128) {
+        float4 pv[4];
+        if (join_pfx) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = wsc[w * G + h];
-          const float4 v = *reinterpret_cast<const float4*>(co + (w * G + h) * CS + d4 * 4);
-          acc.x += sc * v.x;
-          acc.y += sc * v.y;
-          acc.z += sc * v.z;
-          acc.w += sc * v.w;
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u < G * (D / 4) ? j0 + 32 * u : 0;
+            const int h = j / (D / 4), d4 = j - h * (D / 4);
+            pv[u] = __ldcg(reinterpret_cast<const float4*>(a.pre_o + (pre_row0 + h) * D) + d4);
+          }
         }
-        const float inv = merge_inv[h];
-        acc.x *= inv;
-        acc.y *= inv;
-        acc.z *= inv;
-        acc.w *= inv;
-        if (whole) {
-          __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
-          __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-          *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) = pk;
-        } else {
-          *reinterpret_cast<float4*>(a.part_o + (pslot * G + h) * D + d4 * 4) = acc;
-          if (d4 == 0) a.part_lse[pslot * G + h] = merge_m[h];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + 32 * u;
+          if (j >= G * (D / 4)) break;
+          const int h = j / (D / 4), d4 = j - h * (D / 4);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float sc = wsc[w * G + h];
+            const float4 v = *reinterpret_cast<const float4*>(co + (w * G + h) * CS + d4 * 4);
+            acc.x += sc * v.x;
+            acc.y += sc * v.y;
+            acc.z += sc * v.z;
+            acc.w += sc * v.w;
+          }
+          const float inv = merge_inv[h];
+          acc.x *= inv;
+          acc.y *= inv;
+          acc.z *= inv;
+          acc.w *= inv;
+          if (join_pfx) {
+            const float wi = w_item[h], wp = w_pfx[h];
+            acc.x = wi * acc.x + wp * pv[u].x;
+            acc.y = wi * acc.y + wp * pv[u].y;
+            acc.z = wi * acc.z + wp * pv[u].z;
+            acc.w = wi * acc.w + wp * pv[u].w;
+          }
+          if (whole) {
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
+                pk;
+          } else {
+            *reinterpret_cast<float4*>(a.part_o + (pslot * G + h) * D + d4 * 4) = acc;
+            if (d4 == 0) a.part_lse[pslot * G + h] = merge_m[h];
+          }
         }
       }
       __syncwarp();
@@ -796,91 +847,119 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
           // the segment's chunks, plus the prefix partial as chunk nch
           const int np = rec.nch + rec.pfx;
           const int64_t pre_row = (int64_t)b * a.H_q + g * G;
-          auto lse_glob = [&](int c, int h) -> float {
-            return c < rec.nch ? __ldcg(a.part_lse + ((int64_t)rec.slot0 + c) * G + h)
-                               : __ldcg(a.pre_lse + pre_row + h);
+          auto l_src = [&](int c, int h) -> const float* {
+            return c < rec.nch ? a.part_lse + ((int64_t)rec.slot0 + c) * G + h
+                               : a.pre_lse + pre_row + h;
           };
-          // (1) every (chunk, head) log2-sum-exp in one round of loads, the
-          //     per-head max and weight sum from shared memory
-          for (int i = lane; i < np * G && i < kMergeLse; i += 32) merge_lse[i] = lse_glob(i / G, i % G);
+          auto o_src = [&](int c, int h) -> const float* {
+            return c < rec.nch ? a.part_o + (((int64_t)rec.slot0 + c) * G + h) * D
+                               : a.pre_o + (pre_row + h) * D;
+          };
+          // (1) the (chunk, head) log2-sum-exps, staged in shared memory in
+          //     one round of loads when they fit (a segment cut into more
+          //     than kMergeLse / G chunks reads them from L2 instead)
+          const int nl = np * G;
+          const bool staged = nl <= kMergeLse;
+          if (staged)
+            for (int i = lane; i < nl; i += 32) merge_lse[i] = __ldcg(l_src(i / G, i % G));
           __syncwarp();
-          auto lse_at = [&](int c, int h) -> float {
-            return c * G + h < kMergeLse ? merge_lse[c * G + h] : lse_glob(c, h);
-          };
-          if (lane < G) {
+          if (lane < G) {  // per head: max and 1 / sum of the weights
             const int h = lane;
-            float M = -INFINITY;
-            for (int c = 0; c < np; ++c) M = fmaxf(M, lse_at(c, h));
-            float sum = 0.f;
-            if (M != -INFINITY)
-              for (int c = 0; c < np; ++c) sum += exp2f(lse_at(c, h) - M);
+            float M = -INFINITY, sum = 0.f;
+            if (staged) {
+              for (int c = 0; c < np; ++c) M = fmaxf(M, merge_lse[c * G + h]);
+              if (M != -INFINITY)
+                for (int c = 0; c < np; ++c) sum += exp2f(merge_lse[c * G + h] - M);
+            } else {
+              for (int c = 0; c < np; ++c) M = fmaxf(M, __ldcg(l_src(c, h)));
+              if (M != -INFINITY)
+                for (int c = 0; c < np; ++c) sum += exp2f(__ldcg(l_src(c, h)) - M);
+            }
             merge_m[h] = M;
             merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
           }
           __syncwarp();
-          // (2) weighted sum of the chunks' outputs, 4 dims (a slice) per
-          //     lane and load: each lane keeps kMU slices x kMC chunks of
-          //     loads in flight, so a merge costs a few L2 round trips
-          //     instead of one per (slice, chunk group).  Every output sums
-          //     its chunks in chunk order.
+          // (2) staged: the normalised weight of every (chunk, head)
+          if (staged) {
+            for (int i = lane; i < nl; i += 32) {
+              const int h = i % G;
+              const float M = merge_m[h];
+              merge_lse[i] = M == -INFINITY ? 0.f : exp2f(merge_lse[i] - M) * merge_inv[h];
+            }
+          }
+          __syncwarp();
+          // (3) weighted sum of the chunks' outputs, 4 dims (a slice) per
+          //     lane and load.  Each lane keeps kMU slices x kMC chunks of
+          //     loads in flight; the weights come from shared memory (or,
+          //     unstaged, from loads issued in the same batch), so a merge
+          //     costs a few L2 round trips.  Every output sums its chunks in
+          //     chunk order.
           constexpr int kMU = 4, kMC = 4;
           const int nslice = G * (D / 4);
           for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
             float4 acc[kMU];
-            int hh[kMU];
+            int hh[kMU], dd[kMU];
 #pragma unroll
             for (int u = 0; u < kMU; ++u) {
               acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-              const int j = j0 + 32 * u;
-              hh[u] = j < nslice ? j / (D / 4) : 0;
+              const int j = j0 + 32 * u < nslice ? j0 + 32 * u : 0;
+              hh[u] = j / (D / 4);
+              dd[u] = j - hh[u] * (D / 4);
             }
             for (int c0 = 0; c0 < np; c0 += kMC) {
               float4 v[kMU][kMC];
+              float w[kMU][kMC];
 #pragma unroll
-              for (int u = 0; u < kMU; ++u) {
-                const int j = j0 + 32 * u;
-                const int h = hh[u], d4 = j - h * (D / 4);
+              for (int u = 0; u < kMU; ++u)
 #pragma unroll
                 for (int cc = 0; cc < kMC; ++cc) {
-                  const int c = c0 + cc;
-                  v[u][cc] = make_float4(0.f, 0.f, 0.f, 0.f);
-                  if (j < nslice && c < np && merge_m[h] != -INFINITY) {
-                    const float* src = c < rec.nch
-                                           ? a.part_o + (((int64_t)rec.slot0 + c) * G + h) * D
-                                           : a.pre_o + (pre_row + h) * D;
-                    v[u][cc] = __ldcg(reinterpret_cast<const float4*>(src) + d4);
+                  const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
+                  v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
+                }
+              if (staged) {
+#pragma unroll
+                for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc)
+                    w[u][cc] = c0 + cc < np ? merge_lse[(c0 + cc) * G + hh[u]] : 0.f;
+              } else {
+#pragma unroll
+                for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc) {
+                    const int c = c0 + cc < np ? c0 + cc : np - 1;
+                    w[u][cc] = __ldcg(l_src(c, hh[u]));
                   }
+#pragma unroll
+                for (int u = 0; u < kMU; ++u) {
+                  const float M = merge_m[hh[u]];
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc)
+                    w[u][cc] = (c0 + cc < np && M != -INFINITY)
+                                   ? exp2f(w[u][cc] - M) * merge_inv[hh[u]]
+                                   : 0.f;
                 }
               }
 #pragma unroll
-              for (int u = 0; u < kMU; ++u) {
-                const float M = merge_m[hh[u]];
+              for (int u = 0; u < kMU; ++u)
 #pragma unroll
                 for (int cc = 0; cc < kMC; ++cc) {
-                  const int c = c0 + cc;
-                  if (c < np && M != -INFINITY) {
-                    const float w = exp2f(lse_at(c, hh[u]) - M);
-                    acc[u].x += w * v[u][cc].x;
-                    acc[u].y += w * v[u][cc].y;
-                    acc[u].z += w * v[u][cc].z;
-                    acc[u].w += w * v[u][cc].w;
-                  }
+                  acc[u].x += w[u][cc] * v[u][cc].x;
+                  acc[u].y += w[u][cc] * v[u][cc].y;
+                  acc[u].z += w[u][cc] * v[u][cc].z;
+                  acc[u].w += w[u][cc] * v[u][cc].w;
                 }
-              }
             }
 #pragma unroll
             for (int u = 0; u < kMU; ++u) {
-              const int j = j0 + 32 * u;
-              if (j >= nslice) continue;
-              const int h = hh[u], d4 = j - h * (D / 4);
-              const float inv = merge_inv[h];
-              __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x * inv, acc[u].y * inv);
-              __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z * inv, acc[u].w * inv);
+              if (j0 + 32 * u >= nslice) continue;
+              __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+              __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
               uint2 pk;
               pk.x = *reinterpret_cast<uint32_t*>(&lo2);
               pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-              *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
-                  pk;
+              *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + hh[u]) * D +
+                                        dd[u] * 4) = pk;
             }
           }
           if (lane == 0) a.seg_count[seg] = 0;
@@ -889,6 +968,16 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
       }
     }
   }
+}
+
+template <int D, int NW, int NSTAGE, bool ONEBOX>
+__global__ void __launch_bounds__((NW + 2) * 32, 1)
+    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  decode_cta<D, NW, NSTAGE, ONEBOX, false>(a, tmK, tmV, smem, blockIdx.x);
 }
 
 // --------------------------------------------------------------- host side
@@ -983,6 +1072,8 @@ static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void
   if (per_sm < 1) per_sm = 1;
   // persistent grid: every resident CTA takes items until the queue is empty
   const int64_t n = (int64_t)num_sms * per_sm;
+  a.cta_count = (int32_t)n;
+  a.share_ctas = (int32_t)n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n);
   cfg.blockDim = dim3((C::NW + 2) * 32);
