@@ -298,6 +298,16 @@ class DeviceStep:
                                    s.window, workspace=self.ws, err_flag=self.err,
                                    stream=stream)
 
+    def mixed(self, stream, decode_ctas=0):
+        """Decode rows and prefill chunks in one paged_attn_mixed launch."""
+        s = self.step
+        self.pkv.paged_attn_mixed(self.out_dec, self.q_dec, self.dec_bt, self.dec_lens,
+                                  s.max_seq_len_dec(), self.out_pre, self.q_pre, self.cu_q,
+                                  self.cu_k, self.pre_bt, s.max_seqlen_q(), s.max_seqlen_k(),
+                                  self.k_cache, self.v_cache, s.scale, s.window,
+                                  decode_ctas=decode_ctas, workspace=self.ws, err_flag=self.err,
+                                  stream=stream)
+
     def decode_shared_prefix(self, stream):
         """The same decode through the shared-prefix (cascade) entry point."""
         import torch
@@ -561,6 +571,20 @@ def run_mixed(args, device, stream, flush, rank):
     tokens = step.n_new_tokens
     fl = varlen_flops(step)
     hbm_peak, tf_peak, _, src = peaks()
+    # the same step with decode and prefill in one launch (paged_attn_mixed)
+    try:
+        fused_step = time_steps([ds.append, ds.mixed], args.steps, args.warmup, stream, flush,
+                                phase_events=False)
+        torch.cuda.synchronize()
+        if int(ds.err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(ds.err.item())}")
+        fms = float(np.mean([sum(p) for p in fused_step]))
+        fused = {"value": round(tokens / (fms * 1e-3), 1), "unit": "tokens/s",
+                 "ms_per_step": round(fms, 5),
+                 "note": "append, then paged_attn_mixed: decode rows and prefill chunks in one "
+                         "persistent launch (split chosen by the library)"}
+    except Exception as e:
+        fused = {"unavailable": f"{type(e).__name__}: {e}"}
     # the same step with q/k RMSNorm and the rotary embedding fused into the
     # append (the attention layer's whole input transform)
     try:
@@ -604,6 +628,7 @@ def run_mixed(args, device, stream, flush, rank):
             "decode_gb_s": round(decode_bytes(step) / (ph[2] * 1e-3) / 1e9, 2),
             "append_gb_s": round(append_bytes(step, tokens) / (ph[0] * 1e-3) / 1e9, 2),
             "append_bytes": int(append_bytes(step, tokens)),
+            "single_launch": fused,
             "with_rope": with_rope}
 
 

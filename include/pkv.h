@@ -229,6 +229,49 @@ pkv_status paged_attn_varlen(void* out, const void* q,
                              int32_t* err_flag, void* stream);
 
 /*
+ * paged_attn_mixed - the attention of one continuous-batching step in a
+ * single persistent launch: decode rows (as paged_attn_decode) and causal
+ * prefill chunks (as paged_attn_varlen with causal = 1) over the same page
+ * pools.  Source: scripts/benchmarks commit log, batch-sweep commit (vLLM's
+ * chunked prefill packs a step's prefill and decode into the same kernels);
+ * README, "Why continuous batching is still slower than vLLM on this
+ * workload" (separate prefill and decode passes per step).
+ *
+ *   dec_*        the decode half, meaning as paged_attn_decode (dec_batch 0:
+ *                no decode rows)
+ *   pre_*, cu_seq_lens_q/k, max_seqlen_q/k, total_q
+ *                the prefill half, meaning as paged_attn_varlen (pre_batch
+ *                or total_q 0: no prefill)
+ *   window       applies to both halves (<= 0: none)
+ *   decode_ctas  CTAs (one per SM) that start with decode while the others
+ *                run the prefill; those join the decode queue when their
+ *                prefill work is done.  <= 0: chosen from the shapes.
+ *   workspace    as paged_attn_decode, for dec_batch rows
+ *                (paged_attn_decode_workspace_size(dec_batch, ...) bytes)
+ *
+ * Results equal those of the two separate calls (decode may differ in
+ * rounding with the split, like paged_attn_decode between batch shapes).
+ * Supported: head_dim 128, the decode and prefill limits of the separate
+ * calls (group <= 8 dividing 128, page_size a divisor or multiple of 128,
+ * pre_batch <= 1024); else PKV_ERR_UNSUPPORTED.  The prefill half must not
+ * write rows that the decode half reads (distinct out tensors).
+ */
+pkv_status paged_attn_mixed(void* dec_out, const void* dec_q,
+                            const int32_t* dec_block_table, int32_t dec_max_blocks_per_seq,
+                            const int32_t* dec_seq_lens, int32_t dec_batch,
+                            int32_t dec_max_seq_len,
+                            void* pre_out, const void* pre_q,
+                            const int32_t* cu_seq_lens_q, const int32_t* cu_seq_lens_k,
+                            const int32_t* pre_block_table, int32_t pre_max_blocks_per_seq,
+                            int32_t pre_batch, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                            int32_t total_q,
+                            const void* k_cache, const void* v_cache,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t page_size, int64_t num_pages, float scale, int32_t window,
+                            int32_t decode_ctas, void* workspace, size_t workspace_bytes,
+                            int32_t* err_flag, void* stream);
+
+/*
  * paged_attn_decode_static - paged_attn_decode for callers that cannot
  * allocate device memory.  (Not an operation of the pages: it exists for
  * callers of this library that may not call cudaMalloc on the attention

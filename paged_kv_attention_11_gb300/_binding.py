@@ -35,6 +35,10 @@ _SIGS = {
     "paged_attn_decode_shared_prefix": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32,
                                         _c_i32, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64,
                                         _c_i32, _c_f, _c_p, ctypes.c_size_t, _c_p, _c_p],
+    "paged_attn_mixed": [_c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p,
+                         _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i32,
+                         _c_i32, _c_i32, _c_i32, _c_i64, _c_f, _c_i32, _c_i32, _c_p,
+                         ctypes.c_size_t, _c_p, _c_p],
     "pkv_rope_table": [_c_p, _c_i32, _c_i32, ctypes.c_double, _c_p],
     "paged_kv_append_rope": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p,
                              _c_f, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_p, _c_p],
@@ -231,6 +235,40 @@ def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         D, P, num_pages, float(scale), 1 if causal else 0, int(window), _ptr(err_flag),
         _stream(stream)))
     return out
+
+
+def paged_attn_mixed(dec_out: torch.Tensor, dec_q: torch.Tensor, dec_block_table: torch.Tensor,
+                     dec_seq_lens: torch.Tensor, dec_max_seq_len: int, pre_out: torch.Tensor,
+                     pre_q: torch.Tensor, cu_seq_lens_q: torch.Tensor,
+                     cu_seq_lens_k: torch.Tensor, pre_block_table: torch.Tensor,
+                     max_seqlen_q: int, max_seqlen_k: int, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, scale: float, window: int = 0,
+                     decode_ctas: int = 0, workspace: Optional[torch.Tensor] = None,
+                     err_flag: Optional[torch.Tensor] = None, stream=None):
+    """One continuous-batching step in one launch: decode rows (dec_q/dec_out
+    [B, H_q, D]) and causal prefill chunks (pre_q/pre_out [total_q, H_q, D],
+    cu_seq_lens_* [Bp+1]).  Workspace handling as paged_attn_decode."""
+    for n, t in (("dec_out", dec_out), ("dec_q", dec_q), ("pre_out", pre_out),
+                 ("pre_q", pre_q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    for n, t in (("dec_block_table", dec_block_table), ("dec_seq_lens", dec_seq_lens),
+                 ("cu_seq_lens_q", cu_seq_lens_q), ("cu_seq_lens_k", cu_seq_lens_k),
+                 ("pre_block_table", pre_block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    B, H_q, D = dec_q.shape
+    total_q = pre_q.shape[0]
+    num_pages, H_kv, P, _ = k_cache.shape
+    if workspace is None:
+        workspace = decode_workspace(dec_q.device, _stream(stream), max(B, 1), H_q, H_kv, D)
+    _check("paged_attn_mixed", lib().paged_attn_mixed(
+        _ptr(dec_out), _ptr(dec_q), _ptr(dec_block_table), dec_block_table.shape[1],
+        _ptr(dec_seq_lens), B, int(dec_max_seq_len), _ptr(pre_out), _ptr(pre_q),
+        _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), _ptr(pre_block_table),
+        pre_block_table.shape[1], cu_seq_lens_q.shape[0] - 1, int(max_seqlen_q),
+        int(max_seqlen_k), total_q, _ptr(k_cache), _ptr(v_cache), H_q, H_kv, D, P, num_pages,
+        float(scale), int(window), int(decode_ctas), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)))
 
 
 def paged_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

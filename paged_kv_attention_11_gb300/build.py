@@ -19,8 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libpkv.so")
 SOURCES = ["api.cu", "append.cu", "decode.cu", "varlen.cu", "decode_static.cu", "rope_append.cu",
-           "prefix.cu"]
-HEADERS = ["common.cuh", "exp2_math.cuh", "kernels.h", "tcgen05.cuh", "tile16.cuh", "tmap.h"]
+           "prefix.cu", "mixed.cu"]
+HEADERS = ["common.cuh", "decode_body.cuh", "exp2_math.cuh", "kernels.h", "tcgen05.cuh",
+           "tile16.cuh", "tmap.h", "varlen_body.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

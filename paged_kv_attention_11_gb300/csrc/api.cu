@@ -1,5 +1,7 @@
 // C ABI layer: argument validation, TMA descriptor encoding, dispatch.
 // Declarations and the contract of every entry point are in include/pkv.h.
+#include <string.h>
+
 #include <mutex>
 #include <string>
 
@@ -243,6 +245,97 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
                                      num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                                      scale, causal, window, err_flag,
                                      static_cast<cudaStream_t>(stream), sms);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec_block_table,
+                            int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens,
+                            int32_t dec_batch, int32_t dec_max_seq_len, void* pre_out,
+                            const void* pre_q, const int32_t* cu_seq_lens_q,
+                            const int32_t* cu_seq_lens_k, const int32_t* pre_block_table,
+                            int32_t pre_max_blocks_per_seq, int32_t pre_batch,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+                            const void* k_cache, const void* v_cache, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                            int64_t num_pages, float scale, int32_t window, int32_t decode_ctas,
+                            void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                            void* stream) {
+  if (dec_batch < 0 || pre_batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return PKV_ERR_INVALID;
+  if (!(scale >= 0.f)) return PKV_ERR_INVALID;  // NaN or negative
+  // the decode half: every check of paged_attn_decode
+  const pkv_status chk =
+      pkv::decode_check_args(dec_out, dec_q, k_cache, v_cache, dec_block_table,
+                             dec_batch > 0 ? dec_max_blocks_per_seq : 1, dec_seq_lens, dec_batch,
+                             num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                             dec_max_seq_len, scale);
+  if (chk != PKV_OK) return chk;
+  // the prefill half: the checks of paged_attn_varlen (causal)
+  const int G = num_q_heads / num_kv_heads;
+  const bool has_var = pre_batch > 0 && total_q > 0;
+  if (has_var) {
+    if (pre_max_blocks_per_seq <= 0) return PKV_ERR_INVALID;
+    if (!pre_out || !pre_q || !cu_seq_lens_q || !cu_seq_lens_k || !pre_block_table)
+      return PKV_ERR_INVALID;
+    if (!aligned16(pre_out) || !aligned16(pre_q)) return PKV_ERR_INVALID;
+    if ((128 % G) != 0 || pre_batch > 1024) return PKV_ERR_UNSUPPORTED;
+  }
+  if (head_dim != 128 || (128 % page_size != 0 && page_size % 128 != 0))
+    return PKV_ERR_UNSUPPORTED;
+  if (dec_batch == 0 && !has_var) return PKV_OK;
+  if (dec_batch > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return PKV_ERR_INVALID;
+  int sms = 0;
+  if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  if (dec_batch > 0 &&
+      workspace_bytes <
+          pkv::decode_workspace_bytes(dec_batch, num_q_heads, num_kv_heads, head_dim, sms))
+    return PKV_ERR_INVALID;
+  pkv::VarlenMaps maps;
+  if (has_var) {
+    const int box_rows = page_size < 128 ? page_size : 128;
+    if (!encode_q_map(&maps.q, pre_q, head_dim, G, num_kv_heads, total_q) ||
+        !encode_pool_map_groups(&maps.k, k_cache, head_dim, page_size, num_pages, num_kv_heads,
+                                box_rows) ||
+        !encode_pool_map_groups(&maps.v, v_cache, head_dim, page_size, num_pages, num_kv_heads,
+                                box_rows))
+      return cuda_fail(cudaErrorInvalidValue);
+  } else {
+    memset(&maps, 0, sizeof(maps));
+  }
+  pkv::MixedLaunch L;
+  L.dec_out = dec_out;
+  L.dec_q = dec_q;
+  L.dec_block_table = dec_block_table;
+  L.dec_seq_lens = dec_seq_lens;
+  L.dec_max_blocks = dec_max_blocks_per_seq;
+  L.dec_batch = dec_batch;
+  L.dec_max_seq_len = dec_max_seq_len;
+  L.pre_out = pre_out;
+  L.pre_q = pre_q;
+  L.cu_q = cu_seq_lens_q;
+  L.cu_k = cu_seq_lens_k;
+  L.pre_block_table = pre_block_table;
+  L.pre_max_blocks = pre_max_blocks_per_seq;
+  L.pre_batch = has_var ? pre_batch : 0;
+  L.max_seqlen_q = max_seqlen_q;
+  L.max_seqlen_k = max_seqlen_k;
+  L.total_q = total_q;
+  L.k_cache = k_cache;
+  L.v_cache = v_cache;
+  L.H_q = num_q_heads;
+  L.H_kv = num_kv_heads;
+  L.D = head_dim;
+  L.P = page_size;
+  L.num_pages = num_pages;
+  L.scale = scale;
+  L.window = window;
+  L.decode_ctas = decode_ctas;
+  L.workspace = workspace;
+  L.workspace_bytes = workspace_bytes;
+  L.err = err_flag;
+  cudaError_t e = pkv::launch_mixed(L, maps, static_cast<cudaStream_t>(stream), sms);
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }

@@ -1,0 +1,1017 @@
+// paged_attn_decode: one query per sequence over its paged K/V prefix.
+//
+// Semantics: scripts/benchmarks commit log, "Why this works" (decode reads
+// the pool through the page table; the new token is written first, so the
+// query at position len-1 sees keys 0..len-1) and the Gemma-4 sliding-window
+// commit (key allowed iff q_pos - k_pos < window).
+//
+// Design (GB300):
+//  * Work item = a (sequence, kv head) "segment" of 16-key tiles, or a chunk
+//    of one: a segment longer than half of a CTA's fair share of the batch
+//    is cut into equal chunks.  One persistent CTA per SM takes items from
+//    a device-side queue (an atomic counter in the workspace) in
+//    longest-first order, so the SMs finish together whatever the length
+//    mix, and only the few long segments need a merge.
+//  * Producer warp: grabs the next item, writes a record (sequence, head,
+//    tiles, ...) and the G query rows into a 4-deep record ring in shared
+//    memory, then streams the item's K and V tiles: page ids from the
+//    block table (32 per coalesced load), TMA boxes per 16-key tile
+//    (128-byte swizzle) into a deep NSTAGE ring.
+//  * NW consumer warps: take the tiles of each item round-robin.  Per tile
+//    a warp computes S^T = K Q^T (16 keys x 8 heads, GQA group padded to
+//    8) with mma.sync, does the online softmax (exp2, warp shuffles),
+//    transposes P in registers with movmatrix and accumulates
+//    O^T = V^T P^T with mma.sync.  At the end of an item it hands its
+//    (m, l, O) state to the epilogue warp through a double buffer and goes
+//    straight on: no CTA-wide barrier in the stream.
+//  * Epilogue warp: combines the consumer states of an item (log-sum-exp
+//    weights); a whole segment is written as the bf16 output, a chunk as a
+//    partial (o, lse) in the workspace.  The last CTA to deliver a chunk of
+//    a segment -- found with a per-segment arrival counter -- merges the
+//    chunks and writes the output, then resets the counter.  The last CTA
+//    to find the queue empty resets the queue.  No CTA waits for another.
+//  * K/V bytes are read from HBM exactly once.  Launched with programmatic
+//    dependent launch: the prologue overlaps the previous kernel in the
+//    stream; griddepcontrol.wait precedes every read of the inputs.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tile16.cuh"
+
+namespace pkv {
+
+constexpr int kNRec = 4;   // piece records in flight
+constexpr int kMergeLse = 1024;  // (piece, head) log-sum-exps staged in smem for a merge
+// Shortest chunk a segment is cut into (tiles).  Small batches (a few long
+// windowed segments) then still spread over every SM instead of one segment
+// per CTA; large batches cut at half a CTA's share, far above this floor.
+constexpr int kMinChunkTiles = 4;
+constexpr int kMaxSortSeq = 512;  // longest-first queue order up to this batch
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t max_blocks;
+  int32_t batch;
+  int32_t H_q, H_kv, G, P;
+  int64_t num_pages;
+  int32_t window;
+  float scale_log2;
+  int32_t* seg_count;  // [batch * H_kv] arrival counters, zero between calls
+  int32_t* queue;      // [2]: next item, CTAs done; zero between calls
+  float* part_lse;     // [(S + N) * G]
+  float* part_o;       // [(S + N) * G * D]
+  // shared-prefix (cascade) decode: null prefix_lens = plain decode.  A
+  // sequence of group b / group_size whose length exceeds the group's shared
+  // prefix attends only its suffix here, and its result is merged with the
+  // prefix pass's partial (pre_o, pre_lse at row b * H_q + head).
+  const int32_t* prefix_lens;
+  int32_t group_size;
+  const float* pre_o;
+  const float* pre_lse;
+  // CTAs that run the decode body (the last of them to find the queue empty
+  // resets it), and the CTA count a segment's fair share is taken over
+  int32_t cta_count;
+  int32_t share_ctas;
+  int32_t* err;
+};
+
+// Keys [lo, L) of sequence b are attended here; returns the tile range and
+// whether a prefix partial covers keys [0, lo).
+__device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, int& lo,
+                                           int& t_lo, int& t_hi, bool flag, int* pfx = nullptr) {
+  int len = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks * a.P;
+  if (len < 0 || len > cap) {
+    if (flag) raise_err(a.err, PKV_DEVERR_LEN);
+    len = len < 0 ? 0 : cap;
+  }
+  L = len;
+  lo = (a.window > 0 && len > a.window) ? len - a.window : 0;
+  int has_pfx = 0;
+  if (a.prefix_lens != nullptr) {
+    const int pl = shared_prefix_len(a.prefix_lens, b / a.group_size, a.P, cap);
+    if (pl > 0 && len > pl) {
+      lo = pl;
+      has_pfx = 1;
+    }
+  }
+  if (pfx) *pfx = has_pfx;
+  t_lo = lo / kTile;
+  t_hi = (len + kTile - 1) / kTile;
+}
+
+// A piece as the producer hands it to the consumers and the epilogue.
+struct PieceRec {
+  int b, g;          // sequence, kv head
+  int first_tile;    // first 16-key tile (absolute, within the sequence)
+  int n;             // tiles in the item; -1 terminates the stream
+  int L, lo;         // attended keys [lo, L)
+  int nch;           // chunks of the segment (1: the item is the whole segment)
+  int slot0;         // partial slot of chunk 0 of the segment
+  int chunk;         // this item's chunk
+  int pfx;           // 1: a prefix partial joins the merge (cascade)
+};
+
+// Head dims of 512 and more keep the query rows in shared memory (read with
+// ldmatrix per tile) instead of registers, which then hold only O, and hand
+// consumer states to the epilogue through one combine buffer instead of two.
+template <int D>
+struct DecodeLayout {
+  static constexpr bool kQSmem = D >= 512;
+  static constexpr int kNComb = kQSmem ? 1 : 2;
+  // query rows in a record slot: kQSmem: kGP rows padded by 16 bytes (rows
+  // G..kGP-1 zero), so that the 8 rows of an ldmatrix hit distinct banks
+  static constexpr int kQRowBytes = kQSmem ? D * 2 + 16 : D * 2;
+};
+
+// Shared-memory plan (byte offsets from the 1024-aligned base); depends on
+// the runtime GQA group and batch.
+template <int D, int NW, int NSTAGE>
+struct DecodePlan {
+  using Lay = DecodeLayout<D>;
+  static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+  static constexpr int kCombStride = D + 4;             // padded row (floats)
+  int rec, qbuf, qslot, comb, ml, bars, ok, misc, scan, cum, total;
+  __host__ __device__ DecodePlan(int G, int batch) {
+    int o = NSTAGE * kStageBytes;
+    rec = o;   o += kNRec * (int)sizeof(PieceRec);
+    qslot = (Lay::kQSmem ? kGP : G) * Lay::kQRowBytes;
+    qbuf = o;  o += kNRec * qslot;
+    comb = o;  o += Lay::kNComb * NW * G * kCombStride * 4;
+    ml = o;    o += Lay::kNComb * NW * G * 2 * 4;
+    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 2 * Lay::kNComb) * 8;
+    ok = o;    o += NSTAGE * 4;
+    misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
+    scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
+    cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
+    total = 1024 + o;
+  }
+};
+
+// The decode work of one CTA: (NW + 2) warps, threads 0 .. (NW+2)*32-1 of
+// the block.  SUBSET: the block has more threads (the mixed-step kernel
+// hosts this body on part of its warps), so the body synchronises on a
+// named barrier of its own threads instead of the whole block.  `cta` is
+// this CTA's index among the a.cta_count CTAs that run the body; smem is the
+// 1024-aligned base of the dynamic shared memory.
+template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET>
+__device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
+                                           const CUtensorMap& tmV, uint8_t* smem, int cta) {
+  static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
+  // a consumer holds two stages (its tiles t and t + NW) at once; the stage
+  // of tile t + NW is refilled after tile t + NW - NSTAGE <= t - NW, which
+  // the same warp released in an earlier step
+  static_assert(NSTAGE >= 2 * NW, "tile pairs");
+  static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+  using P_ = DecodePlan<D, NW, NSTAGE>;
+  using Lay = DecodeLayout<D>;
+  constexpr bool QS = Lay::kQSmem;
+  constexpr int NCB = Lay::kNComb;
+  constexpr int NT = (NW + 2) * 32;
+  constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
+  constexpr int kBoxBytes = kTile * 128;
+  constexpr int CS = P_::kCombStride;
+  constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;  // producer lanes issuing TMA
+  const int G = a.G;
+  const P_ plan(G, a.batch);
+
+  auto block_sync = [&]() {
+    if (SUBSET) named_bar_sync(1, NT);
+    else __syncthreads();
+  };
+  PieceRec* recs = reinterpret_cast<PieceRec*>(smem + plan.rec);
+  uint8_t* qbuf = smem + plan.qbuf;
+  float* comb_o = reinterpret_cast<float*>(smem + plan.comb);   // [2][NW][G][CS]
+  float* comb_ml = reinterpret_cast<float*>(smem + plan.ml);    // [2][NW][G][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
+  uint64_t* empty = full + NSTAGE;
+  uint64_t* rec_full = empty + NSTAGE;
+  uint64_t* rec_empty = rec_full + kNRec;
+  uint64_t* comb_full = rec_empty + kNRec;  // [NCB]
+  uint64_t* comb_empty = comb_full + NCB;   // [NCB]
+  int* stage_ok = reinterpret_cast<int*>(smem + plan.ok);
+  float* merge_m = reinterpret_cast<float*>(smem + plan.misc);
+  float* merge_inv = merge_m + kGP;
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(merge_inv + kGP);
+  float* merge_lse = merge_inv + kGP + 4;  // [kMergeLse]
+  int* scan_tmp = reinterpret_cast<int*>(smem + plan.scan);
+  int* s_misc = scan_tmp + NW + 4;                              // [4]
+  int* s_nat = reinterpret_cast<int*>(smem + plan.cum);         // [B+1] items before b
+  int* s_sp = s_nat + (a.batch + 1);                            // [B+1] sorted prefix
+  int* s_order = s_sp + (a.batch + 1);                          // [B] sequences, longest first
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int B = a.batch;
+
+  // one barrier per thread (the block has more threads than barriers)
+  static_assert(2 * NSTAGE + 2 * kNRec + 2 * NCB <= NT, "barrier init");
+  {
+    const int i = tid;
+    if (i < NSTAGE) {
+      mbar_init(full + i, 1);
+    } else if (i < 2 * NSTAGE) {
+      mbar_init(full + i, 1);  // empty[i - NSTAGE]
+    } else if (i < 2 * NSTAGE + kNRec) {
+      mbar_init(rec_full + (i - 2 * NSTAGE), 32);
+    } else if (i < 2 * NSTAGE + 2 * kNRec) {
+      mbar_init(rec_full + (i - 2 * NSTAGE), NW * 32 + 32);  // rec_empty
+    } else if (i < 2 * NSTAGE + 2 * kNRec + NCB) {
+      mbar_init(comb_full + (i - 2 * NSTAGE - 2 * kNRec), NW * 32);
+    } else if (i < 2 * NSTAGE + 2 * kNRec + 2 * NCB) {
+      mbar_init(comb_full + (i - 2 * NSTAGE - 2 * kNRec), 32);  // comb_empty
+    }
+    if (i < 2 * NSTAGE + 2 * kNRec + 2 * NCB) fence_mbar_init();
+  }
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (QS) {
+    // rows G..kGP-1 of every query slot stay zero (the padded heads of the
+    // mma N dimension); rows < G are written per item
+    for (int i = tid; i < kNRec * (kGP - G) * (Lay::kQRowBytes / 16); i += NT) {
+      const int per = (kGP - G) * (Lay::kQRowBytes / 16);
+      const int sl = i / per, j = i - sl * per;
+      reinterpret_cast<uint4*>(qbuf + sl * plan.qslot + G * Lay::kQRowBytes)[j] =
+          make_uint4(0, 0, 0, 0);
+    }
+  }
+  pdl_wait();  // inputs may come from the previous kernel in the stream
+  // the producer's first queue grab is issued now; its latency hides behind
+  // the prologue
+  int first_grab = 0;
+  if (warp == NW && lane == 0) first_grab = atomicAdd(a.queue, 1);
+  {
+    // the query rows and block tables, spread over the grid, into L2: the
+    // producers' first items then find them there
+    const int64_t qlines = ((int64_t)B * a.H_q * D * 2 + 127) / 128;
+    const int64_t blines = ((int64_t)B * a.max_blocks * 4 + 127) / 128;
+    const char* qp = reinterpret_cast<const char*>(a.q);
+    const char* bp = reinterpret_cast<const char*>(a.block_table);
+    for (int64_t l = (int64_t)cta * NT + tid; l < qlines + blines;
+         l += (int64_t)a.cta_count * NT) {
+      const char* p = l < qlines ? qp + l * 128 : bp + (l - qlines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+  }
+
+  // ---- work items (every CTA computes the same list, in smem) ----
+  // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
+  // than S_max = max(kMinChunkTiles, W / (2N)) tiles is cut into nch_b
+  // equal chunks.
+  {
+    int local = 0;
+    for (int b = tid; b < B; b += NT) {
+      int L, lo, tl, th;
+      seq_extent(a, b, L, lo, tl, th, cta == 0);
+      const int t = th - tl;
+      s_nat[b] = t;  // tiles, for now
+      local += t;
+      // zero-length sequences have no work item: their zero rows are written here
+      if (t == 0 && b % a.cta_count == cta) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.H_q * D);
+        for (int i = 0; i < a.H_q * D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0) scan_tmp[warp] = local;
+    block_sync();
+    if (tid == 0) {
+      int64_t tot = 0;
+      for (int w = 0; w < NT / 32; ++w) tot += scan_tmp[w];
+      const int64_t W = tot * a.H_kv;
+      const int64_t half_share = (W + 2 * (int64_t)a.share_ctas - 1) / (2 * (int64_t)a.share_ctas);
+      s_misc[0] = (int)(half_share > kMinChunkTiles ? half_share : kMinChunkTiles);  // S_max
+    }
+    block_sync();
+  }
+  const int smax = s_misc[0];
+  auto nch_of = [&](int t) { return (t + smax - 1) / smax; };
+  // items per sequence (natural order) and chunk length (queue order key)
+  for (int b = tid; b < B; b += NT) {
+    const int t = s_nat[b];
+    const int nch = nch_of(t);
+    s_nat[b] = nch * a.H_kv;
+    s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
+  }
+  block_sync();
+  // queue order: sequences by chunk length, longest first, ties by index
+  // (up to kMaxSortSeq sequences; beyond, the natural order).  The rank of b
+  // is the number of sequences that come before it: the B x B comparisons
+  // run in rows of 32 spread over all threads, ranks accumulate in s_order,
+  // and every thread then scatters its sequences to their ranks.
+  if (B <= kMaxSortSeq) {
+    for (int b = tid; b < B; b += NT) s_order[b] = 0;
+    block_sync();
+    const int nc = (B + 31) / 32;
+    for (int u = tid; u < B * nc; u += NT) {
+      const int b = u / nc, c0 = (u - b * nc) * 32;
+      const int kb = s_sp[b];
+      const int c1 = min(B, c0 + 32);
+      int r = 0;
+      for (int c = c0; c < c1; ++c) {
+        const int kc = s_sp[c];
+        r += (kc > kb || (kc == kb && c < b)) ? 1 : 0;
+      }
+      if (r) atomicAdd(s_order + b, r);
+    }
+    block_sync();
+    int rk[(kMaxSortSeq + NT - 1) / NT];
+#pragma unroll
+    for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
+      const int b = tid + k * NT;
+      rk[k] = b < B ? s_order[b] : 0;
+    }
+    block_sync();
+#pragma unroll
+    for (int k = 0; k < (kMaxSortSeq + NT - 1) / NT; ++k) {
+      const int b = tid + k * NT;
+      if (b < B) s_order[rk[k]] = b;
+    }
+  } else {
+    for (int b = tid; b < B; b += NT) s_order[b] = b;
+  }
+  block_sync();
+  for (int k = tid; k < B; k += NT) s_sp[k] = s_nat[s_order[k]];  // items, queue order
+  // both exclusive prefixes in one pass: each thread scans a contiguous run
+  {
+    const int per = (B + NT - 1) / NT;
+    const int i0 = tid * per;
+    block_sync();
+    int l1 = 0, l2 = 0;
+    for (int i = i0; i < i0 + per && i < B; ++i) {
+      l1 += s_nat[i];
+      l2 += s_sp[i];
+    }
+    int c1 = l1, c2 = l2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v1 = __shfl_up_sync(0xffffffffu, c1, o);
+      const int v2 = __shfl_up_sync(0xffffffffu, c2, o);
+      if (lane >= o) {
+        c1 += v1;
+        c2 += v2;
+      }
+    }
+    if (lane == 31) {
+      scan_tmp[warp] = c1;
+      s_misc[4 + warp] = c2;
+    }
+    block_sync();
+    int r1 = c1 - l1, r2 = c2 - l2;
+    for (int w = 0; w < warp; ++w) {
+      r1 += scan_tmp[w];
+      r2 += s_misc[4 + w];
+    }
+    for (int i = i0; i < i0 + per && i < B; ++i) {
+      const int v1 = s_nat[i], v2 = s_sp[i];
+      s_nat[i] = r1;
+      s_sp[i] = r2;
+      r1 += v1;
+      r2 += v2;
+    }
+    if (tid == NT - 1) {
+      s_nat[B] = r1;
+      s_sp[B] = r2;
+    }
+    block_sync();
+  }
+  pdl_launch_dependents();
+  const int T = s_nat[B];  // work items in the batch
+
+  if (warp == NW) {
+    // ============================ producer warp ============================
+    // Items come from the queue one at a time; the next item's query rows
+    // and first 32 page ids are loaded into registers before the current
+    // item is streamed, so no global-memory latency sits between items.
+    constexpr int QV = D / 32;  // query vectors per lane for a group of <= 8 heads
+    bool dead = false;
+    const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
+    struct Item {
+      bool more;
+      int b, g, L, lo, first_tile, n, nch, slot0, chunk, pfx;
+    };
+    auto grab = [&]() -> int {
+      int i = 0;
+      if (lane == 0) i = atomicAdd(a.queue, 1);
+      return __shfl_sync(0xffffffffu, i, 0);
+    };
+    // queue index -> item (sorted sequences; heads; chunks)
+    auto item_at = [&](int i) -> Item {
+      Item it;
+      it.more = i < T;
+      it.b = it.g = it.L = it.lo = it.first_tile = it.nch = it.slot0 = it.chunk = it.pfx = 0;
+      it.n = -1;
+      if (!it.more) return it;
+      int lo = 0, hi = B;  // s_sp[lo] <= i < s_sp[lo+1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_sp[mid] <= i) lo = mid; else hi = mid;
+      }
+      const int b = s_order[lo];
+      const int j = i - s_sp[lo];
+      int L, klo, t_lo, t_hi, pfx;
+      seq_extent(a, b, L, klo, t_lo, t_hi, false, &pfx);
+      const int t = t_hi - t_lo;
+      const int nch = nch_of(t);
+      const int csz = (t + nch - 1) / nch;
+      const int g = j / nch, chunk = j - (j / nch) * nch;
+      it.b = b;
+      it.g = g;
+      it.L = L;
+      it.lo = klo;
+      it.first_tile = t_lo + chunk * csz;
+      it.n = min(csz, t - chunk * csz);
+      it.nch = nch;
+      it.slot0 = s_nat[b] + g * nch;
+      it.chunk = chunk;
+      it.pfx = pfx;
+      return it;
+    };
+    auto prefetch = [&](const Item& p, uint4 (&qr)[QV], int& pages) {
+      pages = -1;
+      if (!p.more) return;
+      const uint4* qsrc =
+          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.b * a.H_q + p.g * G) * D);
+#pragma unroll
+      for (int i = 0; i < QV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < qvec) qr[i] = __ldg(qsrc + v);
+      }
+      if (lane < p.n)
+        pages = __ldg(a.block_table + (int64_t)p.b * a.max_blocks +
+                      ((p.first_tile + lane) * kTile) / a.P);
+    };
+
+    Item cur = item_at(__shfl_sync(0xffffffffu, first_grab, 0));
+    uint4 qcur[QV];
+    int pcur;
+    prefetch(cur, qcur, pcur);
+    int it = 0;  // CTA-wide tile counter
+    int k = 0;   // item counter
+    while (true) {
+      // ---- publish the item record and its query rows ----
+      const int slot = k % kNRec;
+      if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
+      if (cur.more) {
+        uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * plan.qslot);
+#pragma unroll
+        for (int i = 0; i < QV; ++i) {
+          const int v = lane + 32 * i;
+          if (v < qvec) {
+            if (QS) {  // padded rows: vector v of head v / (D/8)
+              const int h = v / (D / 8);
+              qdst[v + h] = qcur[i];
+            } else {
+              qdst[v] = qcur[i];
+            }
+          }
+        }
+      }
+      if (lane == 0) {
+        PieceRec& r = recs[slot];
+        r.b = cur.b;
+        r.g = cur.g;
+        r.first_tile = cur.first_tile;
+        r.n = cur.n;
+        r.L = cur.L;
+        r.lo = cur.lo;
+        r.nch = cur.nch;
+        r.slot0 = cur.slot0;
+        r.chunk = cur.chunk;
+        r.pfx = cur.pfx;
+      }
+      __syncwarp();
+      mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
+      ++k;
+      if (!cur.more) break;
+      // ---- stream the item's tiles ----
+      const int* bt = a.block_table + (int64_t)cur.b * a.max_blocks;
+      const int n = cur.n;
+      int page = pcur;
+      for (int k0 = 0; k0 < n; k0 += 32) {
+        int page_ahead = -1;  // page ids of the following 32 tiles
+        if (k0 + 32 + lane < n)
+          page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
+        const int cnt = min(32, n - k0);
+        // NL lanes issue NL tiles at once, each into its own stage: one warp
+        // instruction launches NL TMA copies instead of one
+        for (int j0 = 0; j0 < cnt; j0 += kIssueLanes) {
+          const int j = j0 + lane;
+          const int pg = __shfl_sync(0xffffffffu, page, j & 31);
+          if (lane < kIssueLanes && j < cnt) {
+            const int itj = it + j;
+            const int s = itj % NSTAGE;
+            const int r = itj / NSTAGE;
+            if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
+            const int key0 = (cur.first_tile + k0 + j) * kTile;
+            const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
+            stage_ok[s] = ok ? 1 : 0;
+            if (ok) {
+              uint8_t* st = smem + s * P_::kStageBytes;
+              mbar_arrive_expect_tx(full + s, P_::kStageBytes);
+              const int row = key0 % a.P;
+              const int z = pg * a.H_kv + cur.g;
+              if (ONEBOX) {
+                tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
+                tma_load_4d(st + P_::kTileBytes, &tmV, full + s, 0, 0, row, z);
+              } else {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                  tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
+                  tma_load_3d(st + P_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
+                              z);
+                }
+              }
+            } else {
+              raise_err(a.err, PKV_DEVERR_PAGE);
+              mbar_arrive(full + s);
+            }
+          }
+          __syncwarp();
+        }
+        it += cnt;
+        page = page_ahead;
+      }
+      // ---- next item: grabbed only once this one is issued, so no CTA holds
+      //      work in reserve at the end; the stage ring covers the latency ----
+      cur = item_at(grab());
+      prefetch(cur, qcur, pcur);
+    }
+    // queue exhausted for this CTA: the last CTA to get here resets it
+    if (lane == 0) {
+      __threadfence();
+      const int done = atomicAdd(a.queue + 1, 1);
+      if (done == a.cta_count - 1) {
+        a.queue[0] = 0;
+        a.queue[1] = 0;
+      }
+    }
+    // drain: every issued load must land before the CTA may exit
+    if (lane == 0) {
+      const int first = it > NSTAGE ? it - NSTAGE : 0;
+      for (int i = first; i < it; ++i)
+        mbar_wait(full + (i % NSTAGE), (i / NSTAGE) & 1, a.err, dead);
+    }
+  } else if (warp < NW) {
+    // ============================== consumer warps ==========================
+    const int quad = lane >> 2;  // 0..7: key row (QK) / head (Q frag)
+    const int qlan = lane & 3;   // 0..3: head pair (2*qlan, 2*qlan+1)
+    bool dead = false;
+    int it_base = 0;
+    for (int k = 0;; ++k) {
+      const int slot = k % kNRec;
+      if (!mbar_wait(rec_full + slot, (k / kNRec) & 1, a.err, dead)) break;
+      const PieceRec rec = recs[slot];
+      // Q^T fragments (B operand of S^T = K Q^T): head = quad, dims by qlan.
+      // Registers (head dims up to 256), or per tile from shared memory.
+      uint32_t qb[QS ? 1 : KS][2];
+      if (!QS) {
+        const bool hv = rec.n >= 0 && quad < G;
+        const uint8_t* qrow = qbuf + slot * plan.qslot + (hv ? quad : 0) * D * 2;
+#pragma unroll
+        for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
+          qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * qlan) * 2)
+                         : 0u;
+          qb[ks][1] =
+              hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 8 + 2 * qlan) * 2) : 0u;
+        }
+        mbar_arrive(rec_empty + slot);  // record and query rows copied to registers
+      }
+      // ldmatrix row address of this lane in the smem query slot: row
+      // lane % 8 (a head), 8 dims at (lane / 8) * 8 of each 32-dim step
+      const uint32_t q_lane_addr = smem_u32(qbuf + slot * plan.qslot) +
+                                   (lane & 7) * Lay::kQRowBytes + (lane >> 3) * 16;
+      if (rec.n < 0) {
+        if (QS) mbar_arrive(rec_empty + slot);
+        break;
+      }
+
+      float o[KS][4];
+#pragma unroll
+      for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+      const int n = rec.n;
+      // this warp takes the item's tiles kk = r, r+NW, ...; r depends only on
+      // where the item starts in the stage ring, and the epilogue combines
+      // the warps in r order, so the result does not depend on the CTA.  The
+      // tiles go two at a time (kk and kk + NW): their QK chains run side by
+      // side, one max and one rescale serve both, and their PV products
+      // accumulate into the same O.
+      const int r0 = ((warp - it_base) % NW + NW) % NW;
+      for (int kk = r0; kk < n; kk += 2 * NW) {
+        const bool two = kk + NW < n;
+        const int it0 = it_base + kk, it1 = it0 + NW;
+        const int s0 = it0 % NSTAGE, s1 = it1 % NSTAGE;
+        const bool landed0 = mbar_wait(full + s0, (it0 / NSTAGE) & 1, a.err, dead);
+        const bool landed1 = two && mbar_wait(full + s1, (it1 / NSTAGE) & 1, a.err, dead);
+        const bool ok0 = landed0 && stage_ok[s0] != 0;
+        const bool ok1 = landed1 && stage_ok[s1] != 0;
+        const uint32_t stK0 = smem_u32(smem + s0 * P_::kStageBytes);
+        const uint32_t stK1 = smem_u32(smem + s1 * P_::kStageBytes);
+        const uint32_t stV0 = stK0 + P_::kTileBytes, stV1 = stK1 + P_::kTileBytes;
+        const int key00 = (rec.first_tile + kk) * kTile, key01 = key00 + NW * kTile;
+
+        // ---- S^T = K Q^T per tile: 16 keys x 8 heads, two chains each ----
+        float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sb0[4] = {0.f, 0.f, 0.f, 0.f};
+        float sa1[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+          if (QS) {
+            // two k-steps per ldmatrix of the query rows, shared by both tiles
+#pragma unroll
+            for (int ks = 0; ks < KS; ks += 2) {
+              uint32_t b00, b01, b10, b11;
+              ldsm_x4(q_lane_addr + ks * 32, b00, b01, b10, b11);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sa0, a0, a1, a2, a3, b00, b01);
+              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sb0, a0, a1, a2, a3, b10, b11);
+              if (two) {
+                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+                mma_bf16_16816(sa1, a0, a1, a2, a3, b00, b01);
+                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2,
+                        a3);
+                mma_bf16_16816(sb1, a0, a1, a2, a3, b10, b11);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+              if (ks & 1) mma_bf16_16816(sb0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              else mma_bf16_16816(sa0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              if (two) {
+                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+                if (ks & 1) mma_bf16_16816(sb1, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                else mma_bf16_16816(sa1, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              }
+            }
+          }
+        }
+        // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
+        auto masked = [&](bool ok, int key, float v) -> float {
+          return (ok && key >= rec.lo && key < rec.L) ? v * a.scale_log2 : -INFINITY;
+        };
+        const float x0A = masked(ok0, key00 + quad, sa0[0] + sb0[0]);
+        const float x0B = masked(ok0, key00 + quad, sa0[1] + sb0[1]);
+        const float x1A = masked(ok0, key00 + quad + 8, sa0[2] + sb0[2]);
+        const float x1B = masked(ok0, key00 + quad + 8, sa0[3] + sb0[3]);
+        const float y0A = masked(ok1, key01 + quad, sa1[0] + sb1[0]);
+        const float y0B = masked(ok1, key01 + quad, sa1[1] + sb1[1]);
+        const float y1A = masked(ok1, key01 + quad + 8, sa1[2] + sb1[2]);
+        const float y1B = masked(ok1, key01 + quad + 8, sa1[3] + sb1[3]);
+        float tA = fmaxf(fmaxf(x0A, x1A), fmaxf(y0A, y1A));
+        float tB = fmaxf(fmaxf(x0B, x1B), fmaxf(y0B, y1B));
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, off));
+          tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, off));
+        }
+        const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);
+        const float uA = nA == -INFINITY ? 0.f : nA;
+        const float uB = nB == -INFINITY ? 0.f : nB;
+        const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
+        const float p0A = exp2f(x0A - uA), p0B = exp2f(x0B - uB);
+        const float p1A = exp2f(x1A - uA), p1B = exp2f(x1B - uB);
+        const float q0A = exp2f(y0A - uA), q0B = exp2f(y0B - uB);
+        const float q1A = exp2f(y1A - uA), q1B = exp2f(y1B - uB);
+        lA = lA * alA + ((p0A + p1A) + (q0A + q1A));
+        lB = lB * alB + ((p0B + p1B) + (q0B + q1B));
+        mA = nA;
+        mB = nB;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          o[i][0] *= alA;
+          o[i][1] *= alB;
+          o[i][2] *= alA;
+          o[i][3] *= alB;
+        }
+        // P^T as the B operand: transpose the 8x8 (key x head) blocks in registers
+        const uint32_t pb0 = movmatrix_t(pack_bf16(p0A, p0B));
+        const uint32_t pb1 = movmatrix_t(pack_bf16(p1A, p1B));
+        const uint32_t pc0 = movmatrix_t(pack_bf16(q0A, q0B));
+        const uint32_t pc1 = movmatrix_t(pack_bf16(q1A, q1B));
+
+        // ---- O^T += V^T P^T for both tiles: D/16 m-tiles of 16 dims x 8 heads ----
+        {
+          const int j = lane >> 3;
+          const int key = (lane & 7) + (j >> 1) * 8;
+#pragma unroll
+          for (int md = 0; md < KS; ++md) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(tile_addr<D, ONEBOX>(stV0, key, 2 * md + (j & 1)), a0, a1, a2, a3);
+            mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
+            if (two) {
+              ldsm_x4_t(tile_addr<D, ONEBOX>(stV1, key, 2 * md + (j & 1)), a0, a1, a2, a3);
+              mma_bf16_16816(o[md], a0, a1, a2, a3, pc0, pc1);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(empty + s0);
+          if (two) mbar_arrive(empty + s1);
+        }
+      }
+      it_base += n;
+      if (QS) mbar_arrive(rec_empty + slot);  // done reading the query rows
+
+      // ---- hand (m, l, O) of this warp to the epilogue warp ----
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        lA += __shfl_xor_sync(0xffffffffu, lA, off);
+        lB += __shfl_xor_sync(0xffffffffu, lB, off);
+      }
+      const int cb = k % NCB;
+      if (k >= NCB) mbar_wait(comb_empty + cb, ((k / NCB) - 1) & 1, a.err, dead);
+      float* co = comb_o + ((cb * NW + r0) * G) * CS;
+      float* cml = comb_ml + ((cb * NW + r0) * G) * 2;
+      const int hA = 2 * qlan, hB = hA + 1;
+#pragma unroll
+      for (int md = 0; md < KS; ++md) {
+        const int d = md * 16 + quad;
+        if (hA < G) {
+          co[hA * CS + d] = o[md][0];
+          co[hA * CS + d + 8] = o[md][2];
+        }
+        if (hB < G) {
+          co[hB * CS + d] = o[md][1];
+          co[hB * CS + d + 8] = o[md][3];
+        }
+      }
+      if (quad == 0) {
+        if (hA < G) {
+          cml[hA * 2] = mA;
+          cml[hA * 2 + 1] = lA;
+        }
+        if (hB < G) {
+          cml[hB * 2] = mB;
+          cml[hB * 2 + 1] = lB;
+        }
+      }
+      mbar_arrive(comb_full + cb);  // every lane releases its own writes
+    }
+  } else {
+    // =============================== epilogue warp ==========================
+    bool dead = false;
+    for (int k = 0;; ++k) {
+      const int slot = k % kNRec;
+      if (!mbar_wait(rec_full + slot, (k / kNRec) & 1, a.err, dead)) break;
+      const PieceRec rec = recs[slot];
+      mbar_arrive(rec_empty + slot);
+      if (rec.n < 0) break;
+      const int cb = k % NCB;
+      mbar_wait(comb_full + cb, (k / NCB) & 1, a.err, dead);
+      const int b = rec.b, g = rec.g;
+      // a segment in one piece is written here; so is one with a prefix
+      // partial (cascade) whose suffix is one piece: the two are joined
+      // inline, with the prefix partial's weight from its log-sum-exp
+      const bool join_pfx = rec.nch == 1 && rec.pfx == 1;
+      const bool whole = rec.nch == 1;
+      const int64_t pre_row0 = (int64_t)b * a.H_q + g * G;
+      float* w_item = merge_lse + NW * kGP;  // [kGP] weights of the joined outputs
+      float* w_pfx = w_item + kGP;           // [kGP]
+      const float* co = comb_o + (cb * NW * G) * CS;
+      const float* cml = comb_ml + (cb * NW * G) * 2;
+      const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
+      // per head: weight of each consumer warp's state, 1/l, log2-sum-exp
+      float* wsc = merge_lse;  // [NW][G] scratch (the merge below reloads it)
+      if (lane < G) {
+        const int h = lane;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, cml[(w * G + h) * 2]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float sc = M == -INFINITY ? 0.f : exp2f(cml[(w * G + h) * 2] - M);
+          wsc[w * G + h] = sc;
+          lsum += sc * cml[(w * G + h) * 2 + 1];
+        }
+        merge_m[h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+        merge_inv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
+        if (join_pfx) {
+          const float li = merge_m[h];
+          const float lp = __ldcg(a.pre_lse + pre_row0 + h);
+          const float m2 = fmaxf(li, lp);
+          const float wi = li == -INFINITY ? 0.f : exp2f(li - m2);
+          const float wp = lp == -INFINITY ? 0.f : exp2f(lp - m2);
+          const float den = wi + wp;
+          w_item[h] = den > 0.f ? wi / den : 0.f;
+          w_pfx[h] = den > 0.f ? wp / den : 0.f;
+        }
+      }
+      __syncwarp();
+      // 4 slices per lane per pass; the prefix partial's loads (cascade)
+      // are issued before any is used
+      for (int j0 = lane; j0 < G * (D / 4); j0 += 128) {
+        float4 pv[4];
+        if (join_pfx) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + 32 * u < G * (D / 4) ? j0 + 32 * u : 0;
+            const int h = j / (D / 4), d4 = j - h * (D / 4);
+            pv[u] = __ldcg(reinterpret_cast<const float4*>(a.pre_o + (pre_row0 + h) * D) + d4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + 32 * u;
+          if (j >= G * (D / 4)) break;
+          const int h = j / (D / 4), d4 = j - h * (D / 4);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float sc = wsc[w * G + h];
+            const float4 v = *reinterpret_cast<const float4*>(co + (w * G + h) * CS + d4 * 4);
+            acc.x += sc * v.x;
+            acc.y += sc * v.y;
+            acc.z += sc * v.z;
+            acc.w += sc * v.w;
+          }
+          const float inv = merge_inv[h];
+          acc.x *= inv;
+          acc.y *= inv;
+          acc.z *= inv;
+          acc.w *= inv;
+          if (join_pfx) {
+            const float wi = w_item[h], wp = w_pfx[h];
+            acc.x = wi * acc.x + wp * pv[u].x;
+            acc.y = wi * acc.y + wp * pv[u].y;
+            acc.z = wi * acc.z + wp * pv[u].z;
+            acc.w = wi * acc.w + wp * pv[u].w;
+          }
+          if (whole) {
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
+                pk;
+          } else {
+            *reinterpret_cast<float4*>(a.part_o + (pslot * G + h) * D + d4 * 4) = acc;
+            if (d4 == 0) a.part_lse[pslot * G + h] = merge_m[h];
+          }
+        }
+      }
+      __syncwarp();
+      mbar_arrive(comb_empty + cb);  // the consumers may refill this buffer
+      if (!whole) {
+        // arrival counter: the last CTA to deliver a chunk of this segment
+        // merges all of them (nobody waits; the counter is reset afterwards)
+        const int64_t seg = (int64_t)b * a.H_kv + g;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          const int old = atomicAdd(a.seg_count + seg, 1);
+          *merge_flag = (old == rec.nch - 1) ? 1 : 0;
+        }
+        __syncwarp();
+        if (*merge_flag) {
+          __threadfence();
+          // the segment's chunks, plus the prefix partial as chunk nch
+          const int np = rec.nch + rec.pfx;
+          const int64_t pre_row = (int64_t)b * a.H_q + g * G;
+          auto l_src = [&](int c, int h) -> const float* {
+            return c < rec.nch ? a.part_lse + ((int64_t)rec.slot0 + c) * G + h
+                               : a.pre_lse + pre_row + h;
+          };
+          auto o_src = [&](int c, int h) -> const float* {
+            return c < rec.nch ? a.part_o + (((int64_t)rec.slot0 + c) * G + h) * D
+                               : a.pre_o + (pre_row + h) * D;
+          };
+          // (1) the (chunk, head) log2-sum-exps, staged in shared memory in
+          //     one round of loads when they fit (a segment cut into more
+          //     than kMergeLse / G chunks reads them from L2 instead)
+          const int nl = np * G;
+          const bool staged = nl <= kMergeLse;
+          if (staged)
+            for (int i = lane; i < nl; i += 32) merge_lse[i] = __ldcg(l_src(i / G, i % G));
+          __syncwarp();
+          if (lane < G) {  // per head: max and 1 / sum of the weights
+            const int h = lane;
+            float M = -INFINITY, sum = 0.f;
+            if (staged) {
+              for (int c = 0; c < np; ++c) M = fmaxf(M, merge_lse[c * G + h]);
+              if (M != -INFINITY)
+                for (int c = 0; c < np; ++c) sum += exp2f(merge_lse[c * G + h] - M);
+            } else {
+              for (int c = 0; c < np; ++c) M = fmaxf(M, __ldcg(l_src(c, h)));
+              if (M != -INFINITY)
+                for (int c = 0; c < np; ++c) sum += exp2f(__ldcg(l_src(c, h)) - M);
+            }
+            merge_m[h] = M;
+            merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
+          }
+          __syncwarp();
+          // (2) staged: the normalised weight of every (chunk, head)
+          if (staged) {
+            for (int i = lane; i < nl; i += 32) {
+              const int h = i % G;
+              const float M = merge_m[h];
+              merge_lse[i] = M == -INFINITY ? 0.f : exp2f(merge_lse[i] - M) * merge_inv[h];
+            }
+          }
+          __syncwarp();
+          // (3) weighted sum of the chunks' outputs, 4 dims (a slice) per
+          //     lane and load.  Each lane keeps kMU slices x kMC chunks of
+          //     loads in flight; the weights come from shared memory (or,
+          //     unstaged, from loads issued in the same batch), so a merge
+          //     costs a few L2 round trips.  Every output sums its chunks in
+          //     chunk order.
+          constexpr int kMU = 4, kMC = 4;
+          const int nslice = G * (D / 4);
+          for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
+            float4 acc[kMU];
+            int hh[kMU], dd[kMU];
+#pragma unroll
+            for (int u = 0; u < kMU; ++u) {
+              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              const int j = j0 + 32 * u < nslice ? j0 + 32 * u : 0;
+              hh[u] = j / (D / 4);
+              dd[u] = j - hh[u] * (D / 4);
+            }
+            for (int c0 = 0; c0 < np; c0 += kMC) {
+              float4 v[kMU][kMC];
+              float w[kMU][kMC];
+#pragma unroll
+              for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                for (int cc = 0; cc < kMC; ++cc) {
+                  const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
+                  v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
+                }
+              if (staged) {
+#pragma unroll
+                for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc)
+                    w[u][cc] = c0 + cc < np ? merge_lse[(c0 + cc) * G + hh[u]] : 0.f;
+              } else {
+#pragma unroll
+                for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc) {
+                    const int c = c0 + cc < np ? c0 + cc : np - 1;
+                    w[u][cc] = __ldcg(l_src(c, hh[u]));
+                  }
+#pragma unroll
+                for (int u = 0; u < kMU; ++u) {
+                  const float M = merge_m[hh[u]];
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc)
+                    w[u][cc] = (c0 + cc < np && M != -INFINITY)
+                                   ? exp2f(w[u][cc] - M) * merge_inv[hh[u]]
+                                   : 0.f;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                for (int cc = 0; cc < kMC; ++cc) {
+                  acc[u].x += w[u][cc] * v[u][cc].x;
+                  acc[u].y += w[u][cc] * v[u][cc].y;
+                  acc[u].z += w[u][cc] * v[u][cc].z;
+                  acc[u].w += w[u][cc] * v[u][cc].w;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kMU; ++u) {
+              if (j0 + 32 * u >= nslice) continue;
+              __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+              __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+              pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+              *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + hh[u]) * D +
+                                        dd[u] * 4) = pk;
+            }
+          }
+          if (lane == 0) a.seg_count[seg] = 0;
+          __syncwarp();
+        }
+      }
+    }
+  }
+}
+
+// Places the arrival counters, the queue and the partial results of a
+// decode call in its workspace (decode.cu).
+void decode_workspace_split(DecodeArgs& a, void* workspace, size_t workspace_bytes,
+                            int32_t batch, int32_t H_kv, int32_t D, int num_sms);
+
+}  // namespace pkv

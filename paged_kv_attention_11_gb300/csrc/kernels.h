@@ -93,9 +93,38 @@ struct VarlenMaps {
   CUtensorMap v;  // same for V
 };
 
+// Arguments of the single-launch mixed step (mixed.cu): decode rows and
+// causal prefill chunks over one pool.
+struct MixedLaunch {
+  void* dec_out;
+  const void* dec_q;
+  const int32_t* dec_block_table;
+  const int32_t* dec_seq_lens;
+  int32_t dec_max_blocks, dec_batch, dec_max_seq_len;
+  void* pre_out;
+  const void* pre_q;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* pre_block_table;
+  int32_t pre_max_blocks, pre_batch, max_seqlen_q, max_seqlen_k, total_q;
+  const void* k_cache;
+  const void* v_cache;
+  int32_t H_q, H_kv, D, P;
+  int64_t num_pages;
+  float scale;
+  int32_t window;
+  int32_t decode_ctas;  // CTAs that start with decode; <= 0: chosen here
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* err;
+};
+
 // keys per KV tile of the varlen kernel for a head_dim (page_size must
 // divide it or be a multiple of it)
 int varlen_kv_tile(int head_dim);
+
+cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStream_t stream,
+                         int num_sms);
 
 cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,
                           const int32_t* cu_k, const int32_t* block_table, int32_t max_blocks,

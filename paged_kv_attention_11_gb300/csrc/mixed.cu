@@ -1,0 +1,204 @@
+// paged_attn_mixed: the attention of one continuous-batching step -- decode
+// rows and prefill chunks -- in a single persistent launch.
+//
+// Source: scripts/benchmarks commit log, batch-sweep commit (vLLM runs
+// chunked prefill and decode of one step packed into the same kernels) and
+// README "Why continuous batching is still slower than vLLM on this
+// workload" (separate prefill and decode passes per step).
+//
+// Decode is bound by HBM bandwidth, prefill by the tensor cores and its own
+// latency chain; run back to back, each leaves the other's resource idle.
+// Here one grid of one CTA per SM splits the step:
+//   * CTAs [0, nd) start with decode (the split-KV body, decode_cta, on
+//     warps 0-5; the dynamic longest-first queue in the workspace);
+//   * CTAs [nd, N) run the prefill chunks (the tcgen05 body, varlen_cta,
+//     with the static snake schedule over those N - nd CTAs), then join the
+//     decode queue and take whatever work is left in it.
+// Every CTA ends in the decode body, so the decode queue's last-CTA reset
+// and the zero rows of empty sequences work as in paged_attn_decode.  The
+// decode body gets more registers than the launch's 168 per thread through
+// setmaxnreg: warpgroups 0-1 (warps 0-7) go to 232, warpgroup 2 to 40.
+#include "decode_body.cuh"
+#include "tmap.h"
+#include "varlen_body.cuh"
+
+namespace pkv {
+
+struct MixedArgs {
+  DecodeArgs dec;
+  VarlenArgs var;
+  int32_t has_dec, has_var;
+};
+
+// the prefill shape of the mixed step (head_dim 128): two Q tiles per item,
+// 128-key tiles, K ring 3, V ring 2
+constexpr int kMixD = 128, kMixNQ = 2, kMixBN = 128, kMixNS = 1, kMixNKS = 3, kMixNVS = 2;
+constexpr int kMixThreads = varlen_threads<kMixNQ>();  // 384
+static_assert(kMixThreads == 384, "three warpgroups");
+
+template <int NSTAGE_DEC>
+__global__ void __launch_bounds__(kMixThreads, 1)
+    mixed_step_kernel(const MixedArgs m, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmKv,
+                      const __grid_constant__ CUtensorMap tmVv,
+                      const __grid_constant__ CUtensorMap tmKd,
+                      const __grid_constant__ CUtensorMap tmVd) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int nd = m.dec.share_ctas;
+  if (m.has_var && (int)blockIdx.x >= nd)
+    varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
+        m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
+  if (m.has_dec) {
+    if (warp >= 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
+      if (warp < 6)
+        decode_cta<kMixD, 4, NSTAGE_DEC, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
+    }
+  }
+}
+
+// CTAs that start with decode when the caller leaves the split open: the
+// smallest count whose decode time (HBM bound, or the per-SM rate below
+// that) does not exceed the prefill time of the remaining CTAs, from the
+// host's estimates of the work (half of the longest decode context per row,
+// prefill pairs from the packed lengths).  Prefill CTAs join the decode
+// queue when they are done, so the estimate may err towards fewer.
+static int mixed_decode_ctas(int num_sms, int64_t dec_batch, int64_t dec_max_seq_len,
+                             int64_t total_q, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                             int H_q, int H_kv, int D) {
+  const double dec_bytes = (double)dec_batch * (double)(dec_max_seq_len / 2 + 1) * H_kv * D * 4.0;
+  double pairs_per_q = (double)max_seqlen_k - 0.5 * (double)max_seqlen_q;
+  if (pairs_per_q < 1.0) pairs_per_q = 1.0;
+  const double var_flops = (double)total_q * pairs_per_q * 4.0 * D * H_q;
+  const double hbm = 6.5e12, per_sm_bw = 55e9, per_sm_flops = 4.4e12;
+  for (int nd = 1; nd < num_sms; ++nd) {
+    double bw = nd * per_sm_bw;
+    if (bw > hbm) bw = hbm;
+    const double t_dec = dec_bytes / bw;
+    const double t_var = var_flops / ((num_sms - nd) * per_sm_flops);
+    if (t_dec <= t_var) return nd;
+  }
+  return num_sms - 1;
+}
+
+template <int NSTAGE_DEC>
+static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const void* k_cache,
+                                  const void* v_cache, size_t smem, cudaStream_t stream,
+                                  int num_sms) {
+  auto kern = mixed_step_kernel<NSTAGE_DEC>;
+  CUtensorMap tmKd, tmVd;
+  if (!encode_pool_map_halves(&tmKd, k_cache, m.dec.P, m.dec.num_pages, m.dec.H_kv) ||
+      !encode_pool_map_halves(&tmVd, v_cache, m.dec.P, m.dec.num_pages, m.dec.H_kv))
+    return cudaErrorInvalidValue;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < (int)smem) {
+    // the prefill body moves registers to its softmax with setmaxnreg: the
+    // launch must hold 168 per thread
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kMixThreads < 8 * 32 * 232 + 4 * 32 * 40) return cudaErrorNotSupported;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = (int)smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_sms);
+  cfg.blockDim = dim3(kMixThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m, vmaps.q, vmaps.k, vmaps.v, tmKd, tmVd);
+}
+
+cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStream_t stream,
+                         int num_sms) {
+  if (L.D != kMixD) return cudaErrorNotSupported;
+  MixedArgs m;
+  m.has_dec = L.dec_batch > 0;
+  m.has_var = L.pre_batch > 0 && L.total_q > 0 && L.max_seqlen_q > 0;
+  // ---- decode arguments (as launch_decode)
+  DecodeArgs& a = m.dec;
+  a.q = static_cast<const __nv_bfloat16*>(L.dec_q);
+  a.out = static_cast<__nv_bfloat16*>(L.dec_out);
+  a.block_table = L.dec_block_table;
+  a.seq_lens = L.dec_seq_lens;
+  a.max_blocks = L.dec_max_blocks;
+  a.batch = L.dec_batch;
+  a.H_q = L.H_q;
+  a.H_kv = L.H_kv;
+  a.G = L.H_q / L.H_kv;
+  a.P = L.P;
+  a.num_pages = L.num_pages;
+  a.window = L.window;
+  a.scale_log2 = L.scale * 1.4426950408889634f;
+  a.prefix_lens = nullptr;
+  a.group_size = 1;
+  a.pre_o = nullptr;
+  a.pre_lse = nullptr;
+  a.err = L.err;
+  decode_workspace_split(a, L.workspace, L.workspace_bytes, L.dec_batch, L.H_kv, L.D, num_sms);
+  // ---- prefill arguments (as launch_varlen)
+  VarlenArgs& v = m.var;
+  const int QP = 128 / a.G;
+  v.out = static_cast<__nv_bfloat16*>(L.pre_out);
+  v.cu_q = L.cu_q;
+  v.cu_k = L.cu_k;
+  v.block_table = L.pre_block_table;
+  v.batch = L.pre_batch;
+  v.max_blocks = L.pre_max_blocks;
+  v.max_q = L.max_seqlen_q;
+  v.R = (L.max_seqlen_q + 2 * QP - 1) / (2 * QP);
+  v.pairs_max = L.pre_batch * v.R;
+  v.H_q = L.H_q;
+  v.H_kv = L.H_kv;
+  v.G = a.G;
+  v.log2G = 0;
+  while ((1 << v.log2G) < v.G) ++v.log2G;
+  v.P = L.P;
+  v.box_rows = L.P < kMixBN ? L.P : kMixBN;
+  v.num_pages = L.num_pages;
+  v.scale_log2 = a.scale_log2;
+  v.causal = 1;
+  v.window = L.window;
+  v.err = L.err;
+  // ---- the split
+  int nd = L.decode_ctas;
+  if (nd <= 0)
+    nd = mixed_decode_ctas(num_sms, L.dec_batch, L.dec_max_seq_len, L.total_q, L.max_seqlen_q,
+                           L.max_seqlen_k, L.H_q, L.H_kv, L.D);
+  if (!m.has_var) nd = num_sms;
+  if (!m.has_dec) nd = 0;
+  if (m.has_var && m.has_dec) nd = nd < 1 ? 1 : (nd > num_sms - 1 ? num_sms - 1 : nd);
+  a.cta_count = num_sms;
+  a.share_ctas = nd > 0 ? nd : num_sms;
+  // ---- shared memory: the larger of the two plans
+  using VS = VarlenSmem<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS>;
+  const size_t var_smem = m.has_var ? VS::bytes(v.batch, v.pairs_max) : 0;
+  const size_t dec24 = DecodePlan<kMixD, 4, 24>(a.G, a.batch).total;
+  const size_t dec16 = DecodePlan<kMixD, 4, 16>(a.G, a.batch).total;
+  constexpr size_t kMax = 227 * 1024;
+  if (var_smem > kMax) return cudaErrorNotSupported;
+  if (!m.has_dec || dec24 <= kMax) {
+    const size_t smem = var_smem > dec24 ? var_smem : dec24;
+    return launch_mixed_t<24>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+  }
+  if (dec16 > kMax) return cudaErrorNotSupported;
+  const size_t smem = var_smem > dec16 ? var_smem : dec16;
+  return launch_mixed_t<16>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+}
+
+}  // namespace pkv

@@ -1,0 +1,117 @@
+"""GPU parity of paged_attn_mixed (one persistent launch for a step's decode
+rows and causal prefill chunks) against the fp64 oracle: the full mixed
+continuous-batching workload (8 prefill chunks on cached prefixes + 120
+decode rows, H 32/8/128, page 16) after this step's append, with the split
+between decode-first and prefill-first CTAs chosen by the library and set
+explicitly at both extremes; a sliding window; steps with only one half;
+and two calls in a row on one workspace (the queue and counters reset)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from _util import assert_close_attn, bf16_dev_to_bits, bf16_dev_to_f64, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import torch  # noqa: F401
+    from paged_kv_attention_11_gb300 import build
+    build.build()
+    import paged_kv_attention_11_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def mixed_case(pkv):
+    """The mixed workload after its append: device pools, inputs, oracle outputs."""
+    import torch
+    step = wl.mixed_step()
+    vals = wl.fill_values(step, 2024)
+    kc, vc = to_dev_bf16(vals.k_cache), to_dev_bf16(vals.v_cache)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(to_dev_bf16(vals.k_new), to_dev_bf16(vals.v_new), kc, vc,
+                        to_dev(step.all_slots), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    hk, hv = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, step.all_slots)
+    return step, vals, kc, vc, hk, hv
+
+
+def _run(pkv, step, vals, kc, vc, window=0, decode_ctas=0, dec=True, pre=True, ws=None):
+    import torch
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qd = to_dev_bf16(vals.q_dec[0]) if dec else torch.empty((0, step.H_q, step.D),
+                                                            dtype=torch.bfloat16, device="cuda")
+    qp = to_dev_bf16(vals.q_pre[0]) if pre else torch.empty((0, step.H_q, step.D),
+                                                            dtype=torch.bfloat16, device="cuda")
+    od = torch.full_like(qd, float("nan"))
+    op = torch.full_like(qp, float("nan"))
+    cu_q = step.cu_seq_lens_q if pre else np.zeros(1, np.int32)
+    cu_k = step.cu_seq_lens_k if pre else np.zeros(1, np.int32)
+    pbt = step.pre_block_table if pre else np.zeros((0, 1), np.int32)
+    dbt = step.dec_block_table if dec else np.zeros((0, 1), np.int32)
+    dl = step.dec_seq_lens if dec else np.zeros(0, np.int32)
+    pkv.paged_attn_mixed(od, qd, to_dev(dbt), to_dev(dl), step.max_seq_len_dec() if dec else 0,
+                         op, qp, to_dev(cu_q), to_dev(cu_k), to_dev(pbt),
+                         step.max_seqlen_q() if pre else 0, step.max_seqlen_k() if pre else 0,
+                         kc, vc, step.scale, window, decode_ctas, workspace=ws, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return od, op
+
+
+def _want(step, vals, hk, hv, window=0):
+    wd = oracle.paged_decode(vals.q_dec[0], hk, hv, step.dec_block_table, step.dec_seq_lens,
+                             step.scale, window)
+    wp = oracle.paged_varlen(vals.q_pre[0], hk, hv, step.cu_seq_lens_q, step.cu_seq_lens_k,
+                             step.pre_block_table, step.scale, True, window)
+    return wd, wp
+
+
+@pytest.fixture(scope="module")
+def want_full(mixed_case):
+    step, vals, _, _, hk, hv = mixed_case
+    return _want(step, vals, hk, hv)
+
+
+@pytest.mark.parametrize("decode_ctas", [0, 1, 40, 100, 151])
+def test_mixed_step_full_workload(pkv, mixed_case, want_full, decode_ctas):
+    step, vals, kc, vc, _, _ = mixed_case
+    od, op = _run(pkv, step, vals, kc, vc, decode_ctas=decode_ctas)
+    wd, wp = want_full
+    assert_close_attn(bf16_dev_to_f64(od), wd, f"mixed decode (split {decode_ctas})")
+    assert_close_attn(bf16_dev_to_f64(op), wp, f"mixed prefill (split {decode_ctas})")
+
+
+def test_mixed_step_sliding_window(pkv, mixed_case):
+    step, vals, kc, vc, hk, hv = mixed_case
+    od, op = _run(pkv, step, vals, kc, vc, window=300)
+    wd, wp = _want(step, vals, hk, hv, window=300)
+    assert_close_attn(bf16_dev_to_f64(od), wd, "mixed decode, window 300")
+    assert_close_attn(bf16_dev_to_f64(op), wp, "mixed prefill, window 300")
+
+
+def test_mixed_step_one_half_only(pkv, mixed_case, want_full):
+    step, vals, kc, vc, _, _ = mixed_case
+    wd, wp = want_full
+    od, _ = _run(pkv, step, vals, kc, vc, pre=False)
+    assert_close_attn(bf16_dev_to_f64(od), wd, "mixed, decode only")
+    _, op = _run(pkv, step, vals, kc, vc, dec=False)
+    assert_close_attn(bf16_dev_to_f64(op), wp, "mixed, prefill only")
+
+
+def test_mixed_step_twice_on_one_workspace(pkv, mixed_case):
+    """The workspace is left ready for the next call: a second call gives
+    the same bits."""
+    import torch
+    step, vals, kc, vc, _, _ = mixed_case
+    need = pkv.decode_workspace_size(step.Bd, step.H_q, step.H_kv, step.D)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    od1, op1 = _run(pkv, step, vals, kc, vc, ws=ws)
+    od2, op2 = _run(pkv, step, vals, kc, vc, ws=ws)
+    assert np.array_equal(bf16_dev_to_bits(od1), bf16_dev_to_bits(od2))
+    assert np.array_equal(bf16_dev_to_bits(op1), bf16_dev_to_bits(op2))
