@@ -165,10 +165,6 @@ template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
-  // a consumer holds two stages (its tiles t and t + NW) at once; the stage
-  // of tile t + NW is refilled after tile t + NW - NSTAGE <= t - NW, which
-  // the same warp released in an earlier step
-  static_assert(NSTAGE >= 2 * NW, "tile pairs");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
   using P_ = DecodePlan<D, NW, NSTAGE>;
   using Lay = DecodeLayout<D>;
@@ -604,77 +600,53 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       const int n = rec.n;
       // this warp takes the item's tiles kk = r, r+NW, ...; r depends only on
       // where the item starts in the stage ring, and the epilogue combines
-      // the warps in r order, so the result does not depend on the CTA.  The
-      // tiles go two at a time (kk and kk + NW): their QK chains run side by
-      // side, one max and one rescale serve both, and their PV products
-      // accumulate into the same O.
+      // the warps in r order, so the result does not depend on the CTA
       const int r0 = ((warp - it_base) % NW + NW) % NW;
-      for (int kk = r0; kk < n; kk += 2 * NW) {
-        const bool two = kk + NW < n;
-        const int it0 = it_base + kk, it1 = it0 + NW;
-        const int s0 = it0 % NSTAGE, s1 = it1 % NSTAGE;
-        const bool landed0 = mbar_wait(full + s0, (it0 / NSTAGE) & 1, a.err, dead);
-        const bool landed1 = two && mbar_wait(full + s1, (it1 / NSTAGE) & 1, a.err, dead);
-        const bool ok0 = landed0 && stage_ok[s0] != 0;
-        const bool ok1 = landed1 && stage_ok[s1] != 0;
-        const uint32_t stK0 = smem_u32(smem + s0 * P_::kStageBytes);
-        const uint32_t stK1 = smem_u32(smem + s1 * P_::kStageBytes);
-        const uint32_t stV0 = stK0 + P_::kTileBytes, stV1 = stK1 + P_::kTileBytes;
-        const int key00 = (rec.first_tile + kk) * kTile, key01 = key00 + NW * kTile;
+      for (int kk = r0; kk < n; kk += NW) {
+        const int it = it_base + kk;
+        const int s = it % NSTAGE;
+        const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
+        const bool ok = landed && stage_ok[s] != 0;
+        const uint32_t stK = smem_u32(smem + s * P_::kStageBytes);
+        const uint32_t stV = stK + P_::kTileBytes;
+        const int key0 = (rec.first_tile + kk) * kTile;
 
-        // ---- S^T = K Q^T per tile: 16 keys x 8 heads, two chains each ----
-        float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sb0[4] = {0.f, 0.f, 0.f, 0.f};
-        float sa1[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S^T = K Q^T: 16 keys x 8 heads, two accumulation chains ----
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
           if (QS) {
-            // two k-steps per ldmatrix of the query rows, shared by both tiles
+            // two k-steps per ldmatrix of the query rows
 #pragma unroll
             for (int ks = 0; ks < KS; ks += 2) {
               uint32_t b00, b01, b10, b11;
               ldsm_x4(q_lane_addr + ks * 32, b00, b01, b10, b11);
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-              mma_bf16_16816(sa0, a0, a1, a2, a3, b00, b01);
-              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
-              mma_bf16_16816(sb0, a0, a1, a2, a3, b10, b11);
-              if (two) {
-                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-                mma_bf16_16816(sa1, a0, a1, a2, a3, b00, b01);
-                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2,
-                        a3);
-                mma_bf16_16816(sb1, a0, a1, a2, a3, b10, b11);
-              }
+              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sa, a0, a1, a2, a3, b00, b01);
+              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
+              mma_bf16_16816(sb, a0, a1, a2, a3, b10, b11);
             }
           } else {
 #pragma unroll
             for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
+              const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(tile_addr<D, ONEBOX>(stK0, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-              if (ks & 1) mma_bf16_16816(sb0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-              else mma_bf16_16816(sa0, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-              if (two) {
-                ldsm_x4(tile_addr<D, ONEBOX>(stK1, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-                if (ks & 1) mma_bf16_16816(sb1, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-                else mma_bf16_16816(sa1, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-              }
+              ldsm_x4(addr, a0, a1, a2, a3);
+              if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              else mma_bf16_16816(sa, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
           }
         }
         // rows: key0+quad (regs 0,1) and key0+quad+8 (regs 2,3); cols: heads 2*qlan, +1
-        auto masked = [&](bool ok, int key, float v) -> float {
-          return (ok && key >= rec.lo && key < rec.L) ? v * a.scale_log2 : -INFINITY;
-        };
-        const float x0A = masked(ok0, key00 + quad, sa0[0] + sb0[0]);
-        const float x0B = masked(ok0, key00 + quad, sa0[1] + sb0[1]);
-        const float x1A = masked(ok0, key00 + quad + 8, sa0[2] + sb0[2]);
-        const float x1B = masked(ok0, key00 + quad + 8, sa0[3] + sb0[3]);
-        const float y0A = masked(ok1, key01 + quad, sa1[0] + sb1[0]);
-        const float y0B = masked(ok1, key01 + quad, sa1[1] + sb1[1]);
-        const float y1A = masked(ok1, key01 + quad + 8, sa1[2] + sb1[2]);
-        const float y1B = masked(ok1, key01 + quad + 8, sa1[3] + sb1[3]);
-        float tA = fmaxf(fmaxf(x0A, x1A), fmaxf(y0A, y1A));
-        float tB = fmaxf(fmaxf(x0B, x1B), fmaxf(y0B, y1B));
+        const int kA = key0 + quad, kB = kA + 8;
+        const bool vA = ok && kA >= rec.lo && kA < rec.L;
+        const bool vB = ok && kB >= rec.lo && kB < rec.L;
+        const float x0A = vA ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
+        const float x0B = vA ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
+        const float x1A = vB ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
+        const float x1B = vB ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
+        float tA = fmaxf(x0A, x1A), tB = fmaxf(x0B, x1B);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, off));
@@ -686,10 +658,8 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         const float alA = exp2f(mA - uA), alB = exp2f(mB - uB);
         const float p0A = exp2f(x0A - uA), p0B = exp2f(x0B - uB);
         const float p1A = exp2f(x1A - uA), p1B = exp2f(x1B - uB);
-        const float q0A = exp2f(y0A - uA), q0B = exp2f(y0B - uB);
-        const float q1A = exp2f(y1A - uA), q1B = exp2f(y1B - uB);
-        lA = lA * alA + ((p0A + p1A) + (q0A + q1A));
-        lB = lB * alB + ((p0B + p1B) + (q0B + q1B));
+        lA = lA * alA + p0A + p1A;
+        lB = lB * alB + p0B + p1B;
         mA = nA;
         mB = nB;
 #pragma unroll
@@ -702,29 +672,21 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         // P^T as the B operand: transpose the 8x8 (key x head) blocks in registers
         const uint32_t pb0 = movmatrix_t(pack_bf16(p0A, p0B));
         const uint32_t pb1 = movmatrix_t(pack_bf16(p1A, p1B));
-        const uint32_t pc0 = movmatrix_t(pack_bf16(q0A, q0B));
-        const uint32_t pc1 = movmatrix_t(pack_bf16(q1A, q1B));
 
-        // ---- O^T += V^T P^T for both tiles: D/16 m-tiles of 16 dims x 8 heads ----
+        // ---- O^T += V^T P^T: D/16 m-tiles of 16 dims x 8 heads ----
         {
           const int j = lane >> 3;
           const int key = (lane & 7) + (j >> 1) * 8;
 #pragma unroll
           for (int md = 0; md < KS; ++md) {
+            const uint32_t addr = tile_addr<D, ONEBOX>(stV, key, 2 * md + (j & 1));
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(tile_addr<D, ONEBOX>(stV0, key, 2 * md + (j & 1)), a0, a1, a2, a3);
+            ldsm_x4_t(addr, a0, a1, a2, a3);
             mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
-            if (two) {
-              ldsm_x4_t(tile_addr<D, ONEBOX>(stV1, key, 2 * md + (j & 1)), a0, a1, a2, a3);
-              mma_bf16_16816(o[md], a0, a1, a2, a3, pc0, pc1);
-            }
           }
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(empty + s0);
-          if (two) mbar_arrive(empty + s1);
-        }
+        if (lane == 0) mbar_arrive(empty + s);
       }
       it_base += n;
       if (QS) mbar_arrive(rec_empty + slot);  // done reading the query rows
