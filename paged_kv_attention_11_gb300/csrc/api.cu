@@ -218,7 +218,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   if (causal != 0 && causal != 1) return PKV_ERR_INVALID;
   if (!causal && window > 0) return PKV_ERR_INVALID;
   const int G = num_q_heads / num_kv_heads;
-  if (!supported_head_dim(head_dim) || page_size % 16 != 0 || (128 % G) != 0 ||
+  if (!decode_head_dim(head_dim) || page_size % 16 != 0 || (128 % G) != 0 ||
       num_pages * (int64_t)num_kv_heads > 0x7fffffffLL || batch > 1024)
     return PKV_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0) return PKV_OK;
@@ -238,7 +238,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
       !encode_pool_map_groups(&maps.k, k_cache, head_dim, page_size, num_pages, num_kv_heads,
                               box_rows) ||
       !encode_pool_map_groups(&maps.v, v_cache, head_dim, page_size, num_pages, num_kv_heads,
-                              box_rows))
+                              box_rows, pkv::varlen_v_cols(head_dim)))
     return cuda_fail(cudaErrorInvalidValue);
   cudaError_t e = pkv::launch_varlen(out, maps, cu_seq_lens_q, cu_seq_lens_k, block_table,
                                      max_blocks_per_seq, batch, max_seqlen_q, total_q,

@@ -122,6 +122,9 @@ struct MixedLaunch {
 // keys per KV tile of the varlen kernel for a head_dim (page_size must
 // divide it or be a multiple of it)
 int varlen_kv_tile(int head_dim);
+// columns of V (and of O) one varlen work item covers (head_dim, or half of
+// it at 512)
+int varlen_v_cols(int head_dim);
 
 cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStream_t stream,
                          int num_sms);

@@ -4,7 +4,7 @@
 
 namespace pkv {
 
-template <int D, int NQ, int BN, int NS, int NKS, int NVS>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS, int DV>
 __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
     varlen_fwd_kernel(const VarlenArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -12,24 +12,24 @@ __global__ void __launch_bounds__(varlen_threads<NQ>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  varlen_cta<D, NQ, BN, NS, NKS, NVS, false>(a, tmQ, tmK, tmV, smem, blockIdx.x, gridDim.x);
+  varlen_cta<D, NQ, BN, NS, NKS, NVS, false, DV>(a, tmQ, tmK, tmV, smem, blockIdx.x, gridDim.x);
 }
 
 // --------------------------------------------------------------- host side
-template <int D, int NQ, int BN, int NS, int NKS, int NVS>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS, int DV = D>
 static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
                                    cudaStream_t stream, int num_sms) {
-  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS>;
-  auto kern = varlen_fwd_kernel<D, NQ, BN, NS, NKS, NVS>;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS, DV>;
+  auto kern = varlen_fwd_kernel<D, NQ, BN, NS, NKS, NVS, DV>;
   const size_t smem = S_::bytes(a.batch, a.pairs_max);
   if (smem > 227 * 1024) {
     // the deep rings do not fit next to this batch's schedule: fewer slots
     if (NKS > 2)
-      return launch_varlen_t<D, NQ, BN, NS, (NKS > 2 ? NKS - 1 : 2), NVS>(a, maps, stream,
-                                                                          num_sms);
+      return launch_varlen_t<D, NQ, BN, NS, (NKS > 2 ? NKS - 1 : 2), NVS, DV>(a, maps, stream,
+                                                                              num_sms);
     if (NVS > 2)
-      return launch_varlen_t<D, NQ, BN, NS, NKS, (NVS > 2 ? NVS - 1 : 2)>(a, maps, stream,
-                                                                          num_sms);
+      return launch_varlen_t<D, NQ, BN, NS, NKS, (NVS > 2 ? NVS - 1 : 2), DV>(a, maps, stream,
+                                                                              num_sms);
     return cudaErrorNotSupported;
   }
   static int configured[64] = {0};
@@ -53,7 +53,7 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
     configured[dev] = (int)smem;
   }
   // persistent grid: one CTA per SM, never more CTAs than work items
-  const int64_t items_max = (int64_t)a.batch * a.H_kv * a.R;
+  const int64_t items_max = (int64_t)a.batch * a.H_kv * a.R * (D / DV);
   const int64_t grid = items_max < num_sms ? items_max : num_sms;
   if (grid <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
@@ -69,7 +69,15 @@ static cudaError_t launch_varlen_t(const VarlenArgs& a, const VarlenMaps& maps,
   return cudaLaunchKernelEx(&cfg, kern, a, maps.q, maps.k, maps.v);
 }
 
-int varlen_kv_tile(int head_dim) { return head_dim == 256 ? 64 : 128; }
+int varlen_kv_tile(int head_dim) {
+  return head_dim == 512 ? 32 : (head_dim == 256 ? 64 : 128);
+}
+
+// head_dim 512: one Q tile (128 x 512 bf16, 128 KB) fills half of shared
+// memory and its fp32 O would fill all 512 TMEM columns, so a work item
+// computes one 256-column half of O (S = Q K^T over all 512 dims, twice per
+// Q tile) over 32-key tiles.
+int varlen_v_cols(int head_dim) { return head_dim == 512 ? 256 : head_dim; }
 
 cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q,
                           const int32_t* cu_k, const int32_t* block_table, int32_t max_blocks,
@@ -116,6 +124,10 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
       a.R = (max_seqlen_q + QP - 1) / QP;
       a.pairs_max = batch * a.R;
       return launch_varlen_t<256, 1, 64, 2, 2, 2>(a, maps, stream, num_sms);
+    case 512:
+      a.R = (max_seqlen_q + QP - 1) / QP;
+      a.pairs_max = batch * a.R;
+      return launch_varlen_t<512, 1, 32, 2, 2, 2, 256>(a, maps, stream, num_sms);
     default:
       return cudaErrorNotSupported;
   }

@@ -55,7 +55,12 @@
 
 namespace pkv {
 
-constexpr int kMaxSortPairs = 256;  // (chunk, item) pairs ordered by exact length
+// (chunk, item) pairs ordered by exact length; head_dim 512 keeps fewer, its
+// tiles leave less shared memory for the schedule
+template <int D>
+constexpr int max_sort_pairs() {
+  return D >= 512 ? 32 : 256;
+}
 
 struct VarlenArgs {
   __nv_bfloat16* out;
@@ -74,25 +79,31 @@ struct VarlenArgs {
   int32_t* err;
 };
 
-template <int D, int NQ, int BN, int NS, int NKS, int NVS>
+// DV: the width of O (and of the V columns) one work item computes; D / DV
+// items cover a Q tile (head_dim 512: two halves of 256, each recomputing S)
+template <int D, int NQ, int BN, int NS, int NKS, int NVS, int DV = D>
 struct VarlenSmem {
   static constexpr int kQBytes = 128 * D * 2;              // one Q tile
   // a K/V tile is [row group][64-column chunk][8 rows][128 B]: 8-row atoms
-  // of a chunk kAtomStride apart, chunks 1024 B apart
+  // of a chunk kAtomStride apart (K: D/64 chunks; V: DV/64), chunks 1024 B
+  // apart
   static constexpr int kAtomStride = (D / 64) * 1024;
-  static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
+  static constexpr int kVAtomStride = (DV / 64) * 1024;
+  static constexpr int kSlotBytes = BN * D * 2;            // one K tile
+  static constexpr int kVSlotBytes = BN * DV * 2;          // one V tile (DV columns)
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + NQ * kQBytes;   // K ring: NKS tiles
   static constexpr int kVOff = kKOff + NKS * kSlotBytes;  // V ring: NVS tiles
-  static constexpr int kBarOff = kVOff + NVS * kSlotBytes;
+  static constexpr int kBarOff = kVOff + NVS * kVSlotBytes;
   // q_full[NQ] q_empty[NQ] k_full[NKS] k_empty[NKS] v_full[NVS] v_empty[NVS]
   // s_full[NQ*NS] p_full[NQ*NS] o_done[NQ]
   static constexpr int kNumBars = 2 * NQ + 2 * NKS + 2 * NVS + 2 * NQ * NS + NQ;
   static constexpr int kTmemOff = kBarOff + kNumBars * 8;
   static constexpr int kSchedOff = kTmemOff + 16;
   // then: q_len[B] k_len[B] pair_prefix[B+1] key[P] order[P] with
-  // P = min(pairs, kMaxSortPairs)
+  // P = min(pairs, max_sort_pairs<D>())
   static size_t bytes(int batch, int pairs) {
+    constexpr int kMaxSortPairs = max_sort_pairs<D>();
     const size_t np = (size_t)(pairs < kMaxSortPairs ? pairs : kMaxSortPairs);
     const size_t need = kSchedOff + (size_t)batch * 8 + (size_t)(batch + 1) * 4 + np * 8 + 16;
     // at least 116 KB so that only one CTA (and its 512 TMEM columns) fits
@@ -104,6 +115,7 @@ struct VarlenSmem {
 // Item geometry shared by every role of the CTA.
 struct Item {
   int b, g, qp;          // chunk, kv head, index of the item within the chunk
+  int half;              // which DV-wide part of O (0 when DV == D)
   int q0, q_len, k_len;  // chunk's first row in q/out, its query and key counts
   int p_begin;           // first chunk row of the item
   int t_lo, n;           // first KV tile, number of KV tiles (0: no key for any row)
@@ -112,11 +124,12 @@ struct Item {
 
 template <int NQ, int BN>
 __device__ __forceinline__ Item make_item(const VarlenArgs& a, int b, int g, int qp, int q0,
-                                          int q_len, int k_len) {
+                                          int q_len, int k_len, int half = 0) {
   Item it;
   it.b = b;
   it.g = g;
   it.qp = qp;
+  it.half = half;
   it.q0 = q0;
   it.q_len = q_len;
   it.k_len = k_len;
@@ -158,20 +171,22 @@ __host__ __device__ constexpr int varlen_threads() {
 // the block runs other work afterwards (the mixed-step kernel), so the
 // body gives the warps back the launch's register count and invalidates its
 // mbarriers before it returns.
-template <int D, int NQ, int BN, int NS, int NKS, int NVS, bool HOSTED>
+template <int D, int NQ, int BN, int NS, int NKS, int NVS, bool HOSTED, int DV = D>
 __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMap& tmQ,
                                            const CUtensorMap& tmK, const CUtensorMap& tmV,
                                            uint8_t* smem, int cta, int ncta) {
-  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS>;
+  using S_ = VarlenSmem<D, NQ, BN, NS, NKS, NVS, DV>;
+  constexpr int NH = D / DV;  // O parts per Q tile
+  static_assert(D % DV == 0 && DV % 64 == 0, "O parts");
   constexpr int NT = varlen_threads<NQ>();
   constexpr int kProdWarp = 4 * NQ;
   constexpr int kMmaWarp = 4 * NQ + 1;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, BN, false);
-  constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, D, true);
-  constexpr int kOCol = NQ * NS * BN;  // S/P buffer (x, b) at (x*NS + b)*BN; O_x at kOCol + x*D
-  static_assert(kOCol + NQ * D <= (int)kTmemCols, "TMEM columns");
-  static_assert(BN == 64 || BN == 128, "KV tile");
+  constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, DV, true);
+  constexpr int kOCol = NQ * NS * BN;  // S/P buffer (x, b) at (x*NS + b)*BN; O_x at kOCol + x*DV
+  static_assert(kOCol + NQ * DV <= (int)kTmemCols, "TMEM columns");
+  static_assert(BN == 32 || BN == 64 || BN == 128, "KV tile");
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S_::kBarOff);
   uint64_t* q_full = bars;                     // [NQ]
@@ -188,6 +203,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
   int* s_klen = s_qlen + a.batch;                              // clamped k_len per chunk
   int* s_pfx = s_klen + a.batch;                               // [B+1] pairs before chunk b
   int* s_key = s_pfx + a.batch + 1;                            // KV tiles of pair p
+  constexpr int kMaxSortPairs = max_sort_pairs<D>();
   int* s_porder = s_key + min(a.pairs_max, kMaxSortPairs);     // pairs, most tiles first
 
   const int tid = threadIdx.x;
@@ -228,7 +244,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
   // ------------------------------------------------ schedule (every CTA)
   // A pair (chunk b, item qp) covers NQ Q tiles of chunk b; with the H_kv
   // heads it makes H_kv work items of equal cost.  Pairs are ordered by
-  // their number of KV tiles, most first (exactly, up to kMaxSortPairs
+  // their number of KV tiles, most first (exactly, up to max_sort_pairs
   // pairs; beyond that in chunk order), and the sorted items are dealt to
   // the CTAs in a snake (0..N-1, N-1..0, ...) so that every CTA gets a
   // similar total.
@@ -282,18 +298,19 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     }
   }
   __syncthreads();
-  const int T = TP * a.H_kv;
+  const int T = TP * a.H_kv * NH;
   pdl_launch_dependents();
 
-  // item i (sorted order) -> (chunk, head, item within chunk); identical in
-  // every role
+  // item i (sorted order) -> (chunk, head, item within chunk, O part);
+  // identical in every role
   auto item_at = [&](int i) -> Item {
-    const int sp = i / a.H_kv;
-    const int g = i - sp * a.H_kv;
+    const int sp = i / (a.H_kv * NH);
+    const int r = i - sp * (a.H_kv * NH);
+    const int g = r / NH, half = r - (r / NH) * NH;
     const int p = sorted ? s_porder[sp] : sp;
     int b, qp;
     pair_at(p, b, qp);
-    return make_item<NQ, BN>(a, b, g, qp, __ldg(a.cu_q + b), s_qlen[b], s_klen[b]);
+    return make_item<NQ, BN>(a, b, g, qp, __ldg(a.cu_q + b), s_qlen[b], s_klen[b], half);
   };
   // the k-th item of this CTA (snake over the CTAs)
   const int NC = ncta;
@@ -324,7 +341,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     c.k = -1;
     c.j = 0;
     c.m = -1;
-    c.it = Item{0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    c.it = Item{0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     return c;
   };
 
@@ -399,6 +416,8 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     uint64_t* rfull = isK ? k_full : v_full;
     uint64_t* rempty = isK ? k_empty : v_empty;
     uint8_t* rbase = smem + (isK ? S_::kKOff : S_::kVOff);
+    const int slot_bytes = isK ? S_::kSlotBytes : S_::kVSlotBytes;
+    const int row_bytes = (isK ? D : DV) * 2;  // one key's columns in the slot
     const CUtensorMap* tm = isK ? &tmK : &tmV;
     const Box none = {0, 0, 0, false};
     Cursor c0 = cursor0();  // tile being loaded
@@ -411,12 +430,15 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     while (h0) {
       if (lane == 0) {
         if (t >= nring) mbar_wait(rempty + s, ph ^ 1, a.err, dead);
-        mbar_arrive_expect_tx(rfull + s, S_::kSlotBytes);
+        mbar_arrive_expect_tx(rfull + s, slot_bytes);
       }
       __syncwarp();
       const int z = box_z(b0);
-      if (lane < nbox)  // one box: this lane's page slice of the tile, all columns
-        tma_load_5d(rbase + s * S_::kSlotBytes + lane * R * D * 2, tm, rfull + s, 0, 0, 0,
+      // V: the item's DV-wide column part, starting at 64-column chunk
+      // half * DV / 64 of the pool rows
+      const int chunk0 = isK ? 0 : c0.it.half * (DV / 64);
+      if (lane < nbox)  // one box: this lane's page slice of the tile, its columns
+        tma_load_5d(rbase + s * slot_bytes + lane * R * row_bytes, tm, rfull + s, 0, 0, chunk0,
                     b0.row / 8, z);
       if (isK && c0.j == 0 && lane == 0) {
         // a new item: its Q tiles (after the K tile, which does not wait for
@@ -462,6 +484,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
       // LBO = the 1024 B chunk stride, atoms along the keys kAtomStride apart
       constexpr uint32_t kHi = tc::sw128_hi(1024);
       constexpr uint32_t kHiKV = tc::sw128_hi(S_::kAtomStride);
+      constexpr uint32_t kHiV = tc::sw128_hi(S_::kVAtomStride);
       const uint32_t q_lo0 = tc::sw128_lo(sQ, 16);
       const uint32_t k_lo0 = tc::sw128_lo(smem_u32(smem + S_::kKOff), 16);
       const uint32_t v_lo0 = tc::sw128_lo(smem_u32(smem + S_::kVOff), 1024);
@@ -506,22 +529,22 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
           // O_x (+)= P_x(t) V(t): A = P in the TMEM columns of S buffer (x, t % NS)
           const int sb = x * NS + t % NS;
           if (x == 0) mbar_wait_converged(v_full + sv, (t / NVS) & 1, a.err, dead);
-          const uint32_t blo = v_lo0 + sv * (S_::kSlotBytes >> 4);
+          const uint32_t blo = v_lo0 + sv * (S_::kVSlotBytes >> 4);
           // K=16 steps: 8 P columns and two 8-key atoms of V apart
-          constexpr uint32_t kVStep = (2 * S_::kAtomStride) >> 4;
+          constexpr uint32_t kVStep = (2 * S_::kVAtomStride) >> 4;
           mbar_wait_converged(p_full + sb, (t / NS) & 1, a.err, dead);
           tc::fence_after_sync();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (BN == 128) {
-              tc::mma_ts_x4<kVStep>(tmem + kOCol + x * D, tmem + sb * BN + h * 32,
-                                    blo + h * 4 * kVStep, kHiKV, kIdescO,
+              tc::mma_ts_x4<kVStep>(tmem + kOCol + x * DV, tmem + sb * BN + h * 32,
+                                    blo + h * 4 * kVStep, kHiV, kIdescO,
                                     (cv.j > 0 || h > 0) ? 1u : 0u);
             } else {
 #pragma unroll
               for (int ks = h * (BN / 32); ks < (h + 1) * (BN / 32); ++ks)
-                tc::mma_ts_w(tmem + kOCol + x * D, tmem + sb * BN + ks * 8, blo + ks * kVStep,
-                             kHiKV, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_ts_w(tmem + kOCol + x * DV, tmem + sb * BN + ks * 8, blo + ks * kVStep,
+                             kHiV, kIdescO, (cv.j > 0 || ks > 0) ? 1u : 0u);
             }
           }
           // O_x is read back only at the item's end (and, with two S
@@ -554,7 +577,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t o_addr = lane_base + kOCol + x * D;
+    const uint32_t o_addr = lane_base + kOCol + x * DV;
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
     int t = 0;
@@ -564,13 +587,15 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
       const int p = it.p_begin + x * QP + (r >> a.log2G);  // chunk row of this thread
       const bool row_valid = p < it.q_len;
       const int hh = r & (a.G - 1);
+      // this item's DV columns of the output row
       __nv_bfloat16* orow =
-          a.out + ((int64_t)(it.q0 + (row_valid ? p : 0)) * a.H_q + it.g * a.G + hh) * D;
+          a.out + ((int64_t)(it.q0 + (row_valid ? p : 0)) * a.H_q + it.g * a.G + hh) * D +
+          it.half * DV;
       if (it.n == 0) {  // no key for any row of the item: zero rows
         if (row_valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+          for (int v = 0; v < DV / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -661,14 +686,15 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
             tc::st_32x32b_x32(s_addr + h * 32,
                               *reinterpret_cast<const uint32_t(*)[32]>(&s[h * 32]));
           else
-            tc::st_32x32b_x16(s_addr + h * 16, &s[h * 16]);
+            (BN == 64) ? tc::st_32x32b_x16(s_addr + h * 16, &s[h * 16])
+                       : tc::st_32x32b_x8(s_addr + h * 8, &s[h * 8]);
           if (h == 0) {
             // O must be rescaled before the first half's PV; done here, once
             // the first half of the S row is dead, to keep registers free
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
               const uint64_t al2 = f2(alpha, alpha);
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
+              for (int c = 0; c < DV / 32; ++c) {
                 uint32_t o[32];
                 tc::ld_32x32b_x32(o_addr + c * 32, o);
                 tc::wait_ld();
@@ -702,7 +728,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
         tc::ld_32x32b_x32(o_addr + c * 32, o);
         tc::wait_ld();

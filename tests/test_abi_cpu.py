@@ -187,6 +187,8 @@ def test_shared_prefix_decode_validates_on_host(lib):
     assert call(gs=8) == 2                 # 8 members x 4 heads: 32 rows > 16 at head_dim 128
     assert call(D=512, H_q=8, H_kv=8, gs=1) == 2   # head_dim 512 has no prefix pass
     assert call(B=0, gs=4) == 0            # empty batch: no-op
-    # head_dim 512 is a decode shape but not a varlen one
-    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 8, 2, 512, 16, 64,
+    # head_dim 1024 is no shape of either call
+    assert L.paged_attn_varlen(P, P, P, P, P, P, P, 4, 2, 64, 64, 100, 8, 2, 1024, 16, 64,
                                0.1, 1, 0, None, None) == 2
+    assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 8, 2, 1024, 16, 64, 64, 0.1, 0, P,
+                               1 << 20, None, None) == 2

@@ -60,7 +60,7 @@ def test_varlen_tiny_single_chunk(pkv):
     assert_close_attn(got, want, "tiny")
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
 @pytest.mark.parametrize("H", [(8, 8), (8, 4), (8, 2), (8, 1), (32, 8)])
 def test_varlen_shapes(pkv, D, H):
     P = 64 if D == 256 else 16
@@ -203,3 +203,22 @@ def test_varlen_bad_page_flags_no_fault(pkv):
                                step.cu_seq_lens_k, step.pre_block_table, step.scale)
     assert_close_attn(bf16_dev_to_f64(out)[:64], want[:64], "untouched chunk")
     assert np.all(np.isfinite(bf16_dev_to_f64(out)))
+
+
+def test_varlen_head_dim_512_workload(pkv):
+    """The full-attention regime with 512-wide heads: 4 prefill chunks of
+    1024 tokens, 8 q heads on 1 kv head, page 16 (each Q tile's O is
+    computed in two 256-column halves)."""
+    step = wl.full_d512(n_dec=4)
+    vals = wl.fill_values(step, 512)
+    got, want, _ = _varlen(pkv, step, vals)
+    assert_close_attn(got, want, "head_dim 512 prefill")
+
+
+@pytest.mark.parametrize("window,P", [(100, 16), (0, 64), (513, 32)])
+def test_varlen_head_dim_512_window_pages(pkv, window, P):
+    step = _prefill_step(5120 + window + P, 16, 2, 512, P, [0, 300, 17], [400, 129, 64],
+                         window=window)
+    vals = wl.fill_values(step, 77)
+    got, want, _ = _varlen(pkv, step, vals)
+    assert_close_attn(got, want, f"D=512 window={window} P={P}")
