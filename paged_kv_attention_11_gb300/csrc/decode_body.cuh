@@ -160,8 +160,10 @@ struct DecodePlan {
 // hosts this body on part of its warps), so the body synchronises on a
 // named barrier of its own threads instead of the whole block.  `cta` is
 // this CTA's index among the a.cta_count CTAs that run the body; smem is the
-// 1024-aligned base of the dynamic shared memory.
-template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET>
+// 1024-aligned base of the dynamic shared memory.  LEAN: the merge keeps
+// fewer loads in flight, so that the body fits the register budget of a
+// larger block.
+template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET, bool LEAN = false>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
@@ -895,7 +897,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           //     unstaged, from loads issued in the same batch), so a merge
           //     costs a few L2 round trips.  Every output sums its chunks in
           //     chunk order.
-          constexpr int kMU = 4, kMC = 4;
+          constexpr int kMU = LEAN ? 2 : 4, kMC = LEAN ? 2 : 4;
           const int nslice = G * (D / 4);
           for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
             float4 acc[kMU];

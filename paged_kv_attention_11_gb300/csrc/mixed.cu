@@ -15,9 +15,9 @@
 //     with the static snake schedule over those N - nd CTAs), then join the
 //     decode queue and take whatever work is left in it.
 // Every CTA ends in the decode body, so the decode queue's last-CTA reset
-// and the zero rows of empty sequences work as in paged_attn_decode.  The
-// decode body gets more registers than the launch's 168 per thread through
-// setmaxnreg: warpgroups 0-1 (warps 0-7) go to 232, warpgroup 2 to 40.
+// and the zero rows of empty sequences work as in paged_attn_decode.  No
+// warp moves registers (setmaxnreg): both bodies run in the launch's 168 per
+// thread, the decode body with its lean merge.
 #include "decode_body.cuh"
 #include "tmap.h"
 #include "varlen_body.cuh"
@@ -28,6 +28,7 @@ struct MixedArgs {
   DecodeArgs dec;
   VarlenArgs var;
   int32_t has_dec, has_var;
+  int32_t var_first;  // first CTA that starts with the prefill
 };
 
 // the prefill shape of the mixed step (head_dim 128): two Q tiles per item,
@@ -47,19 +48,12 @@ __global__ void __launch_bounds__(kMixThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
-  const int nd = m.dec.share_ctas;
+  const int nd = m.var_first;
   if (m.has_var && (int)blockIdx.x >= nd)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
-  if (m.has_dec) {
-    if (warp >= 8) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
-    } else {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
-      if (warp < 6)
-        decode_cta<kMixD, 4, NSTAGE_DEC, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
-    }
-  }
+  if (m.has_dec && warp < 6)
+    decode_cta<kMixD, 4, NSTAGE_DEC, true, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
 }
 
 // CTAs that start with decode when the caller leaves the split open: the
@@ -101,12 +95,6 @@ static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const v
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (configured[dev] < (int)smem) {
-    // the prefill body moves registers to its softmax with setmaxnreg: the
-    // launch must hold 168 per thread
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * kMixThreads < 8 * 32 * 232 + 4 * 32 * 40) return cudaErrorNotSupported;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = (int)smem;
@@ -180,9 +168,10 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   if (nd <= 0)
     nd = mixed_decode_ctas(num_sms, L.dec_batch, L.dec_max_seq_len, L.total_q, L.max_seqlen_q,
                            L.max_seqlen_k, L.H_q, L.H_kv, L.D);
-  if (!m.has_var) nd = num_sms;
-  if (!m.has_dec) nd = 0;
   if (m.has_var && m.has_dec) nd = nd < 1 ? 1 : (nd > num_sms - 1 ? num_sms - 1 : nd);
+  if (!m.has_var) nd = num_sms;  // decode only: every CTA starts with decode
+  if (!m.has_dec) nd = 0;        // prefill only: every CTA runs the prefill
+  m.var_first = nd;
   a.cta_count = num_sms;
   a.share_ctas = nd > 0 ? nd : num_sms;
   // ---- shared memory: the larger of the two plans

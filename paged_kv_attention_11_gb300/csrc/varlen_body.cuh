@@ -168,8 +168,9 @@ __host__ __device__ constexpr int varlen_threads() {
 // The varlen work of one CTA (all varlen_threads<NQ>() threads of the
 // block).  `cta` is this CTA's index among the `ncta` CTAs that share the
 // static schedule; smem is the 1024-aligned dynamic shared memory.  HOSTED:
-// the block runs other work afterwards (the mixed-step kernel), so the
-// body gives the warps back the launch's register count and invalidates its
+// the block runs other work afterwards (the mixed-step kernel): every warp
+// keeps the launch's register count (no setmaxnreg moves, so each code path
+// after the body sees the same budget) and the body invalidates its
 // mbarriers before it returns.
 template <int D, int NQ, int BN, int NS, int NKS, int NVS, bool HOSTED, int DV = D>
 __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMap& tmQ,
@@ -366,7 +367,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
   // threads x 168 registers; after the change 4 warps x 104 + 8 warps x 200
   // use the same total, and every SM sub-partition holds at most 504 per lane.
   if (warp >= kProdWarp) {
-    if (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
+    if (NQ == 2 && !HOSTED) asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
   if (warp == kProdWarp || warp == kProdWarp + 2) {
     // ====================== TMA producers: K (+Q) and V ======================
     // Warp kProdWarp loads the Q tiles and the K tiles, warp kProdWarp+2 the
@@ -570,7 +571,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
     }
   }
   } else {
-    if (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
+    if (NQ == 2 && !HOSTED) asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     // ======================== softmax warpgroups ============================
     bool dead = false;
     const int x = warp >> 2;  // which Q tile of the item
@@ -746,10 +747,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
       }
       tc::fence_before_sync();
     }
-    if (HOSTED && NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
   }
-  if (HOSTED && NQ == 2 && warp >= kProdWarp)
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
 
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -115,3 +115,20 @@ def test_mixed_step_twice_on_one_workspace(pkv, mixed_case):
     od2, op2 = _run(pkv, step, vals, kc, vc, ws=ws)
     assert np.array_equal(bf16_dev_to_bits(od1), bf16_dev_to_bits(od2))
     assert np.array_equal(bf16_dev_to_bits(op1), bf16_dev_to_bits(op2))
+
+
+def test_mixed_step_small(pkv):
+    """A small mixed step (2 prefill chunks, 8 decode rows, 4/2/128 heads)
+    with the split at 3 decode-first CTAs."""
+    import torch
+    step = wl.mixed_step(n_chunks=2, n_dec=8, H_q=8, H_kv=2, num_pages=2048)
+    vals = wl.fill_values(step, 11)
+    kc, vc = to_dev_bf16(vals.k_cache), to_dev_bf16(vals.v_cache)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(to_dev_bf16(vals.k_new), to_dev_bf16(vals.v_new), kc, vc,
+                        to_dev(step.all_slots), err_flag=err)
+    hk, hv = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, step.all_slots)
+    od, op = _run(pkv, step, vals, kc, vc, decode_ctas=3)
+    wd, wp = _want(step, vals, hk, hv)
+    assert_close_attn(bf16_dev_to_f64(od), wd, "small mixed decode")
+    assert_close_attn(bf16_dev_to_f64(op), wp, "small mixed prefill")
