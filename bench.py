@@ -433,10 +433,14 @@ def run_ours(args):
             import torch.distributed as dist
             dist.barrier()
 
-    if args.only == "mixed":
-        mixed = run_mixed(args, device, stream, flush, rank)
+    sections = {"mixed": ("mixed_step", run_mixed), "sliding": ("sliding_step", run_sliding),
+                "grpo": ("grpo_step", run_grpo), "d512": ("head_dim_512_step", run_full512)}
+    if args.only in sections:
+        # one section alone (profiling runs)
+        key, fn = sections[args.only]
+        res = fn(args, device, stream, flush, rank)
         if rank == 0:
-            print(json.dumps({"metric": "mixed-step tokens/sec", "mixed_step": mixed}), flush=True)
+            print(json.dumps({"metric": METRIC, key: res}), flush=True)
         return
 
     # ---- headline: Qwen3-shaped decode step -------------------------------
@@ -884,8 +888,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true",
                     help="omit the CPU oracle baseline (profiling runs)")
-    ap.add_argument("--only", choices=["decode", "mixed"], default=None,
-                    help="run only the decode step or only the mixed step (profiling runs)")
+    ap.add_argument("--only", choices=["decode", "mixed", "sliding", "grpo", "d512"],
+                    default=None,
+                    help="run only one section: the headline decode step, the mixed step, "
+                         "the sliding-window step, the GRPO step or the head_dim 512 step "
+                         "(profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -48,7 +48,7 @@ constexpr int kMergeLse = 1024;  // (piece, head) log-sum-exps staged in smem fo
 // Shortest chunk a segment is cut into (tiles).  Small batches (a few long
 // windowed segments) then still spread over every SM instead of one segment
 // per CTA; large batches cut at half a CTA's share, far above this floor.
-constexpr int kMinChunkTiles = 4;
+constexpr int kMinChunkTiles = 16;
 constexpr int kMaxSortSeq = 512;  // longest-first queue order up to this batch
 
 struct DecodeArgs {

@@ -57,10 +57,10 @@ def _case(seed, B, long_len, H_q=32, H_kv=8, D=128, P=16):
 def _longest_segment_is_split(lens, H_kv, P, n_sms):
     """The decode kernel cuts a (sequence, kv head) segment into chunks when
     it has more 16-key tiles than half of one CTA's share of the batch's
-    tiles (one persistent CTA per SM) and more than 4."""
+    tiles (one persistent CTA per SM) and more than 16."""
     tiles = -(-lens.astype(np.int64) // 16)
     half_share = -(-int(tiles.sum()) * H_kv // (2 * n_sms))
-    return int(tiles.max()) > max(4, half_share)
+    return int(tiles.max()) > max(16, half_share)
 
 
 def _args(out, q, kc, vc, bt, lens, scale):
