@@ -39,33 +39,42 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
 # from an ncu capture on a GB300, with the SHA-256 prefix of the kernel's
-# source file at capture time.  A value is reported only while the source
-# still has that hash; once the kernel changes the field is null until a new
-# capture replaces the entry.
+# source files (concatenated, in the order listed) at capture time.  A value
+# is reported only while the sources still have that hash; once the kernel
+# changes the field is null until a new capture replaces the entry.  The
+# summaries under profiles/ give the command and the other counters.
 #   decode_qwen3: decode_split_kernel<128,4,24,1> on the qwen3_decode step
-#                 (316.78 + 4.15 MB; profiles/decode_split_kernel_qwen3_decode.md)
-#   varlen_mixed: varlen_fwd_kernel<128,2,128,1,3,2> on the mixed step
-#                 (78.50 + 9.11 MB; profiles/varlen_fwd_kernel_mixed_step.md)
-#   append_rope_mixed: kv_append_rope_kernel<128> on the mixed step, both
-#                 norms (70.27 + 13.77 MB; profiles/kv_append_rope_kernel_mixed_step.md)
+#   decode_d512:  decode_split_kernel<512,2,4,0> on the head_dim 512 step
+#   varlen_mixed: varlen_fwd_kernel<128,2,128,1,3,2,128> on the mixed step
+#   varlen_d512:  varlen_fwd_kernel<512,1,32,2,2,2,256> on the head_dim 512 step
+#   mixed_single: mixed_step_kernel<24> on the mixed step
+#   append_rope_mixed: kv_append_rope_kernel<128> on the mixed step, both norms
+_DEC_SRC = ("decode.cu", "decode_body.cuh", "tile16.cuh", "common.cuh")
+_VAR_SRC = ("varlen.cu", "varlen_body.cuh", "tcgen05.cuh", "exp2_math.cuh", "common.cuh")
+_MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcgen05.cuh", "exp2_math.cuh", "common.cuh")
 TRAFFIC = {
-    "decode_qwen3": (320_930_048, "decode.cu", "24056982da403059"),
-    "varlen_mixed": (87_604_224, "varlen.cu", "8c512d957a881826"),
-    "append_rope_mixed": (84_039_936, "rope_append.cu", "e68e8d036bcc4835"),
+    "decode_qwen3": (320_338_176, _DEC_SRC, "6f3ecdc387ae482f"),
+    "decode_d512": (573_545_984, _DEC_SRC, "6f3ecdc387ae482f"),
+    "varlen_mixed": (87_270_400, _VAR_SRC, "810427e15105ef5f"),
+    "varlen_d512": (42_845_952, _VAR_SRC, "810427e15105ef5f"),
+    "mixed_single": (1_220_206_336, _MIX_SRC, "339460b49c782943"),
+    "append_rope_mixed": (84_039_936, ("rope_append.cu",), "e68e8d036bcc4835"),
 }
 
 
 def traffic_bytes(key: str):
-    """The captured traffic of TRAFFIC[key], or None when the kernel source
-    has changed since the capture."""
+    """The captured traffic of TRAFFIC[key], or None when a kernel source
+    file has changed since the capture."""
     import hashlib
-    nbytes, src, sha = TRAFFIC[key]
-    path = os.path.join(ROOT, "paged_kv_attention_11_gb300", "csrc", src)
+    nbytes, files, sha = TRAFFIC[key]
+    m = hashlib.sha256()
     try:
-        cur = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+        for f in files:
+            with open(os.path.join(ROOT, "paged_kv_attention_11_gb300", "csrc", f), "rb") as fh:
+                m.update(fh.read())
     except OSError:
         return None
-    return nbytes if cur == sha else None
+    return nbytes if m.hexdigest()[:16] == sha else None
 
 
 # ------------------------------------------------------------------ helpers
@@ -585,8 +594,10 @@ def run_mixed(args, device, stream, flush, rank):
         fms = float(np.mean([sum(p) for p in fused_step]))
         fused = {"value": round(tokens / (fms * 1e-3), 1), "unit": "tokens/s",
                  "ms_per_step": round(fms, 5),
+                 "traffic": traffic_bytes("mixed_single"),
                  "note": "append, then paged_attn_mixed: decode rows and prefill chunks in one "
-                         "persistent launch (split chosen by the library)"}
+                         "persistent launch (split chosen by the library); traffic is the "
+                         "mixed kernel's DRAM bytes per launch"}
     except Exception as e:
         fused = {"unavailable": f"{type(e).__name__}: {e}"}
     # the same step with q/k RMSNorm and the rotary embedding fused into the
@@ -756,10 +767,11 @@ def run_full512(args, device, stream, flush, rank):
             "decode_roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
                                 "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                                 "peak_source": src, "algorithmic_bytes": int(db),
-                                "traffic": None},
+                                "traffic": traffic_bytes("decode_d512")},
             "varlen_roofline": {"bound": "tensor", "achieved": round(tfs, 2), "peak": tf_peak,
                                 "unit": "TFLOP/s", "frac": round(tfs / tf_peak, 4),
-                                "peak_source": src, "algorithmic_flops": fl, "traffic": None,
+                                "peak_source": src, "algorithmic_flops": fl,
+                                "traffic": traffic_bytes("varlen_d512"),
                                 "note": "algorithmic flops count QK^T once; the kernel "
                                         "computes it for each 256-column half of O"}}
 

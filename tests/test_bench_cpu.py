@@ -99,3 +99,13 @@ def test_positions_agree_with_slots():
                   + [step.dec_block_table[b] for b in range(step.Bd)])
         slots = np.array([int(t[p // step.P]) * step.P + p % step.P for t, p in zip(tables, pos)])
         assert np.array_equal(slots, step.all_slots)
+
+
+def test_traffic_entries_name_existing_sources():
+    # every captured-traffic entry hashes files that exist, and the value is
+    # either the capture's byte count or None (sources changed since)
+    for key, (nbytes, files, sha) in bench.TRAFFIC.items():
+        for f in files:
+            assert os.path.isfile(os.path.join(bench.ROOT, "paged_kv_attention_11_gb300", "csrc", f)), f
+        assert len(sha) == 16 and nbytes > 0
+        assert bench.traffic_bytes(key) in (nbytes, None)
