@@ -9,7 +9,6 @@
 #include "kernels.h"
 #include "tmap.h"
 
-using pkv::encode_pool_map;
 using pkv::encode_pool_map_groups;
 using pkv::encode_q_map;
 

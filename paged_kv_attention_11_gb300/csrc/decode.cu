@@ -5,14 +5,15 @@
 
 namespace pkv {
 
-template <int D, int NW, int NSTAGE, bool ONEBOX>
+template <int D, int NW, int NSTAGE>
 __global__ void __launch_bounds__((NW + 2) * 32, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  decode_cta<D, NW, NSTAGE, ONEBOX, false>(a, tmK, tmV, smem, blockIdx.x);
+  // 8 consumer warps leave 168 registers a thread: the merge keeps fewer loads in flight
+  decode_cta<D, NW, NSTAGE, false, (NW >= 8)>(a, tmK, tmV, smem, blockIdx.x);
 }
 
 // --------------------------------------------------------------- host side
@@ -27,9 +28,6 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
 #endif
 #ifndef PKV_DEC_CTAS
 #define PKV_DEC_CTAS 1
-#endif
-#ifndef PKV_DEC_ONEBOX
-#define PKV_DEC_ONEBOX 1   // head_dim 128: one contiguous 4 KB TMA box per tile
 #endif
 template <int D>
 struct DecodeCfg;
@@ -88,15 +86,13 @@ static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
   using P_ = DecodePlan<D, NW, NSTAGE>;
-  constexpr bool kOneBox = (D == 128) && (PKV_DEC_ONEBOX != 0);
-  auto kern = decode_split_kernel<D, NW, NSTAGE, kOneBox>;
+  auto kern = decode_split_kernel<D, NW, NSTAGE>;
   (void)max_seq_len;
+  // one TMA box per 16-key K or V tile (all D columns of one page and head)
   CUtensorMap tmK, tmV;
   const bool enc_ok =
-      kOneBox ? (encode_pool_map_halves(&tmK, k_cache, a.P, a.num_pages, a.H_kv) &&
-                 encode_pool_map_halves(&tmV, v_cache, a.P, a.num_pages, a.H_kv))
-              : (encode_pool_map(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv) &&
-                 encode_pool_map(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv));
+      encode_pool_map_groups(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv, kTile) &&
+      encode_pool_map_groups(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv, kTile);
   if (!enc_ok) return cudaErrorInvalidValue;
   const size_t smem = P_(a.G, a.batch).total;
   if (smem > 227 * 1024) return cudaErrorNotSupported;

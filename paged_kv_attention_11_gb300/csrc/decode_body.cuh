@@ -50,6 +50,16 @@ constexpr int kMergeLse = 1024;  // (piece, head) log-sum-exps staged in smem fo
 // per CTA; large batches cut at half a CTA's share, far above this floor.
 constexpr int kMinChunkTiles = 16;
 constexpr int kMaxSortSeq = 512;  // longest-first queue order up to this batch
+// Batches up to this size keep each sequence's clamped length in shared
+// memory, so the producer maps a queue index to its item without a global
+// load; larger ones re-read seq_lens.
+constexpr int kLenCacheSeq = 1024;
+
+// a compile-time int carried by value (for generic lambdas)
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -83,15 +93,12 @@ struct DecodeArgs {
 
 // Keys [lo, L) of sequence b are attended here; returns the tile range and
 // whether a prefix partial covers keys [0, lo).
-__device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, int& lo,
-                                           int& t_lo, int& t_hi, bool flag, int* pfx = nullptr) {
-  int len = __ldg(a.seq_lens + b);
+// The attended keys [lo, len) of sequence b of (clamped) length len and its
+// 16-key tiles [t_lo, t_hi): the window, or the shared prefix of a cascade
+// (pfx = 1: a prefix partial joins the merge).
+__device__ __forceinline__ void extent_of_len(const DecodeArgs& a, int b, int len, int& lo,
+                                              int& t_lo, int& t_hi, int* pfx) {
   const int cap = a.max_blocks * a.P;
-  if (len < 0 || len > cap) {
-    if (flag) raise_err(a.err, PKV_DEVERR_LEN);
-    len = len < 0 ? 0 : cap;
-  }
-  L = len;
   lo = (a.window > 0 && len > a.window) ? len - a.window : 0;
   int has_pfx = 0;
   if (a.prefix_lens != nullptr) {
@@ -104,6 +111,20 @@ __device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, i
   if (pfx) *pfx = has_pfx;
   t_lo = lo / kTile;
   t_hi = (len + kTile - 1) / kTile;
+}
+
+// Length of sequence b from seq_lens, clamped to the block table (flag:
+// raise PKV_DEVERR_LEN for an out-of-range length), and its extent.
+__device__ __forceinline__ void seq_extent(const DecodeArgs& a, int b, int& L, int& lo,
+                                           int& t_lo, int& t_hi, bool flag, int* pfx = nullptr) {
+  int len = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks * a.P;
+  if (len < 0 || len > cap) {
+    if (flag) raise_err(a.err, PKV_DEVERR_LEN);
+    len = len < 0 ? 0 : cap;
+  }
+  L = len;
+  extent_of_len(a, b, len, lo, t_lo, t_hi, pfx);
 }
 
 // A piece as the producer hands it to the consumers and the epilogue.
@@ -119,12 +140,10 @@ struct PieceRec {
 };
 
 // Head dims of 512 and more keep the query rows in shared memory (read with
-// ldmatrix per tile) instead of registers, which then hold only O, and hand
-// consumer states to the epilogue through one combine buffer instead of two.
+// ldmatrix per tile) instead of registers, which then hold only O.
 template <int D>
 struct DecodeLayout {
   static constexpr bool kQSmem = D >= 512;
-  static constexpr int kNComb = kQSmem ? 1 : 2;
   // query rows in a record slot: kQSmem: kGP rows padded by 16 bytes (rows
   // G..kGP-1 zero), so that the 8 rows of an ldmatrix hit distinct banks
   static constexpr int kQRowBytes = kQSmem ? D * 2 + 16 : D * 2;
@@ -138,19 +157,23 @@ struct DecodePlan {
   static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
   static constexpr int kCombStride = D + 4;             // padded row (floats)
+  // consumer states reach the epilogue through two combine buffers, or one
+  // where the buffer is large (head_dim 512, or 8 consumer warps)
+  static constexpr int kNComb = (Lay::kQSmem || NW >= 8) ? 1 : 2;
   int rec, qbuf, qslot, comb, ml, bars, ok, misc, scan, cum, total;
   __host__ __device__ DecodePlan(int G, int batch) {
     int o = NSTAGE * kStageBytes;
     rec = o;   o += kNRec * (int)sizeof(PieceRec);
     qslot = (Lay::kQSmem ? kGP : G) * Lay::kQRowBytes;
     qbuf = o;  o += kNRec * qslot;
-    comb = o;  o += Lay::kNComb * NW * G * kCombStride * 4;
-    ml = o;    o += Lay::kNComb * NW * G * 2 * 4;
-    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 2 * Lay::kNComb) * 8;
+    comb = o;  o += kNComb * NW * G * kCombStride * 4;
+    ml = o;    o += kNComb * NW * G * 2 * 4;
+    bars = o;  o += (2 * NSTAGE + 2 * kNRec + 2 * kNComb) * 8;
     ok = o;    o += NSTAGE * 4;
     misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
     scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
-    cum = o;   o += (batch + 1) * 4 * 3;  // natural prefix, sorted prefix, order
+    // natural prefix, sorted prefix, order; lengths up to kLenCacheSeq sequences
+    cum = o;   o += (batch + 1) * 4 * (batch <= kLenCacheSeq ? 4 : 3);
     total = 1024 + o;
   }
 };
@@ -163,7 +186,7 @@ struct DecodePlan {
 // 1024-aligned base of the dynamic shared memory.  LEAN: the merge keeps
 // fewer loads in flight, so that the body fits the register budget of a
 // larger block.
-template <int D, int NW, int NSTAGE, bool ONEBOX, bool SUBSET, bool LEAN = false>
+template <int D, int NW, int NSTAGE, bool SUBSET, bool LEAN = false>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
@@ -171,12 +194,12 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   using P_ = DecodePlan<D, NW, NSTAGE>;
   using Lay = DecodeLayout<D>;
   constexpr bool QS = Lay::kQSmem;
-  constexpr int NCB = Lay::kNComb;
+  constexpr int NCB = P_::kNComb;
   constexpr int NT = (NW + 2) * 32;
   constexpr int KS = D / 16;  // mma k-steps for QK, m-tiles for PV
-  constexpr int kBoxBytes = kTile * 128;
   constexpr int CS = P_::kCombStride;
-  constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;  // producer lanes issuing TMA
+  constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;  // producer lanes testing stages
+  static_assert(kIssueLanes < 32, "a run of free stages ends inside the warp");
   const int G = a.G;
   const P_ plan(G, a.batch);
 
@@ -204,6 +227,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   int* s_nat = reinterpret_cast<int*>(smem + plan.cum);         // [B+1] items before b
   int* s_sp = s_nat + (a.batch + 1);                            // [B+1] sorted prefix
   int* s_order = s_sp + (a.batch + 1);                          // [B] sequences, longest first
+  int* s_len = a.batch <= kLenCacheSeq ? s_order + (a.batch + 1) : nullptr;  // [B] lengths
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -273,6 +297,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       seq_extent(a, b, L, lo, tl, th, cta == 0);
       const int t = th - tl;
       s_nat[b] = t;  // tiles, for now
+      if (s_len) s_len[b] = L;
       local += t;
       // zero-length sequences have no work item: their zero rows are written here
       if (t == 0 && b % a.cta_count == cta) {
@@ -305,10 +330,23 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   block_sync();
   // queue order: sequences by chunk length, longest first, ties by index
   // (up to kMaxSortSeq sequences; beyond, the natural order).  The rank of b
-  // is the number of sequences that come before it: the B x B comparisons
-  // run in rows of 32 spread over all threads, ranks accumulate in s_order,
-  // and every thread then scatters its sequences to their ranks.
-  if (B <= kMaxSortSeq) {
+  // is the number of sequences that come before it.  Up to one sequence per
+  // thread, each thread counts its own; beyond, the B x B comparisons run in
+  // rows of 32 spread over all threads, ranks accumulate in s_order, and
+  // every thread then scatters its sequences to their ranks.
+  if (B <= NT) {
+    // one thread per sequence: its rank is the number of keys ahead of it
+    if (tid < B) {
+      const int kb = s_sp[tid];
+      int r = 0;
+#pragma unroll 8
+      for (int c = 0; c < B; ++c) {
+        const int kc = s_sp[c];
+        r += (kc > kb || (kc == kb && c < tid)) ? 1 : 0;
+      }
+      s_order[r] = tid;
+    }
+  } else if (B <= kMaxSortSeq) {
     for (int b = tid; b < B; b += NT) s_order[b] = 0;
     block_sync();
     const int nc = (B + 31) / 32;
@@ -419,7 +457,12 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       const int b = s_order[lo];
       const int j = i - s_sp[lo];
       int L, klo, t_lo, t_hi, pfx;
-      seq_extent(a, b, L, klo, t_lo, t_hi, false, &pfx);
+      if (s_len) {
+        L = s_len[b];
+        extent_of_len(a, b, L, klo, t_lo, t_hi, &pfx);
+      } else {
+        seq_extent(a, b, L, klo, t_lo, t_hi, false, &pfx);
+      }
       const int t = t_hi - t_lo;
       const int nch = nch_of(t);
       const int csz = (t + nch - 1) / nch;
@@ -439,6 +482,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     auto prefetch = [&](const Item& p, uint4 (&qr)[QV], int& pages) {
       pages = -1;
       if (!p.more) return;
+      // page ids first: the first TMA copies need them, the query rows only
+      // the record
+      if (lane < p.n)
+        pages = __ldg(a.block_table + (int64_t)p.b * a.max_blocks +
+                      ((p.first_tile + lane) * kTile) / a.P);
       const uint4* qsrc =
           reinterpret_cast<const uint4*>(a.q + ((int64_t)p.b * a.H_q + p.g * G) * D);
 #pragma unroll
@@ -446,9 +494,6 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         const int v = lane + 32 * i;
         if (v < qvec) qr[i] = __ldg(qsrc + v);
       }
-      if (lane < p.n)
-        pages = __ldg(a.block_table + (int64_t)p.b * a.max_blocks +
-                      ((p.first_tile + lane) * kTile) / a.P);
     };
 
     Item cur = item_at(__shfl_sync(0xffffffffu, first_grab, 0));
@@ -458,41 +503,53 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     int it = 0;  // CTA-wide tile counter
     int k = 0;   // item counter
     while (true) {
-      // ---- publish the item record and its query rows ----
-      const int slot = k % kNRec;
-      if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
-      if (cur.more) {
-        uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * plan.qslot);
+      // ---- the item record and its query rows, to the consumers and the
+      //      epilogue.  It goes out after the item's first window of tiles
+      //      is issued, or before the first wait on a busy stage, whichever
+      //      comes first (the item's own consumers may be the ones to free
+      //      that stage), so the first copies of a CTA leave without waiting
+      //      for the query rows. ----
+      bool published = false;
+      auto publish = [&]() {
+        const int slot = k % kNRec;
+        if (k >= kNRec) mbar_wait(rec_empty + slot, ((k / kNRec) - 1) & 1, a.err, dead);
+        if (cur.more) {
+          uint4* qdst = reinterpret_cast<uint4*>(qbuf + slot * plan.qslot);
 #pragma unroll
-        for (int i = 0; i < QV; ++i) {
-          const int v = lane + 32 * i;
-          if (v < qvec) {
-            if (QS) {  // padded rows: vector v of head v / (D/8)
-              const int h = v / (D / 8);
-              qdst[v + h] = qcur[i];
-            } else {
-              qdst[v] = qcur[i];
+          for (int i = 0; i < QV; ++i) {
+            const int v = lane + 32 * i;
+            if (v < qvec) {
+              if (QS) {  // padded rows: vector v of head v / (D/8)
+                const int h = v / (D / 8);
+                qdst[v + h] = qcur[i];
+              } else {
+                qdst[v] = qcur[i];
+              }
             }
           }
         }
+        if (lane == 0) {
+          PieceRec& r = recs[slot];
+          r.b = cur.b;
+          r.g = cur.g;
+          r.first_tile = cur.first_tile;
+          r.n = cur.n;
+          r.L = cur.L;
+          r.lo = cur.lo;
+          r.nch = cur.nch;
+          r.slot0 = cur.slot0;
+          r.chunk = cur.chunk;
+          r.pfx = cur.pfx;
+        }
+        __syncwarp();
+        mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
+        ++k;
+        published = true;
+      };
+      if (!cur.more) {
+        publish();
+        break;
       }
-      if (lane == 0) {
-        PieceRec& r = recs[slot];
-        r.b = cur.b;
-        r.g = cur.g;
-        r.first_tile = cur.first_tile;
-        r.n = cur.n;
-        r.L = cur.L;
-        r.lo = cur.lo;
-        r.nch = cur.nch;
-        r.slot0 = cur.slot0;
-        r.chunk = cur.chunk;
-        r.pfx = cur.pfx;
-      }
-      __syncwarp();
-      mbar_arrive(rec_full + slot);  // all 32 lanes: each releases its own writes
-      ++k;
-      if (!cur.more) break;
       // ---- stream the item's tiles ----
       const int* bt = a.block_table + (int64_t)cur.b * a.max_blocks;
       const int n = cur.n;
@@ -502,17 +559,31 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         if (k0 + 32 + lane < n)
           page_ahead = __ldg(bt + ((cur.first_tile + k0 + 32 + lane) * kTile) / a.P);
         const int cnt = min(32, n - k0);
-        // NL lanes issue NL tiles at once, each into its own stage: one warp
-        // instruction launches NL TMA copies instead of one
-        for (int j0 = 0; j0 < cnt; j0 += kIssueLanes) {
-          const int j = j0 + lane;
-          const int pg = __shfl_sync(0xffffffffu, page, j & 31);
-          if (lane < kIssueLanes && j < cnt) {
-            const int itj = it + j;
-            const int s = itj % NSTAGE;
-            const int r = itj / NSTAGE;
-            if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
-            const int key0 = (cur.first_tile + k0 + j) * kTile;
+        // Tiles go out in order, each as soon as its own stage is free:
+        // lanes test the stages of the next kIssueLanes tiles (distinct
+        // stages, so no test can see a phase two rounds old), and the run of
+        // free stages from the first one is issued by one warp instruction.
+        // When the first stage is still busy, lane 0 waits on it alone; the
+        // consumers free stages in order, so it is the next to free.
+        for (int j = 0; j < cnt;) {
+          const int jl = j + lane;
+          const int pg = __shfl_sync(0xffffffffu, page, jl & 31);
+          const int itj = it + jl;
+          const int s = itj % NSTAGE;
+          const int r = itj / NSTAGE;
+          const bool mine = lane < kIssueLanes && jl < cnt;
+          const bool free_ = mine && (r == 0 || mbar_test_wait(empty + s, (r - 1) & 1));
+          const uint32_t fm = __ballot_sync(0xffffffffu, free_);
+          int run = __ffs(~fm) - 1;  // free stages in a row from tile j
+          if (run == 0) {
+            if (!published) publish();
+            if (lane == 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
+            __syncwarp();
+            run = 1;
+            if (__shfl_sync(0xffffffffu, (int)dead, 0)) dead = true;
+          }
+          if (lane < run) {
+            const int key0 = (cur.first_tile + k0 + jl) * kTile;
             const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
             stage_ok[s] = ok ? 1 : 0;
             if (ok) {
@@ -520,24 +591,18 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
               mbar_arrive_expect_tx(full + s, P_::kStageBytes);
               const int row = key0 % a.P;
               const int z = pg * a.H_kv + cur.g;
-              if (ONEBOX) {
-                tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
-                tma_load_4d(st + P_::kTileBytes, &tmV, full + s, 0, 0, row, z);
-              } else {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                  tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
-                  tma_load_3d(st + P_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
-                              z);
-                }
-              }
+              // one box per tile: 16 keys x all D columns of one page and head
+              tma_load_5d(st, &tmK, full + s, 0, 0, 0, row / 8, z);
+              tma_load_5d(st + P_::kTileBytes, &tmV, full + s, 0, 0, 0, row / 8, z);
             } else {
               raise_err(a.err, PKV_DEVERR_PAGE);
               mbar_arrive(full + s);
             }
           }
           __syncwarp();
+          j += run;
         }
+        if (!published) publish();
         it += cnt;
         page = page_ahead;
       }
@@ -624,15 +689,15 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
               uint32_t b00, b01, b10, b11;
               ldsm_x4(q_lane_addr + ks * 32, b00, b01, b10, b11);
               uint32_t a0, a1, a2, a3;
-              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+              ldsm_x4(tile_addr<D>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
               mma_bf16_16816(sa, a0, a1, a2, a3, b00, b01);
-              ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
+              ldsm_x4(tile_addr<D>(stK, key, 2 * ks + 2 + (lane >> 4)), a0, a1, a2, a3);
               mma_bf16_16816(sb, a0, a1, a2, a3, b10, b11);
             }
           } else {
 #pragma unroll
             for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
-              const uint32_t addr = tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4));
+              const uint32_t addr = tile_addr<D>(stK, key, 2 * ks + (lane >> 4));
               uint32_t a0, a1, a2, a3;
               ldsm_x4(addr, a0, a1, a2, a3);
               if (ks & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
@@ -681,7 +746,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           const int key = (lane & 7) + (j >> 1) * 8;
 #pragma unroll
           for (int md = 0; md < KS; ++md) {
-            const uint32_t addr = tile_addr<D, ONEBOX>(stV, key, 2 * md + (j & 1));
+            const uint32_t addr = tile_addr<D>(stV, key, 2 * md + (j & 1));
             uint32_t a0, a1, a2, a3;
             ldsm_x4_t(addr, a0, a1, a2, a3);
             mma_bf16_16816(o[md], a0, a1, a2, a3, pb0, pb1);
@@ -895,76 +960,83 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           //     lane and load.  Each lane keeps kMU slices x kMC chunks of
           //     loads in flight; the weights come from shared memory (or,
           //     unstaged, from loads issued in the same batch), so a merge
-          //     costs a few L2 round trips.  Every output sums its chunks in
-          //     chunk order.
-          constexpr int kMU = LEAN ? 2 : 4, kMC = LEAN ? 2 : 4;
+          //     costs a few L2 round trips.  Two chunks (the common split)
+          //     take twice the slices per batch instead of idle chunk slots.
+          //     Every output sums its chunks in chunk order.
           const int nslice = G * (D / 4);
-          for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
-            float4 acc[kMU];
-            int hh[kMU], dd[kMU];
+          auto wsum = [&](auto mu_c, auto mc_c) {
+          constexpr int kMU = decltype(mu_c)::value, kMC = decltype(mc_c)::value;
+            for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
+              float4 acc[kMU];
+              int hh[kMU], dd[kMU];
 #pragma unroll
-            for (int u = 0; u < kMU; ++u) {
-              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-              const int j = j0 + 32 * u < nslice ? j0 + 32 * u : 0;
-              hh[u] = j / (D / 4);
-              dd[u] = j - hh[u] * (D / 4);
-            }
-            for (int c0 = 0; c0 < np; c0 += kMC) {
-              float4 v[kMU][kMC];
-              float w[kMU][kMC];
-#pragma unroll
-              for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                for (int cc = 0; cc < kMC; ++cc) {
-                  const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
-                  v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
-                }
-              if (staged) {
-#pragma unroll
-                for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                  for (int cc = 0; cc < kMC; ++cc)
-                    w[u][cc] = c0 + cc < np ? merge_lse[(c0 + cc) * G + hh[u]] : 0.f;
-              } else {
+              for (int u = 0; u < kMU; ++u) {
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int j = j0 + 32 * u < nslice ? j0 + 32 * u : 0;
+                hh[u] = j / (D / 4);
+                dd[u] = j - hh[u] * (D / 4);
+              }
+              for (int c0 = 0; c0 < np; c0 += kMC) {
+                float4 v[kMU][kMC];
+                float w[kMU][kMC];
 #pragma unroll
                 for (int u = 0; u < kMU; ++u)
 #pragma unroll
                   for (int cc = 0; cc < kMC; ++cc) {
-                    const int c = c0 + cc < np ? c0 + cc : np - 1;
-                    w[u][cc] = __ldcg(l_src(c, hh[u]));
+                    const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
+                    v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
                   }
+                if (staged) {
 #pragma unroll
-                for (int u = 0; u < kMU; ++u) {
-                  const float M = merge_m[hh[u]];
+                  for (int u = 0; u < kMU; ++u)
 #pragma unroll
-                  for (int cc = 0; cc < kMC; ++cc)
-                    w[u][cc] = (c0 + cc < np && M != -INFINITY)
-                                   ? exp2f(w[u][cc] - M) * merge_inv[hh[u]]
-                                   : 0.f;
+                    for (int cc = 0; cc < kMC; ++cc)
+                      w[u][cc] = c0 + cc < np ? merge_lse[(c0 + cc) * G + hh[u]] : 0.f;
+                } else {
+#pragma unroll
+                  for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                    for (int cc = 0; cc < kMC; ++cc) {
+                      const int c = c0 + cc < np ? c0 + cc : np - 1;
+                      w[u][cc] = __ldcg(l_src(c, hh[u]));
+                    }
+#pragma unroll
+                  for (int u = 0; u < kMU; ++u) {
+                    const float M = merge_m[hh[u]];
+#pragma unroll
+                    for (int cc = 0; cc < kMC; ++cc)
+                      w[u][cc] = (c0 + cc < np && M != -INFINITY)
+                                     ? exp2f(w[u][cc] - M) * merge_inv[hh[u]]
+                                     : 0.f;
+                  }
                 }
+#pragma unroll
+                for (int u = 0; u < kMU; ++u)
+#pragma unroll
+                  for (int cc = 0; cc < kMC; ++cc) {
+                    acc[u].x += w[u][cc] * v[u][cc].x;
+                    acc[u].y += w[u][cc] * v[u][cc].y;
+                    acc[u].z += w[u][cc] * v[u][cc].z;
+                    acc[u].w += w[u][cc] * v[u][cc].w;
+                  }
               }
 #pragma unroll
-              for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                for (int cc = 0; cc < kMC; ++cc) {
-                  acc[u].x += w[u][cc] * v[u][cc].x;
-                  acc[u].y += w[u][cc] * v[u][cc].y;
-                  acc[u].z += w[u][cc] * v[u][cc].z;
-                  acc[u].w += w[u][cc] * v[u][cc].w;
-                }
+              for (int u = 0; u < kMU; ++u) {
+                if (j0 + 32 * u >= nslice) continue;
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+                *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + hh[u]) * D +
+                                          dd[u] * 4) = pk;
+              }
             }
-#pragma unroll
-            for (int u = 0; u < kMU; ++u) {
-              if (j0 + 32 * u >= nslice) continue;
-              __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-              __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-              uint2 pk;
-              pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-              pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-              *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + hh[u]) * D +
-                                        dd[u] * 4) = pk;
-            }
-          }
+          };
+          if (np <= 2)
+            wsum(IntC<LEAN ? 4 : 8>{}, IntC<2>{});
+          else
+            wsum(IntC<LEAN ? 2 : 4>{}, IntC<LEAN ? 2 : 4>{});
           if (lane == 0) a.seg_count[seg] = 0;
           __syncwarp();
         }

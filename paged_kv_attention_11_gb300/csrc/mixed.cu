@@ -10,7 +10,8 @@
 // latency chain; run back to back, each leaves the other's resource idle.
 // Here one grid of one CTA per SM splits the step:
 //   * CTAs [0, nd) start with decode (the split-KV body, decode_cta, on
-//     warps 0-5; the dynamic longest-first queue in the workspace);
+//     warps 0-5; the dynamic longest-first queue in the workspace.  8
+//     consumer warps on warps 0-9 measured no faster);
 //   * CTAs [nd, N) run the prefill chunks (the tcgen05 body, varlen_cta,
 //     with the static snake schedule over those N - nd CTAs), then join the
 //     decode queue and take whatever work is left in it.
@@ -36,6 +37,11 @@ struct MixedArgs {
 constexpr int kMixD = 128, kMixNQ = 2, kMixBN = 128, kMixNS = 1, kMixNKS = 3, kMixNVS = 2;
 constexpr int kMixThreads = varlen_threads<kMixNQ>();  // 384
 static_assert(kMixThreads == 384, "three warpgroups");
+#ifndef PKV_MIX_DEC_NW
+#define PKV_MIX_DEC_NW 4
+#endif
+constexpr int kMixDecNW = PKV_MIX_DEC_NW;  // decode consumer warps (+ producer + epilogue)
+static_assert((kMixDecNW + 2) * 32 <= kMixThreads, "decode warps fit the block");
 
 template <int NSTAGE_DEC>
 __global__ void __launch_bounds__(kMixThreads, 1)
@@ -52,8 +58,8 @@ __global__ void __launch_bounds__(kMixThreads, 1)
   if (m.has_var && (int)blockIdx.x >= nd)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
-  if (m.has_dec && warp < 6)
-    decode_cta<kMixD, 4, NSTAGE_DEC, true, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
+  if (m.has_dec && warp < kMixDecNW + 2)
+    decode_cta<kMixD, kMixDecNW, NSTAGE_DEC, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
 }
 
 // CTAs that start with decode when the caller leaves the split open: the
@@ -86,8 +92,8 @@ static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const v
                                   int num_sms) {
   auto kern = mixed_step_kernel<NSTAGE_DEC>;
   CUtensorMap tmKd, tmVd;
-  if (!encode_pool_map_halves(&tmKd, k_cache, m.dec.P, m.dec.num_pages, m.dec.H_kv) ||
-      !encode_pool_map_halves(&tmVd, v_cache, m.dec.P, m.dec.num_pages, m.dec.H_kv))
+  if (!encode_pool_map_groups(&tmKd, k_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile) ||
+      !encode_pool_map_groups(&tmVd, v_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile))
     return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
@@ -177,8 +183,8 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   // ---- shared memory: the larger of the two plans
   using VS = VarlenSmem<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS>;
   const size_t var_smem = m.has_var ? VS::bytes(v.batch, v.pairs_max) : 0;
-  const size_t dec24 = DecodePlan<kMixD, 4, 24>(a.G, a.batch).total;
-  const size_t dec16 = DecodePlan<kMixD, 4, 16>(a.G, a.batch).total;
+  const size_t dec24 = DecodePlan<kMixD, kMixDecNW, 24>(a.G, a.batch).total;
+  const size_t dec16 = DecodePlan<kMixD, kMixDecNW, 16>(a.G, a.batch).total;
   constexpr size_t kMax = 227 * 1024;
   if (var_smem > kMax) return cudaErrorNotSupported;
   if (!m.has_dec || dec24 <= kMax) {

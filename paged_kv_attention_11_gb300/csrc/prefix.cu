@@ -94,7 +94,7 @@ __device__ __forceinline__ PfxItem prefix_item(const PrefixArgs& a, int i, bool 
   return it;
 }
 
-template <int D, int NTQ, int NSTAGE, bool ONEBOX>
+template <int D, int NTQ, int NSTAGE>
 __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
     prefix_pass_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
@@ -103,8 +103,8 @@ __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
   constexpr int KS = D / 16;
   constexpr int R = P_::R;
   constexpr int CS = P_::kCombStride;
-  constexpr int kBoxBytes = kTile * 128;
   constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;
+  static_assert(kIssueLanes < 32, "a run of free stages ends inside the warp");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -143,14 +143,25 @@ __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
         int page = -1;
         if (k0 + lane < item.n) page = __ldg(bt + ((k0 + lane) * kTile) / a.P);
         const int cnt = min(32, item.n - k0);
-        for (int j0 = 0; j0 < cnt; j0 += kIssueLanes) {
-          const int jj = j0 + lane;
+        // in order, each tile as soon as its stage is free (as in the decode
+        // producer: a run of free stages per warp instruction)
+        for (int j = 0; j < cnt;) {
+          const int jj = j + lane;
           const int pg = __shfl_sync(0xffffffffu, page, jj & 31);
-          if (lane < kIssueLanes && jj < cnt) {
-            const int t = it + jj;
-            const int s = t % NSTAGE;
-            const int r = t / NSTAGE;
-            if (r > 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
+          const int t = it + jj;
+          const int s = t % NSTAGE;
+          const int r = t / NSTAGE;
+          const bool mine = lane < kIssueLanes && jj < cnt;
+          const bool free_ = mine && (r == 0 || mbar_test_wait(empty + s, (r - 1) & 1));
+          const uint32_t fm = __ballot_sync(0xffffffffu, free_);
+          int run = __ffs(~fm) - 1;
+          if (run == 0) {
+            if (lane == 0) mbar_wait(empty + s, (r - 1) & 1, a.err, dead);
+            __syncwarp();
+            run = 1;
+            if (__shfl_sync(0xffffffffu, (int)dead, 0)) dead = true;
+          }
+          if (lane < run) {
             const bool ok = pg >= 0 && (int64_t)pg < a.num_pages;
             stage_ok[s] = ok ? 1 : 0;
             if (ok) {
@@ -158,23 +169,15 @@ __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
               mbar_arrive_expect_tx(full + s, P_::kStageBytes);
               const int row = ((k0 + jj) * kTile) % a.P;
               const int z = pg * a.H_kv + item.g;
-              if (ONEBOX) {
-                tma_load_4d(st, &tmK, full + s, 0, 0, row, z);
-                tma_load_4d(st + P_::kTileBytes, &tmV, full + s, 0, 0, row, z);
-              } else {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                  tma_load_3d(st + c * kBoxBytes, &tmK, full + s, c * 64, row, z);
-                  tma_load_3d(st + P_::kTileBytes + c * kBoxBytes, &tmV, full + s, c * 64, row,
-                              z);
-                }
-              }
+              tma_load_5d(st, &tmK, full + s, 0, 0, 0, row / 8, z);
+              tma_load_5d(st + P_::kTileBytes, &tmV, full + s, 0, 0, 0, row / 8, z);
             } else {
               raise_err(a.err, PKV_DEVERR_PAGE);
               mbar_arrive(full + s);
             }
           }
           __syncwarp();
+          j += run;
         }
         it += cnt;
       }
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(tile_addr<D, ONEBOX>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+            ldsm_x4(tile_addr<D>(stK, key, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
             for (int t = 0; t < NTQ; ++t)
               mma_bf16_16816(sc[t], a0, a1, a2, a3, qb[ks][t][0], qb[ks][t][1]);
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__((kPfxConsumers + 1) * 32, 1)
 #pragma unroll
           for (int md = 0; md < KS; ++md) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(tile_addr<D, ONEBOX>(stV, key, 2 * md + (jq & 1)), a0, a1, a2, a3);
+            ldsm_x4_t(tile_addr<D>(stV, key, 2 * md + (jq & 1)), a0, a1, a2, a3);
 #pragma unroll
             for (int t = 0; t < NTQ; ++t)
               mma_bf16_16816(o[md][t], a0, a1, a2, a3, pb[t][0], pb[t][1]);
@@ -378,15 +381,12 @@ template <int D, int NTQ>
 static cudaError_t launch_prefix_t(const PrefixArgs& a, const void* k_cache, const void* v_cache,
                                    cudaStream_t stream, int num_sms) {
   constexpr int NSTAGE = PrefixCfg<D>::NSTAGE;
-  constexpr bool kOneBox = D == 128;
   using P_ = PrefixPlan<D, NTQ, NSTAGE>;
-  auto kern = prefix_pass_kernel<D, NTQ, NSTAGE, kOneBox>;
+  auto kern = prefix_pass_kernel<D, NTQ, NSTAGE>;
   CUtensorMap tmK, tmV;
   const bool enc_ok =
-      kOneBox ? (encode_pool_map_halves(&tmK, k_cache, a.P, a.num_pages, a.H_kv) &&
-                 encode_pool_map_halves(&tmV, v_cache, a.P, a.num_pages, a.H_kv))
-              : (encode_pool_map(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv) &&
-                 encode_pool_map(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv));
+      encode_pool_map_groups(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv, kTile) &&
+      encode_pool_map_groups(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv, kTile);
   if (!enc_ok) return cudaErrorInvalidValue;
   static_assert(P_::kTotal <= 227 * 1024, "prefix pass shared memory");
   static bool configured[64] = {false};

@@ -11,18 +11,16 @@ constexpr int kTile = 16;  // keys per pipeline stage
 constexpr int kGP = 8;     // query rows per mma N tile (the GQA group, padded)
 
 // Shared-memory address of 16-byte chunk c (0..D/8-1) of key row `key` in a
-// staged tile.  Default staging: D/64 boxes of [16 rows x 128 B] (one box
-// per 64-column slice).  ONEBOX (head_dim 128): one box of 32 rows x 128 B,
-// row = 2*key + c/8.  Both are 128-byte swizzled: 16-byte unit u of a row r
-// sits at unit u ^ (r % 8).
-template <int D, bool ONEBOX>
+// staged K or V tile.  A tile is one TMA box of the pool's 5-D view
+// {64 columns, 8 rows, D/64 column chunks, P/8 row groups, pages*H_kv}: it
+// lands as [row group (2)][column chunk (D/64)][8 rows][128 bytes], every
+// [8 rows][128 bytes] block one 1024-byte swizzle atom (16-byte unit u of
+// row r at unit u ^ r).  The 8 rows an ldmatrix reads (8 consecutive keys,
+// one column chunk) sit in 8 distinct bank groups.
+template <int D>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int key, int c) {
-  if (ONEBOX) {
-    const int rp = 2 * key + (c >> 3);
-    return base + rp * 128 + (((c & 7) ^ (rp & 7)) << 4);
-  } else {
-    return base + (c >> 3) * (kTile * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4);
-  }
+  return base + (key >> 3) * (D / 64) * 1024 + (c >> 3) * 1024 + (key & 7) * 128 +
+         (((c & 7) ^ (key & 7)) << 4);
 }
 
 }  // namespace pkv

@@ -29,23 +29,7 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// K or V pool [num_pages, H_kv, P, D] bf16 viewed as {D, P, num_pages*H_kv};
-// box = 64 columns x 16 rows, 128-byte swizzle.
-inline bool encode_pool_map(CUtensorMap* m, const void* base, int D, int P, int64_t num_pages,
-                     int H_kv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P * D * 2};
-  cuuint32_t box[3] = {64, 16, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// K or V pool for the varlen kernel, viewed as {64 columns, 8 rows, D/64
+// K or V pool for the varlen and decode kernels, viewed as {64 columns, 8 rows, D/64
 // column chunks, P/8 row groups, num_pages*H_kv}: one box {64, 8, D/64,
 // rows/8, 1} is `rows` keys of one page and head, and lands in shared memory
 // as [row group][column chunk][8 rows][128 bytes], 128-byte swizzled: every
@@ -79,24 +63,6 @@ inline bool encode_q_map(CUtensorMap* m, const void* base, int D, int G, int H_k
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2,
                            (cuuint64_t)H_kv * G * D * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G)};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// K or V pool with head_dim 128 viewed as {64, 2, P, num_pages*H_kv}: one
-// box {64, 2, 16, 1} is a whole contiguous 16-key tile (4 KB); in shared
-// memory it lands as 32 rows of 128 bytes (row = 2*key + half), 128-byte
-// swizzled.
-inline bool encode_pool_map_halves(CUtensorMap* m, const void* base, int P, int64_t num_pages,
-                                   int H_kv) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {64, 2, (cuuint64_t)P, (cuuint64_t)(num_pages * H_kv)};
-  cuuint64_t strides[3] = {128, 256, (cuuint64_t)P * 256};
-  cuuint32_t box[4] = {64, 2, 16, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
