@@ -21,6 +21,17 @@ __device__ __forceinline__ void raise_err(int32_t* err, int bits) {
   if (err != nullptr) atomicOr(err, bits);
 }
 
+// Global int32 flags another CTA writes or reads while this one runs: the
+// access goes to L2 every time (ordering comes from the fences around it).
+__device__ __forceinline__ int ld_volatile_i32(const int32_t* p) {
+  int v;
+  asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_i32(int32_t* p, int v) {
+  asm volatile("st.volatile.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

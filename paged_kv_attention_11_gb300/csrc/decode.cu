@@ -12,8 +12,7 @@ __global__ void __launch_bounds__((NW + 2) * 32, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  // 8 consumer warps leave 168 registers a thread: the merge keeps fewer loads in flight
-  decode_cta<D, NW, NSTAGE, false, (NW >= 8)>(a, tmK, tmV, smem, blockIdx.x);
+  decode_cta<D, NW, NSTAGE, false>(a, tmK, tmV, smem, blockIdx.x);
 }
 
 // --------------------------------------------------------------- host side
@@ -55,13 +54,13 @@ static int64_t decode_max_pieces(int32_t batch, int32_t H_kv, int32_t D, int num
   return (int64_t)batch * H_kv + 2 * (int64_t)num_sms * decode_ctas_per_sm(D);
 }
 
-// Workspace: [seg_count: batch*H_kv int32][queue: 2 int32] ...
-//            [part_lse: pieces*G f32][part_o: pieces*G*D f32]
+// Workspace: [seg_count: batch*H_kv int32][merge_jobs: batch*H_kv int32]
+//            [queue: 8 int32] ... [part_lse: pieces*G f32][part_o: pieces*G*D f32]
 // (partials aligned to the end of the caller's buffer)
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
   const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
   const int64_t G = H_q / H_kv;
-  return align256(((size_t)batch * H_kv + 2) * 4) + align256((size_t)pieces * G * 4) +
+  return align256(((size_t)batch * H_kv * 2 + 8) * 4) + align256((size_t)pieces * G * 4) +
          align256((size_t)pieces * G * D * 4);
 }
 
@@ -73,7 +72,8 @@ void decode_workspace_split(DecodeArgs& a, void* workspace, size_t workspace_byt
   const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.seg_count = reinterpret_cast<int32_t*>(ws);
-  a.queue = a.seg_count + (int64_t)batch * H_kv;
+  a.merge_jobs = a.seg_count + (int64_t)batch * H_kv;
+  a.queue = a.merge_jobs + (int64_t)batch * H_kv;
   uint8_t* end = ws + (workspace_bytes & ~size_t(255));
   end -= align256((size_t)pieces * a.G * D * 4);
   a.part_o = reinterpret_cast<float*>(end);

@@ -44,7 +44,7 @@
 namespace pkv {
 
 constexpr int kNRec = 4;   // piece records in flight
-constexpr int kMergeLse = 1024;  // (piece, head) log-sum-exps staged in smem for a merge
+constexpr int kEpiScratch = 10 * kGP;  // epilogue weights: [NW][G] per warp, then the join's two
 // Shortest chunk a segment is cut into (tiles).  Small batches (a few long
 // windowed segments) then still spread over every SM instead of one segment
 // per CTA; large batches cut at half a CTA's share, far above this floor.
@@ -72,8 +72,10 @@ struct DecodeArgs {
   int64_t num_pages;
   int32_t window;
   float scale_log2;
-  int32_t* seg_count;  // [batch * H_kv] arrival counters, zero between calls
-  int32_t* queue;      // [2]: next item, CTAs done; zero between calls
+  int32_t* seg_count;   // [batch * H_kv] arrival counters, zero between calls
+  int32_t* merge_jobs;  // [batch * H_kv] completed chunked segments (+1), zero between calls
+  int32_t* queue;       // [8]: next item, CTAs done with items; next merge job, jobs
+                        // posted, CTAs done merging; zero between calls
   float* part_lse;     // [(S + N) * G]
   float* part_o;       // [(S + N) * G * D]
   // shared-prefix (cascade) decode: null prefix_lens = plain decode.  A
@@ -170,7 +172,7 @@ struct DecodePlan {
     ml = o;    o += kNComb * NW * G * 2 * 4;
     bars = o;  o += (2 * NSTAGE + 2 * kNRec + 2 * kNComb) * 8;
     ok = o;    o += NSTAGE * 4;
-    misc = o;  o += 2 * kGP * 4 + 16 + kMergeLse * 4;
+    misc = o;  o += 2 * kGP * 4 + 16 + kEpiScratch * 4;
     scan = o;  o += (NW + 2) * 4 + 8 + 16 + (NW + 2) * 4;
     // natural prefix, sorted prefix, order; lengths up to kLenCacheSeq sequences
     cum = o;   o += (batch + 1) * 4 * (batch <= kLenCacheSeq ? 4 : 3);
@@ -183,10 +185,8 @@ struct DecodePlan {
 // hosts this body on part of its warps), so the body synchronises on a
 // named barrier of its own threads instead of the whole block.  `cta` is
 // this CTA's index among the a.cta_count CTAs that run the body; smem is the
-// 1024-aligned base of the dynamic shared memory.  LEAN: the merge keeps
-// fewer loads in flight, so that the body fits the register budget of a
-// larger block.
-template <int D, int NW, int NSTAGE, bool SUBSET, bool LEAN = false>
+// 1024-aligned base of the dynamic shared memory.
+template <int D, int NW, int NSTAGE, bool SUBSET>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
@@ -220,8 +220,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   int* stage_ok = reinterpret_cast<int*>(smem + plan.ok);
   float* merge_m = reinterpret_cast<float*>(smem + plan.misc);
   float* merge_inv = merge_m + kGP;
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(merge_inv + kGP);
-  float* merge_lse = merge_inv + kGP + 4;  // [kMergeLse]
+  float* epi_w = merge_inv + kGP + 4;  // [kEpiScratch]
   int* scan_tmp = reinterpret_cast<int*>(smem + plan.scan);
   int* s_misc = scan_tmp + NW + 4;                              // [4]
   int* s_nat = reinterpret_cast<int*>(smem + plan.cum);         // [B+1] items before b
@@ -315,17 +314,25 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       const int64_t W = tot * a.H_kv;
       const int64_t half_share = (W + 2 * (int64_t)a.share_ctas - 1) / (2 * (int64_t)a.share_ctas);
       s_misc[0] = (int)(half_share > kMinChunkTiles ? half_share : kMinChunkTiles);  // S_max
+      s_misc[1] = 0;  // sequences cut into more than one chunk
     }
     block_sync();
   }
   const int smax = s_misc[0];
   auto nch_of = [&](int t) { return (t + smax - 1) / smax; };
   // items per sequence (natural order) and chunk length (queue order key)
-  for (int b = tid; b < B; b += NT) {
-    const int t = s_nat[b];
-    const int nch = nch_of(t);
-    s_nat[b] = nch * a.H_kv;
-    s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
+  {
+    int chunked = 0;
+    for (int b = tid; b < B; b += NT) {
+      const int t = s_nat[b];
+      const int nch = nch_of(t);
+      s_nat[b] = nch * a.H_kv;
+      s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
+      chunked += nch > 1 ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) chunked += __shfl_xor_sync(0xffffffffu, chunked, o);
+    if (lane == 0 && chunked) atomicAdd(s_misc + 1, chunked);
   }
   block_sync();
   // queue order: sequences by chunk length, longest first, ties by index
@@ -504,11 +511,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     int k = 0;   // item counter
     while (true) {
       // ---- the item record and its query rows, to the consumers and the
-      //      epilogue.  It goes out after the item's first window of tiles
-      //      is issued, or before the first wait on a busy stage, whichever
-      //      comes first (the item's own consumers may be the ones to free
-      //      that stage), so the first copies of a CTA leave without waiting
-      //      for the query rows. ----
+      //      epilogue.  It goes out right after the item's first issue
+      //      instruction (up to 16 tiles), and always before a wait on a
+      //      busy stage (the item's own consumers may be the ones to free
+      //      it), so a CTA's first copies leave without waiting for the
+      //      query rows. ----
       bool published = false;
       auto publish = [&]() {
         const int slot = k % kNRec;
@@ -601,8 +608,9 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           }
           __syncwarp();
           j += run;
+          // the consumers start on the first copies while the rest go out
+          if (!published) publish();
         }
-        if (!published) publish();
         it += cnt;
         page = page_ahead;
       }
@@ -811,13 +819,13 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       const bool join_pfx = rec.nch == 1 && rec.pfx == 1;
       const bool whole = rec.nch == 1;
       const int64_t pre_row0 = (int64_t)b * a.H_q + g * G;
-      float* w_item = merge_lse + NW * kGP;  // [kGP] weights of the joined outputs
+      float* w_item = epi_w + NW * kGP;  // [kGP] weights of the joined outputs
       float* w_pfx = w_item + kGP;           // [kGP]
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
       const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
       // per head: weight of each consumer warp's state, 1/l, log2-sum-exp
-      float* wsc = merge_lse;  // [NW][G] scratch (the merge below reloads it)
+      float* wsc = epi_w;  // [NW][G] scratch
       if (lane < G) {
         const int h = lane;
         float M = -INFINITY;
@@ -900,153 +908,175 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       __syncwarp();
       mbar_arrive(comb_empty + cb);  // the consumers may refill this buffer
       if (!whole) {
-        // arrival counter: the last CTA to deliver a chunk of this segment
-        // merges all of them (nobody waits; the counter is reset afterwards)
+        // arrival counter: the CTA that delivers the last chunk of this
+        // segment posts it to the merge queue (nobody waits here; the
+        // counter is reset for the next call)
         const int64_t seg = (int64_t)b * a.H_kv + g;
         __threadfence();
         __syncwarp();
         if (lane == 0) {
           const int old = atomicAdd(a.seg_count + seg, 1);
-          *merge_flag = (old == rec.nch - 1) ? 1 : 0;
+          if (old == rec.nch - 1) {
+            a.seg_count[seg] = 0;
+            __threadfence();  // every chunk's partial before the post
+            const int j = atomicAdd(a.queue + 3, 1);
+            st_volatile_i32(a.merge_jobs + j, (int)seg + 1);
+          }
         }
         __syncwarp();
-        if (*merge_flag) {
-          __threadfence();
-          // the segment's chunks, plus the prefix partial as chunk nch
-          const int np = rec.nch + rec.pfx;
-          const int64_t pre_row = (int64_t)b * a.H_q + g * G;
-          auto l_src = [&](int c, int h) -> const float* {
-            return c < rec.nch ? a.part_lse + ((int64_t)rec.slot0 + c) * G + h
-                               : a.pre_lse + pre_row + h;
-          };
-          auto o_src = [&](int c, int h) -> const float* {
-            return c < rec.nch ? a.part_o + (((int64_t)rec.slot0 + c) * G + h) * D
-                               : a.pre_o + (pre_row + h) * D;
-          };
-          // (1) the (chunk, head) log2-sum-exps, staged in shared memory in
-          //     one round of loads when they fit (a segment cut into more
-          //     than kMergeLse / G chunks reads them from L2 instead)
-          const int nl = np * G;
-          const bool staged = nl <= kMergeLse;
-          if (staged)
-            for (int i = lane; i < nl; i += 32) merge_lse[i] = __ldcg(l_src(i / G, i % G));
-          __syncwarp();
-          if (lane < G) {  // per head: max and 1 / sum of the weights
-            const int h = lane;
-            float M = -INFINITY, sum = 0.f;
-            if (staged) {
-              for (int c = 0; c < np; ++c) M = fmaxf(M, merge_lse[c * G + h]);
-              if (M != -INFINITY)
-                for (int c = 0; c < np; ++c) sum += exp2f(merge_lse[c * G + h] - M);
-            } else {
-              for (int c = 0; c < np; ++c) M = fmaxf(M, __ldcg(l_src(c, h)));
-              if (M != -INFINITY)
-                for (int c = 0; c < np; ++c) sum += exp2f(__ldcg(l_src(c, h)) - M);
-            }
-            merge_m[h] = M;
-            merge_inv[h] = sum > 0.f ? 1.f / sum : 0.f;
-          }
-          __syncwarp();
-          // (2) staged: the normalised weight of every (chunk, head)
-          if (staged) {
-            for (int i = lane; i < nl; i += 32) {
-              const int h = i % G;
-              const float M = merge_m[h];
-              merge_lse[i] = M == -INFINITY ? 0.f : exp2f(merge_lse[i] - M) * merge_inv[h];
+      }
+    }
+  }
+
+  // ============================ merge phase ================================
+  // Segments cut into chunks are merged by the CTAs that have run out of
+  // items, with all their warps: a CTA takes the next posted segment (in
+  // the order the segments completed), waits for its post if it is still
+  // being computed elsewhere (every CTA of the grid is resident, so the
+  // post comes), and combines the chunks' partials with their log-sum-exp
+  // weights.  The stage ring is free scratch now: the producer has drained
+  // every copy it issued.
+  // segments with more than one chunk: each is posted exactly once (none:
+  // the CTA ends here, touching no merge counter)
+  const int n_jobs = s_misc[1] * a.H_kv;
+  if (n_jobs > 0) {
+    block_sync();
+    volatile int* s_job = s_misc + 2;  // [2]: queue index, segment
+    float* wts = reinterpret_cast<float*>(smem);  // [np * G] weights, then [2][G]
+    bool mdead = false;
+    while (true) {
+      if (tid == 0) s_job[0] = atomicAdd(a.queue + 2, 1);
+      block_sync();
+      const int idx = s_job[0];
+      if (idx >= n_jobs) break;
+      if (tid == 0) {
+        int v = ld_volatile_i32(a.merge_jobs + idx);
+        if (v == 0 && !mdead) {
+          const unsigned long long t0 = globaltimer();
+          while ((v = ld_volatile_i32(a.merge_jobs + idx)) == 0) {
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+              raise_err(a.err, PKV_DEVERR_TIMEOUT);
+              mdead = true;
+              break;
             }
           }
-          __syncwarp();
-          // (3) weighted sum of the chunks' outputs, 4 dims (a slice) per
-          //     lane and load.  Each lane keeps kMU slices x kMC chunks of
-          //     loads in flight; the weights come from shared memory (or,
-          //     unstaged, from loads issued in the same batch), so a merge
-          //     costs a few L2 round trips.  Two chunks (the common split)
-          //     take twice the slices per batch instead of idle chunk slots.
-          //     Every output sums its chunks in chunk order.
-          const int nslice = G * (D / 4);
-          auto wsum = [&](auto mu_c, auto mc_c) {
-          constexpr int kMU = decltype(mu_c)::value, kMC = decltype(mc_c)::value;
-            for (int j0 = lane; j0 < nslice; j0 += 32 * kMU) {
-              float4 acc[kMU];
-              int hh[kMU], dd[kMU];
-#pragma unroll
-              for (int u = 0; u < kMU; ++u) {
-                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                const int j = j0 + 32 * u < nslice ? j0 + 32 * u : 0;
-                hh[u] = j / (D / 4);
-                dd[u] = j - hh[u] * (D / 4);
-              }
-              for (int c0 = 0; c0 < np; c0 += kMC) {
-                float4 v[kMU][kMC];
-                float w[kMU][kMC];
-#pragma unroll
-                for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                  for (int cc = 0; cc < kMC; ++cc) {
-                    const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
-                    v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
-                  }
-                if (staged) {
-#pragma unroll
-                  for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                    for (int cc = 0; cc < kMC; ++cc)
-                      w[u][cc] = c0 + cc < np ? merge_lse[(c0 + cc) * G + hh[u]] : 0.f;
-                } else {
-#pragma unroll
-                  for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                    for (int cc = 0; cc < kMC; ++cc) {
-                      const int c = c0 + cc < np ? c0 + cc : np - 1;
-                      w[u][cc] = __ldcg(l_src(c, hh[u]));
-                    }
-#pragma unroll
-                  for (int u = 0; u < kMU; ++u) {
-                    const float M = merge_m[hh[u]];
-#pragma unroll
-                    for (int cc = 0; cc < kMC; ++cc)
-                      w[u][cc] = (c0 + cc < np && M != -INFINITY)
-                                     ? exp2f(w[u][cc] - M) * merge_inv[hh[u]]
-                                     : 0.f;
-                  }
-                }
-#pragma unroll
-                for (int u = 0; u < kMU; ++u)
-#pragma unroll
-                  for (int cc = 0; cc < kMC; ++cc) {
-                    acc[u].x += w[u][cc] * v[u][cc].x;
-                    acc[u].y += w[u][cc] * v[u][cc].y;
-                    acc[u].z += w[u][cc] * v[u][cc].z;
-                    acc[u].w += w[u][cc] * v[u][cc].w;
-                  }
-              }
-#pragma unroll
-              for (int u = 0; u < kMU; ++u) {
-                if (j0 + 32 * u >= nslice) continue;
-                __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-                __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-                uint2 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-                pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-                *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + hh[u]) * D +
-                                          dd[u] * 4) = pk;
-              }
-            }
-          };
-          if (np <= 2)
-            wsum(IntC<LEAN ? 4 : 8>{}, IntC<2>{});
-          else
-            wsum(IntC<LEAN ? 2 : 4>{}, IntC<LEAN ? 2 : 4>{});
-          if (lane == 0) a.seg_count[seg] = 0;
-          __syncwarp();
         }
+        st_volatile_i32(a.merge_jobs + idx, 0);
+        s_job[1] = v - 1;
+        __threadfence();  // the chunks' partials after the post
+      }
+      block_sync();
+      const int seg = s_job[1];
+      if (seg < 0) break;
+      const int b = seg / a.H_kv, g = seg - b * a.H_kv;
+      const int nch = (s_nat[b + 1] - s_nat[b]) / a.H_kv;
+      const int64_t slot0 = (int64_t)s_nat[b] + (int64_t)g * nch;
+      int L, klo, t_lo, t_hi, pfx;
+      if (s_len) {
+        L = s_len[b];
+        extent_of_len(a, b, L, klo, t_lo, t_hi, &pfx);
+      } else {
+        seq_extent(a, b, L, klo, t_lo, t_hi, false, &pfx);
+      }
+      // the segment's chunks, plus the prefix partial as chunk nch (cascade)
+      const int np = nch + pfx;
+      const int64_t row0 = (int64_t)b * a.H_q + g * G;
+      auto l_src = [&](int c, int h) -> const float* {
+        return c < nch ? a.part_lse + (slot0 + c) * G + h : a.pre_lse + row0 + h;
+      };
+      auto o_src = [&](int c, int h) -> const float* {
+        return c < nch ? a.part_o + ((slot0 + c) * G + h) * D : a.pre_o + (row0 + h) * D;
+      };
+      const int nl = np * G;
+      float* wm = wts + nl;  // [G] max, [G] 1 / sum
+      for (int i = tid; i < nl; i += NT) wts[i] = __ldcg(l_src(i / G, i % G));
+      block_sync();
+      if (tid < G) {  // per head: max and 1 / sum of the weights
+        const int h = tid;
+        float M = -INFINITY, sum = 0.f;
+        for (int c = 0; c < np; ++c) M = fmaxf(M, wts[c * G + h]);
+        if (M != -INFINITY)
+          for (int c = 0; c < np; ++c) sum += exp2f(wts[c * G + h] - M);
+        wm[h] = M;
+        wm[G + h] = sum > 0.f ? 1.f / sum : 0.f;
+      }
+      block_sync();
+      for (int i = tid; i < nl; i += NT) {
+        const int h = i % G;
+        const float M = wm[h];
+        wts[i] = M == -INFINITY ? 0.f : exp2f(wts[i] - M) * wm[G + h];
+      }
+      block_sync();
+      // weighted sum of the chunks' outputs, 4 dims (a slice) per load; each
+      // thread keeps kS slices x kMC chunks of loads in flight (two chunks,
+      // the common split: twice the slices); every output sums its chunks
+      // in chunk order
+      auto wsum = [&](auto s_c, auto mc_c) {
+        constexpr int kS = decltype(s_c)::value, kMC = decltype(mc_c)::value;
+        constexpr int Q4 = D / 4;
+        for (int j0 = tid; j0 < G * Q4; j0 += NT * kS) {
+          float4 acc[kS];
+          int hh[kS], dd[kS];
+#pragma unroll
+          for (int u = 0; u < kS; ++u) {
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int j = j0 + NT * u < G * Q4 ? j0 + NT * u : 0;
+            hh[u] = j / Q4;
+            dd[u] = j - hh[u] * Q4;
+          }
+          for (int c0 = 0; c0 < np; c0 += kMC) {
+            float4 v[kS][kMC];
+#pragma unroll
+            for (int u = 0; u < kS; ++u)
+#pragma unroll
+              for (int cc = 0; cc < kMC; ++cc) {
+                const int c = c0 + cc < np ? c0 + cc : np - 1;  // clamped: weight 0 below
+                v[u][cc] = __ldcg(reinterpret_cast<const float4*>(o_src(c, hh[u])) + dd[u]);
+              }
+#pragma unroll
+            for (int u = 0; u < kS; ++u)
+#pragma unroll
+              for (int cc = 0; cc < kMC; ++cc) {
+                const float w = c0 + cc < np ? wts[(c0 + cc) * G + hh[u]] : 0.f;
+                acc[u].x += w * v[u][cc].x;
+                acc[u].y += w * v[u][cc].y;
+                acc[u].z += w * v[u][cc].z;
+                acc[u].w += w * v[u][cc].w;
+              }
+          }
+#pragma unroll
+          for (int u = 0; u < kS; ++u) {
+            if (j0 + NT * u >= G * Q4) continue;
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(a.out + (row0 + hh[u]) * D + dd[u] * 4) = pk;
+          }
+        }
+      };
+      if (np <= 2)
+        wsum(IntC<8>{}, IntC<2>{});
+      else
+        wsum(IntC<4>{}, IntC<4>{});
+      block_sync();  // the next job reuses the weights and the job slots
+    }
+    // the last CTA out of the merge phase resets its counters
+    if (tid == 0) {
+      __threadfence();
+      const int done = atomicAdd(a.queue + 4, 1);
+      if (done == a.cta_count - 1) {
+        a.queue[2] = 0;
+        a.queue[3] = 0;
+        a.queue[4] = 0;
       }
     }
   }
 }
 
-// Places the arrival counters, the queue and the partial results of a
-// decode call in its workspace (decode.cu).
+// Places the arrival counters, the merge queue, the item queue and the
+// partial results of a decode call in its workspace (decode.cu).
 void decode_workspace_split(DecodeArgs& a, void* workspace, size_t workspace_bytes,
                             int32_t batch, int32_t H_kv, int32_t D, int num_sms);
 

@@ -18,7 +18,7 @@
 // Every CTA ends in the decode body, so the decode queue's last-CTA reset
 // and the zero rows of empty sequences work as in paged_attn_decode.  No
 // warp moves registers (setmaxnreg): both bodies run in the launch's 168 per
-// thread, the decode body with its lean merge.
+// thread.
 #include "decode_body.cuh"
 #include "tmap.h"
 #include "varlen_body.cuh"
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kMixThreads, 1)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
   if (m.has_dec && warp < kMixDecNW + 2)
-    decode_cta<kMixD, kMixDecNW, NSTAGE_DEC, true, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
+    decode_cta<kMixD, kMixDecNW, NSTAGE_DEC, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
 }
 
 // CTAs that start with decode when the caller leaves the split open: the
