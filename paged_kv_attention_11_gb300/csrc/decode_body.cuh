@@ -48,7 +48,19 @@ constexpr int kEpiScratch = 10 * kGP;  // epilogue weights: [NW][G] per warp, th
 // Shortest chunk a segment is cut into (tiles).  Small batches (a few long
 // windowed segments) then still spread over every SM instead of one segment
 // per CTA; large batches cut at half a CTA's share, far above this floor.
+#ifndef PKV_DEC_MIN_CHUNK_KB
+#define PKV_DEC_MIN_CHUNK_KB 0
+#endif
 constexpr int kMinChunkTiles = 16;
+// and at least this many bytes of K+V per chunk (0: no byte floor)
+constexpr int kMinChunkBytes = PKV_DEC_MIN_CHUNK_KB * 1024;
+// What a merge costs, as bytes one CTA would stream in the same time (~8 us
+// at ~60 GB/s per SM, measured on the sliding-window step; the merge code
+// runs once per CTA, so its instructions come cold from memory).
+#ifndef PKV_DEC_MERGE_COST_KB
+#define PKV_DEC_MERGE_COST_KB 480
+#endif
+constexpr int kMergeCostBytes = PKV_DEC_MERGE_COST_KB * 1024;
 constexpr int kMaxSortSeq = 512;  // longest-first queue order up to this batch
 // Batches up to this size keep each sequence's clamped length in shared
 // memory, so the producer maps a queue index to its item without a global
@@ -288,9 +300,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   // ---- work items (every CTA computes the same list, in smem) ----
   // tiles of sequence b: t_b; units W = sum t_b * H_kv; a segment longer
   // than S_max = max(kMinChunkTiles, W / (2N)) tiles is cut into nch_b
-  // equal chunks.
+  // equal chunks -- unless the longest segment is within the cost of a
+  // merge of S_max (kMergeCostBytes of streaming), where cutting would not
+  // end the call sooner: then nothing is cut.
   {
-    int local = 0;
+    int local = 0, lmax = 0;
     for (int b = tid; b < B; b += NT) {
       int L, lo, tl, th;
       seq_extent(a, b, L, lo, tl, th, cta == 0);
@@ -298,6 +312,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       s_nat[b] = t;  // tiles, for now
       if (s_len) s_len[b] = L;
       local += t;
+      lmax = t > lmax ? t : lmax;
       // zero-length sequences have no work item: their zero rows are written here
       if (t == 0 && b % a.cta_count == cta) {
         uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.H_q * D);
@@ -305,15 +320,29 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-    if (lane == 0) scan_tmp[warp] = local;
+    for (int o = 16; o > 0; o >>= 1) {
+      local += __shfl_xor_sync(0xffffffffu, local, o);
+      lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    }
+    if (lane == 0) {
+      scan_tmp[warp] = local;
+      s_misc[4 + warp] = lmax;  // free until the prefix scan below
+    }
     block_sync();
     if (tid == 0) {
       int64_t tot = 0;
-      for (int w = 0; w < NT / 32; ++w) tot += scan_tmp[w];
+      int tmax = 0;
+      for (int w = 0; w < NT / 32; ++w) {
+        tot += scan_tmp[w];
+        tmax = max(tmax, s_misc[4 + w]);
+      }
       const int64_t W = tot * a.H_kv;
       const int64_t half_share = (W + 2 * (int64_t)a.share_ctas - 1) / (2 * (int64_t)a.share_ctas);
-      s_misc[0] = (int)(half_share > kMinChunkTiles ? half_share : kMinChunkTiles);  // S_max
+      int64_t floor_tiles = kMinChunkTiles;
+      if ((int64_t)kMinChunkBytes / (64 * D) > floor_tiles) floor_tiles = kMinChunkBytes / (64 * D);
+      int64_t cut = half_share > floor_tiles ? half_share : floor_tiles;
+      if ((int64_t)tmax <= cut + kMergeCostBytes / (64 * D)) cut = tmax > 0 ? tmax : 1;
+      s_misc[0] = (int)cut;  // S_max
       s_misc[1] = 0;  // sequences cut into more than one chunk
     }
     block_sync();
@@ -954,6 +983,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         if (v == 0 && !mdead) {
           const unsigned long long t0 = globaltimer();
           while ((v = ld_volatile_i32(a.merge_jobs + idx)) == 0) {
+            __nanosleep(128);  // the posts are far apart; keep the L2 line quiet
             if (globaltimer() - t0 > kWaitTimeoutNs) {
               raise_err(a.err, PKV_DEVERR_TIMEOUT);
               mdead = true;

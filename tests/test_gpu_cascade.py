@@ -112,6 +112,22 @@ def test_cascade_shapes_and_edges(pkv, D, H, gs):
     assert_close_attn(got, want, f"cascade D={D} H={H} group={gs}")
 
 
+@pytest.mark.parametrize("D", [128, 256])
+def test_cascade_long_suffix_merges_with_prefix(pkv, D):
+    """Suffixes long enough that the decode cuts them into chunks: the merge
+    phase then weighs the prefix partial with the suffix chunks."""
+    rng = np.random.default_rng(900 + D)
+    P, gs = 16, 4
+    prefix_pages = [16, 2, 0]
+    suffix = np.array([6000, 5000, 40, 1, 3000, 7000, 2, 900, 4500, 10, 6500, 300])
+    q, kc, vc, bt, lens = _groups(rng, 3, gs, prefix_pages, suffix, 16, 2, D, P)
+    pl = np.array(prefix_pages, np.int32) * P
+    got, err = _cascade(pkv, q, kc, vc, bt, lens, gs, pl, 1 / np.sqrt(D))
+    assert err == 0
+    want = oracle.paged_decode(q, kc, vc, bt, lens, 1 / np.sqrt(D))
+    assert_close_attn(got, want, f"cascade long suffix D={D}")
+
+
 def test_cascade_bad_prefix_and_short_last_group(pkv):
     rng = np.random.default_rng(99)
     P, D, gs = 16, 128, 4

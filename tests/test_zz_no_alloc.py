@@ -54,13 +54,16 @@ def _case(seed, B, long_len, H_q=32, H_kv=8, D=128, P=16):
     return q, kc, vc, bt, lens
 
 
-def _longest_segment_is_split(lens, H_kv, P, n_sms):
+def _longest_segment_is_split(lens, H_kv, P, n_sms, D):
     """The decode kernel cuts a (sequence, kv head) segment into chunks when
     it has more 16-key tiles than half of one CTA's share of the batch's
-    tiles (one persistent CTA per SM) and more than 16."""
+    tiles (one persistent CTA per SM) and more than 16, and the longest
+    segment exceeds that cut by more than a merge's cost (480 KB of K+V,
+    64*D bytes per tile)."""
     tiles = -(-lens.astype(np.int64) // 16)
     half_share = -(-int(tiles.sum()) * H_kv // (2 * n_sms))
-    return int(tiles.max()) > max(16, half_share)
+    cut = max(16, half_share)
+    return int(tiles.max()) > cut + (480 * 1024) // (64 * D)
 
 
 def _args(out, q, kc, vc, bt, lens, scale):
@@ -78,7 +81,7 @@ def test_static_scratch_decode_matches_oracle_and_workspace_decode_twice(lib):
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     for call, (seed, B, long_len) in enumerate([(101, 64, 20000), (202, 23, 9000)]):
         q, kc, vc, bt, lens = _case(seed, B, long_len)
-        assert _longest_segment_is_split(lens, kc.shape[1], kc.shape[2], n_sms)
+        assert _longest_segment_is_split(lens, kc.shape[1], kc.shape[2], n_sms, q.shape[2])
         qd, kd, vd = to_dev_bf16(q), to_dev_bf16(kc), to_dev_bf16(vc)
         btd, ld = to_dev(bt), to_dev(lens)
         scale = 1.0 / np.sqrt(q.shape[2])
