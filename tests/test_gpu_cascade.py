@@ -112,15 +112,15 @@ def test_cascade_shapes_and_edges(pkv, D, H, gs):
     assert_close_attn(got, want, f"cascade D={D} H={H} group={gs}")
 
 
-@pytest.mark.parametrize("D", [128, 256])
-def test_cascade_long_suffix_merges_with_prefix(pkv, D):
+@pytest.mark.parametrize("D,H", [(128, (8, 2)), (256, (4, 2))])
+def test_cascade_long_suffix_merges_with_prefix(pkv, D, H):
     """Suffixes long enough that the decode cuts them into chunks: the merge
     phase then weighs the prefix partial with the suffix chunks."""
     rng = np.random.default_rng(900 + D)
     P, gs = 16, 4
     prefix_pages = [16, 2, 0]
     suffix = np.array([6000, 5000, 40, 1, 3000, 7000, 2, 900, 4500, 10, 6500, 300])
-    q, kc, vc, bt, lens = _groups(rng, 3, gs, prefix_pages, suffix, 16, 2, D, P)
+    q, kc, vc, bt, lens = _groups(rng, 3, gs, prefix_pages, suffix, H[0], H[1], D, P)
     pl = np.array(prefix_pages, np.int32) * P
     got, err = _cascade(pkv, q, kc, vc, bt, lens, gs, pl, 1 / np.sqrt(D))
     assert err == 0
