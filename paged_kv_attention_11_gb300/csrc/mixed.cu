@@ -168,6 +168,7 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   v.scale_log2 = a.scale_log2;
   v.causal = 1;
   v.window = L.window;
+  v.out_v8 = (reinterpret_cast<uintptr_t>(L.pre_out) & 31) == 0 ? 1 : 0;
   v.err = L.err;
   // ---- the split
   int nd = L.decode_ctas;

@@ -109,6 +109,7 @@ cudaError_t launch_varlen(void* out, const VarlenMaps& maps, const int32_t* cu_q
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
   a.window = window;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0 ? 1 : 0;
   a.err = err;
   if (max_seqlen_q <= 0) return cudaSuccess;
   switch (D) {

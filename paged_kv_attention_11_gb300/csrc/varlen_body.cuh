@@ -76,8 +76,20 @@ struct VarlenArgs {
   int64_t num_pages;
   float scale_log2;
   int32_t causal, window;
+  int32_t out_v8;  // out is 32-byte aligned: the epilogue writes 32-byte words
   int32_t* err;
 };
+
+#ifndef PKV_VAR_EPI_BATCH
+#define PKV_VAR_EPI_BATCH 1
+#endif
+
+// One 32-byte global store of 8 words (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(uint32_t* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 
 // DV: the width of O (and of the V columns) one work item computes; D / DV
 // items cover a Q tile (head_dim 512: two halves of 256, each recomputing S)
@@ -727,6 +739,38 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
       ++mi;
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+#if PKV_VAR_EPI_BATCH
+      // two 32-column loads per wait; each 32 columns leave as two 32-byte
+      // (or four 16-byte) stores of the thread's row
+      static_assert((DV / 32) % 2 == 0, "pairs of 32-column chunks");
+#pragma unroll
+      for (int c = 0; c < DV / 32; c += 2) {
+        uint32_t o[2][32];
+        tc::ld_32x32b_x32(o_addr + c * 32, o[0]);
+        tc::ld_32x32b_x32(o_addr + (c + 1) * 32, o[1]);
+        tc::wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16(__uint_as_float(o[e][2 * i]) * inv,
+                                __uint_as_float(o[e][2 * i + 1]) * inv);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(orow + (c + e) * 32);
+            if (a.out_v8) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) st_global_v8(dst + 8 * h, pk + 8 * h);
+            } else {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(dst)[v] =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+      }
+#else
       uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
@@ -745,6 +789,7 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
           }
         }
       }
+#endif
       tc::fence_before_sync();
     }
   }
