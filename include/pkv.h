@@ -24,14 +24,15 @@
  *   of a sequence with block-table row T lives in page T[p / page_size],
  *   row p % page_size.  A slot is page * page_size + row.
  * - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
- * - Supported shapes of the attention calls: head_dim in {64, 128, 256}
- *   (paged_attn_decode and paged_attn_decode_static also 512);
+ * - Supported shapes of the attention calls: head_dim in {64, 128, 256,
+ *   512} (paged_attn_decode_shared_prefix and paged_attn_mixed: see there);
  *   page_size a multiple of 16 (decode tests use 16 and 64, varlen tests 16
  *   to 256), and for varlen a divisor or a multiple of its key tile (128
- *   keys for head_dim 64 and 128, 64 for 256); num_q_heads a multiple of
- *   num_kv_heads with a group of at most 8 for decode and dividing 128 for
- *   varlen; decode batch <= 4096 and varlen batch <= 1024 (their schedules
- *   live in shared memory).
+ *   keys for head_dim 64 and 128, 64 for 256, 32 for 512); num_q_heads a
+ *   multiple of num_kv_heads with a group of at most 8 for decode and
+ *   dividing 128 for varlen; decode batch <= 4096 and varlen batch <= 1024
+ *   (their schedules live in shared memory; varlen at head_dim 512, whose
+ *   Q tile takes 128 KB of it, up to 64).
  *   Anything else returns PKV_ERR_UNSUPPORTED.  The append calls take any
  *   page_size >= 1; paged_kv_append any head_dim that is a multiple of 8,
  *   paged_kv_append_rope head_dim in {64, 128, 256}.
