@@ -703,7 +703,8 @@ def run_grpo(args, device, stream, flush, rank):
     page range): append 256 rows, decode 256 sequences whose 256-token prefix
     pages are shared by 4 generations."""
     try:
-        step = wl.grpo_layer(layers=36, layer=35)
+        nl = max(1, int(getattr(args, "grpo_layers", 36)))
+        step = wl.grpo_layer(layers=nl, layer=nl - 1)
         ds = DeviceStep(step, wl.BASE_SEED + 5 + 1000 * rank, device)
         per = time_steps([ds.append, ds.decode], args.steps, args.warmup, stream, flush,
                          phase_events=False)
@@ -722,7 +723,7 @@ def run_grpo(args, device, stream, flush, rank):
     logical = decode_bytes(step) + append_bytes(step, step.Bd)
     unique = grpo_unique_bytes(step) + append_bytes(step, step.Bd)
     return {"workload": "grpo: 64 prompts x 4 generations, prefix 256 shared, completion "
-                        "~U[0,3840], H 32/8/128, page 16, 36 layers in one pool "
+                        f"~U[0,3840], H 32/8/128, page 16, {nl} layers in one pool "
                         f"({step.num_pages} pages)",
             "layer_step_us": round(ms * 1e3, 2),
             "step_ms_36_layers": round(36 * ms, 3),
@@ -920,6 +921,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-cpu", action="store_true",
                     help="omit the CPU oracle baseline (profiling runs)")
+    ap.add_argument("--grpo-layers", type=int, default=36,
+                    help="layers of the GRPO pool (the timed layer is the last; fewer layers "
+                         "keep the same per-layer work in a smaller pool, for profilers)")
     ap.add_argument("--only", choices=["decode", "mixed", "sliding", "grpo", "d512"],
                     default=None,
                     help="run only one section: the headline decode step, the mixed step, "
