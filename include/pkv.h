@@ -146,6 +146,34 @@ pkv_status paged_attn_decode(void* out, const void* q,
                              int32_t* err_flag, void* stream);
 
 /*
+ * paged_attn_decode_append - the decode step with its append fused in: the
+ * same result as paged_kv_append of each sequence's newest token (slot =
+ * block_table[b][(seq_lens[b]-1) / page_size] * page_size +
+ * (seq_lens[b]-1) % page_size) followed by paged_attn_decode, in one launch
+ * (the decode step of the rollout engine: scripts/benchmarks commit log,
+ * "Files", the in-kernel k_cache[addr] = k_val write, and "Why this works").
+ *
+ *   k_new, v_new  [batch, num_kv_heads, head_dim] bf16: sequence b's new
+ *                 token (read), 16-byte aligned
+ *   k_cache, v_cache  the pools, written at each sequence's position
+ *                 seq_lens[b]-1 (a sequence of length 0 writes nothing)
+ *   every other argument as paged_attn_decode (same workspace).
+ *
+ * The row is written by the CTA that reads the tile holding that position,
+ * before its TMA copies of the tile; no other work of the call reads it.
+ * An out-of-range page id of that position skips the write and raises
+ * PKV_DEVERR_PAGE.
+ */
+pkv_status paged_attn_decode_append(void* out, const void* q, const void* k_new,
+                                    const void* v_new, void* k_cache, void* v_cache,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int64_t num_pages, int32_t max_seq_len, float scale,
+                                    int32_t window, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_flag, void* stream);
+
+/*
  * paged_attn_decode_shared_prefix - paged_attn_decode for batches whose
  * sequences come in groups that share their leading pages (cascade
  * decode).  Source: the grpo_equivalence page (num_generations = 4

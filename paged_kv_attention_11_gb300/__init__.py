@@ -6,8 +6,9 @@ Three calls, same names as the C ABI (include/pkv.h):
 * ``paged_attn_decode`` one query per sequence over its paged prefix
 * ``paged_attn_varlen`` packed variable-length (prefill) attention
 
-plus ``paged_attn_mixed`` (a step's decode rows and prefill chunks in one
-launch), ``paged_attn_decode_shared_prefix`` (decode that reads a prefix
+plus ``paged_attn_decode_append`` (the decode step with its append in the
+same launch), ``paged_attn_mixed`` (a step's decode rows and prefill chunks
+in one launch), ``paged_attn_decode_shared_prefix`` (decode that reads a prefix
 shared by a group of sequences once per group), ``paged_kv_append_rope`` (the
 append with q/k RMSNorm and the rotary embedding fused in) and
 ``rope_table`` (its cos/sin table).
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     lib,
     lib_path,
     paged_attn_decode,
+    paged_attn_decode_append,
     paged_attn_decode_shared_prefix,
     paged_attn_decode_static,
     paged_attn_mixed,

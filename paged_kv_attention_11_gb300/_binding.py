@@ -25,6 +25,9 @@ _SIGS = {
     "paged_attn_decode": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_i32,
                           _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32, _c_p, ctypes.c_size_t,
                           _c_p, _c_p],
+    "paged_attn_decode_append": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32,
+                                 _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_f, _c_i32,
+                                 _c_p, ctypes.c_size_t, _c_p, _c_p],
     "paged_attn_varlen": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32,
                           _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_f, _c_i32,
                           _c_i32, _c_p, _c_p],
@@ -179,6 +182,35 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
         float(scale), int(window), _ptr(workspace), workspace.numel(), _ptr(err_flag),
         _stream(stream)))
+    return out
+
+
+def paged_attn_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor,
+                             v_new: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor,
+                             max_seq_len: int, scale: float, window: int = 0,
+                             workspace: Optional[torch.Tensor] = None,
+                             err_flag: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """paged_attn_decode with each sequence's new K/V row ([B, H_kv, D]
+    k_new/v_new) written to position seq_lens[b]-1 of its pages by the same
+    launch.  Workspace handling as paged_attn_decode."""
+    for n, t in (("out", out), ("q", q), ("k_new", k_new), ("v_new", v_new),
+                 ("k_cache", k_cache), ("v_cache", v_cache)):
+        _bf16(t, n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    B, H_q, D = q.shape
+    num_pages, H_kv, P, _ = k_cache.shape
+    if tuple(k_new.shape) != (B, H_kv, D) or tuple(v_new.shape) != (B, H_kv, D):
+        raise ValueError("k_new and v_new must be [batch, num_kv_heads, head_dim]")
+    if workspace is None:
+        workspace = decode_workspace(q.device, _stream(stream), B, H_q, H_kv, D)
+    _check("paged_attn_decode_append", lib().paged_attn_decode_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages,
+        int(max_seq_len), float(scale), int(window), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)))
     return out
 
 

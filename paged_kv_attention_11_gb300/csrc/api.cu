@@ -143,6 +143,35 @@ pkv_status paged_attn_decode(void* out, const void* q, const void* k_cache, cons
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
+pkv_status paged_attn_decode_append(void* out, const void* q, const void* k_new,
+                                    const void* v_new, void* k_cache, void* v_cache,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                    int64_t num_pages, int32_t max_seq_len, float scale,
+                                    int32_t window, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_flag, void* stream) {
+  const pkv_status chk =
+      pkv::decode_check_args(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                             batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                             max_seq_len, scale);
+  if (chk != PKV_OK || batch == 0) return chk;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_INVALID;
+  int sms = 0;
+  if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
+  if (workspace_bytes <
+      pkv::decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, sms))
+    return PKV_ERR_INVALID;
+  const pkv::DecodeAppend app = {k_new, v_new};
+  cudaError_t e = pkv::launch_decode(
+      out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, batch, num_q_heads,
+      num_kv_heads, head_dim, page_size, num_pages, max_seq_len, scale, window, workspace,
+      workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), sms, nullptr, &app);
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace

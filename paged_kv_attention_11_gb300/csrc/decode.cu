@@ -169,8 +169,13 @@ cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const v
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
                           float scale, int32_t window, void* workspace, size_t workspace_bytes,
                           int32_t* err, cudaStream_t stream, int num_sms,
-                          const DecodeCascade* cascade) {
+                          const DecodeCascade* cascade, const DecodeAppend* append) {
   DecodeArgs a;
+  // the pools are written only by the fused append (append != null)
+  a.k_new = append ? static_cast<const uint4*>(append->k_new) : nullptr;
+  a.v_new = append ? static_cast<const uint4*>(append->v_new) : nullptr;
+  a.k_pool = append ? static_cast<uint4*>(const_cast<void*>(k_cache)) : nullptr;
+  a.v_pool = append ? static_cast<uint4*>(const_cast<void*>(v_cache)) : nullptr;
   a.prefix_lens = cascade ? cascade->prefix_lens : nullptr;
   a.group_size = cascade ? cascade->group_size : 1;
   a.pre_o = cascade ? cascade->pre_o : nullptr;

@@ -102,6 +102,13 @@ struct DecodeArgs {
   // resets it), and the CTA count a segment's fair share is taken over
   int32_t cta_count;
   int32_t share_ctas;
+  // fused append (null k_new: none): row b of k_new / v_new [batch, H_kv, D]
+  // is sequence b's newest token, written to position seq_lens[b] - 1 of
+  // its pages (k_pool / v_pool) before that tile is read
+  const uint4* k_new;
+  const uint4* v_new;
+  uint4* k_pool;
+  uint4* v_pool;
   int32_t* err;
 };
 
@@ -515,8 +522,47 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       it.pfx = pfx;
       return it;
     };
+    // fused append: the item whose tiles hold key L-1 writes the new K/V row
+    // of its (sequence, kv head) first.  Lane l holds 16-byte vector l of
+    // the K row then of the V row (kNV per lane).
+    constexpr int kRowVec = D / 8;                      // vectors of one row
+    constexpr int kNV = (2 * kRowVec + 31) / 32;        // per lane
+    uint4 nrow[kNV];
+    int npage = -1;  // page of key L-1 (-1: nothing to write)
+    auto prefetch_new = [&](const Item& p) {
+      npage = -1;
+      if (a.k_new == nullptr || !p.more || p.n <= 0 || p.L <= 0) return;
+      const int last = (p.L - 1) / kTile;
+      if (last < p.first_tile || last >= p.first_tile + p.n) return;
+      npage = __ldg(a.block_table + (int64_t)p.b * a.max_blocks + (p.L - 1) / a.P);
+      const int64_t row = (int64_t)p.b * a.H_kv + p.g;
+#pragma unroll
+      for (int i = 0; i < kNV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < kRowVec) nrow[i] = __ldg(a.k_new + row * kRowVec + v);
+        else if (v < 2 * kRowVec) nrow[i] = __ldg(a.v_new + row * kRowVec + (v - kRowVec));
+      }
+    };
+    auto write_new = [&](const Item& p) {
+      if (npage < 0) return;
+      if ((int64_t)npage >= a.num_pages) {
+        if (lane == 0) raise_err(a.err, PKV_DEVERR_PAGE);
+        return;
+      }
+      const int64_t dst = (((int64_t)npage * a.H_kv + p.g) * a.P + (p.L - 1) % a.P) * kRowVec;
+#pragma unroll
+      for (int i = 0; i < kNV; ++i) {
+        const int v = lane + 32 * i;
+        if (v < kRowVec) a.k_pool[dst + v] = nrow[i];
+        else if (v < 2 * kRowVec) a.v_pool[dst + (v - kRowVec)] = nrow[i];
+      }
+      // the rows must be seen by the TMA (async proxy) copies of this item
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    };
     auto prefetch = [&](const Item& p, uint4 (&qr)[QV], int& pages) {
       pages = -1;
+      prefetch_new(p);
       if (!p.more) return;
       // page ids first: the first TMA copies need them, the query rows only
       // the record
@@ -586,7 +632,8 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         publish();
         break;
       }
-      // ---- stream the item's tiles ----
+      // ---- stream the item's tiles (after the fused append's row) ----
+      write_new(cur);
       const int* bt = a.block_table + (int64_t)cur.b * a.max_blocks;
       const int n = cur.n;
       int page = pcur;

@@ -67,13 +67,22 @@ struct DecodeCascade {
   const float* pre_lse;
 };
 
+// Fused append of the decode step: each sequence's newest K/V row, written
+// by the decode kernel to position seq_lens[b] - 1 ([batch, H_kv, D] bf16;
+// the pools as written by paged_kv_append).
+struct DecodeAppend {
+  const void* k_new;
+  const void* v_new;
+};
+
 cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_table, int32_t max_blocks,
                           const int32_t* seq_lens, int32_t batch, int32_t H_q, int32_t H_kv,
                           int32_t D, int32_t P, int64_t num_pages, int32_t max_seq_len,
                           float scale, int32_t window, void* workspace, size_t workspace_bytes,
                           int32_t* err, cudaStream_t stream, int num_sms,
-                          const DecodeCascade* cascade = nullptr);
+                          const DecodeCascade* cascade = nullptr,
+                          const DecodeAppend* append = nullptr);
 
 // Prefix pass of the cascade: partial (o, log2-sum-exp) of every member row
 // over its group's shared prefix.  Query rows per (group, kv head) are

@@ -140,6 +140,8 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   a.window = L.window;
   a.scale_log2 = L.scale * 1.4426950408889634f;
   a.prefix_lens = nullptr;
+  a.k_new = a.v_new = nullptr;
+  a.k_pool = a.v_pool = nullptr;
   a.group_size = 1;
   a.pre_o = nullptr;
   a.pre_lse = nullptr;

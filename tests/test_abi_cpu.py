@@ -192,3 +192,19 @@ def test_shared_prefix_decode_validates_on_host(lib):
                                0.1, 1, 0, None, None) == 2
     assert L.paged_attn_decode(P, P, P, P, P, 4, P, 2, 8, 2, 1024, 16, 64, 64, 0.1, 0, P,
                                1 << 20, None, None) == 2
+
+
+def test_decode_append_validates_on_host(lib):
+    L = _bind(lib)
+    P = 0x1000  # fake, never dereferenced: validation fails first
+
+    def call(kn=P, vn=P, H_q=32, D=128, ws=P, B=8, scale=0.1):
+        return L.paged_attn_decode_append(P, P, kn, vn, P, P, P, 4, P, B, H_q, 8, D, 16, 64, 64,
+                                          scale, 0, ws, 1 << 24, None, None)
+    assert call(kn=None) == 1              # missing new K rows
+    assert call(vn=P + 8) == 1             # misaligned new V rows
+    assert call(ws=P + 64) == 1            # workspace not 256-byte aligned
+    assert call(H_q=30) == 1               # H_q not a multiple of H_kv
+    assert call(scale=float("nan")) == 1
+    assert call(D=96) == 2                 # head_dim outside the decode shapes
+    assert call(B=0, kn=None, vn=None) == 0  # empty batch: no-op
