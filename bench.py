@@ -55,12 +55,12 @@ _VAR_SRC = ("varlen.cu", "varlen_body.cuh", "tcgen05.cuh", "exp2_math.cuh", "com
 _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcgen05.cuh",
             "exp2_math.cuh", "common.cuh")
 TRAFFIC = {
-    "decode_qwen3": (320_436_480, _DEC_SRC, "0f4140a6eccb614e"),
-    "decode_d512": (573_863_168, _DEC_SRC, "0f4140a6eccb614e"),
-    "varlen_mixed": (87_192_832, _VAR_SRC, "2306083a91da3df2"),
-    "varlen_d512": (42_849_024, _VAR_SRC, "2306083a91da3df2"),
-    "mixed_single": (1_231_332_352, _MIX_SRC, "44a285d5be6a8100"),
-    "append_mixed": (23_230_720, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
+    "decode_qwen3": (320_379_392, _DEC_SRC, "a8e385bacff3eb17"),
+    "decode_d512": (573_968_896, _DEC_SRC, "a8e385bacff3eb17"),
+    "varlen_mixed": (92_538_880, _VAR_SRC, "673a7df588a8d73b"),
+    "varlen_d512": (43_752_448, _VAR_SRC, "673a7df588a8d73b"),
+    "mixed_single": (1_250_429_440, _MIX_SRC, "71052bd1c5eb6ed1"),
+    "append_mixed": (23_233_536, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
     "append_rope_mixed": (84_039_936, ("rope_append.cu",), "e68e8d036bcc4835"),
 }
 
@@ -501,7 +501,8 @@ def run_ours(args):
     dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------
-    e2e = None if args.only else run_e2e(ds, step, stream, flush, args, dbytes + abytes)
+    e2e = None if args.only else run_e2e(ds, step, stream, flush, args, dbytes + abytes,
+                                         fused=fused_best)
 
     # ---- secondary: mixed continuous-batching step (tokens/s) -------------
     mixed = None if args.only == "decode" else run_mixed(args, device, stream, flush, rank)
@@ -558,36 +559,61 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes):
-    """Same step through the public API, inputs from pinned host memory."""
+def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes, fused=True):
+    """Same step through the public API, inputs from pinned host memory.
+
+    The step's inputs (q, the new K/V rows, block table, lengths; the slot
+    mapping too on the two-call path) sit in one pinned host buffer and go
+    to the device in one copy, as an engine batches its step metadata; the
+    output comes back in one copy.  ``fused``: paged_attn_decode_append
+    (one launch), else paged_kv_append then paged_attn_decode."""
     import torch
-    host = {
-        "q": ds.q_dec.cpu().pin_memory(), "k_new": ds.k_new.cpu().pin_memory(),
-        "v_new": ds.v_new.cpu().pin_memory(), "slots": ds.slots.cpu().pin_memory(),
-        "bt": ds.dec_bt.cpu().pin_memory(), "lens": ds.dec_lens.cpu().pin_memory(),
-    }
+    parts = {"q": ds.q_dec, "k_new": ds.k_new, "v_new": ds.v_new, "bt": ds.dec_bt,
+             "lens": ds.dec_lens}
+    if not fused:
+        parts["slots"] = ds.slots
+    offs, off = {}, 0
+    for k, t in parts.items():
+        offs[k] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(off, dtype=torch.uint8, device=ds.q_dec.device)
+
+    def view(buf, k):
+        t = parts[k]
+        n = t.numel() * t.element_size()
+        return buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+    for k, t in parts.items():
+        view(host_buf, k).copy_(t.cpu())
+    dev = {k: view(dev_buf, k) for k in parts}
     out_h = torch.empty(ds.out_dec.shape, dtype=ds.out_dec.dtype).pin_memory()
-    dev = {k: torch.empty_like(v, device=ds.q_dec.device) for k, v in host.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in parts.values())
     d2h = out_h.numel() * out_h.element_size()
     pkv = ds.pkv
 
     def full(s):
         with torch.cuda.stream(s):
-            for k in host:
-                dev[k].copy_(host[k], non_blocking=True)
-            pkv.paged_kv_append(dev["k_new"], dev["v_new"], ds.k_cache, ds.v_cache,
-                                dev["slots"], err_flag=ds.err, stream=s)
-            pkv.paged_attn_decode(ds.out_dec, dev["q"], ds.k_cache, ds.v_cache, dev["bt"],
-                                  dev["lens"], step.max_seq_len_dec(), step.scale, step.window,
-                                  workspace=ds.ws, err_flag=ds.err, stream=s)
+            dev_buf.copy_(host_buf, non_blocking=True)
+            if fused:
+                pkv.paged_attn_decode_append(ds.out_dec, dev["q"], dev["k_new"], dev["v_new"],
+                                             ds.k_cache, ds.v_cache, dev["bt"], dev["lens"],
+                                             step.max_seq_len_dec(), step.scale, step.window,
+                                             workspace=ds.ws, err_flag=ds.err, stream=s)
+            else:
+                pkv.paged_kv_append(dev["k_new"], dev["v_new"], ds.k_cache, ds.v_cache,
+                                    dev["slots"], err_flag=ds.err, stream=s)
+                pkv.paged_attn_decode(ds.out_dec, dev["q"], ds.k_cache, ds.v_cache, dev["bt"],
+                                      dev["lens"], step.max_seq_len_dec(), step.scale,
+                                      step.window, workspace=ds.ws, err_flag=ds.err, stream=s)
             out_h.copy_(ds.out_dec, non_blocking=True)
 
     per = time_steps([full], args.steps, args.warmup, stream, flush, graphs=False)
     ms = float(np.mean([p[0] for p in per]))
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h),
+            "path": ("one H2D copy, paged_attn_decode_append, one D2H copy" if fused else
+                     "one H2D copy, paged_kv_append + paged_attn_decode, one D2H copy")}
 
 
 def run_mixed(args, device, stream, flush, rank):

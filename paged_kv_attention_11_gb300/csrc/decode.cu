@@ -5,14 +5,14 @@
 
 namespace pkv {
 
-template <int D, int NW, int NSTAGE>
+template <int D, int NW, int NSTAGE, bool APPEND>
 __global__ void __launch_bounds__((NW + 2) * 32, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  decode_cta<D, NW, NSTAGE, false>(a, tmK, tmV, smem, blockIdx.x);
+  decode_cta<D, NW, NSTAGE, false, APPEND>(a, tmK, tmV, smem, blockIdx.x);
 }
 
 // --------------------------------------------------------------- host side
@@ -81,12 +81,12 @@ void decode_workspace_split(DecodeArgs& a, void* workspace, size_t workspace_byt
   a.part_lse = reinterpret_cast<float*>(end);
 }
 
-template <int D, int NW, int NSTAGE>
+template <int D, int NW, int NSTAGE, bool APPEND>
 static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
   using P_ = DecodePlan<D, NW, NSTAGE>;
-  auto kern = decode_split_kernel<D, NW, NSTAGE>;
+  auto kern = decode_split_kernel<D, NW, NSTAGE, APPEND>;
   (void)max_seq_len;
   // one TMA box per 16-key K or V tile (all D columns of one page and head)
   CUtensorMap tmK, tmV;
@@ -142,23 +142,23 @@ static bool decode_fits(const DecodeArgs& a) {
   return DecodePlan<D, NW, NSTAGE>(a.G, a.batch).total <= 227 * 1024;
 }
 
-template <int D>
+template <int D, bool APPEND>
 static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
   if (decode_fits<D, C::NW, C::NSTAGE>(a))
-    return launch_decode_s<D, C::NW, C::NSTAGE>(a, k_cache, v_cache, max_seq_len, stream,
-                                                 num_sms);
+    return launch_decode_s<D, C::NW, C::NSTAGE, APPEND>(a, k_cache, v_cache, max_seq_len,
+                                                         stream, num_sms);
   if constexpr (D <= 128) {
     if (decode_fits<D, 4, 16>(a))
-      return launch_decode_s<D, 4, 16>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+      return launch_decode_s<D, 4, 16, APPEND>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     if (decode_fits<D, 4, 8>(a))
-      return launch_decode_s<D, 4, 8>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+      return launch_decode_s<D, 4, 8, APPEND>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
   } else if constexpr (D == 256) {
     if (decode_fits<D, 2, 8>(a))
-      return launch_decode_s<D, 2, 8>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+      return launch_decode_s<D, 2, 8, APPEND>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     if (decode_fits<D, 2, 4>(a))
-      return launch_decode_s<D, 2, 4>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+      return launch_decode_s<D, 2, 4, APPEND>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
   }
   return cudaErrorNotSupported;
 }
@@ -195,11 +195,22 @@ cudaError_t launch_decode(void* out, const void* q, const void* k_cache, const v
   a.scale_log2 = scale * 1.4426950408889634f;
   decode_workspace_split(a, workspace, workspace_bytes, batch, H_kv, D, num_sms);
   a.err = err;
+  // the fused append is a separate build of the kernel, so that the plain
+  // decode carries none of its code
+  const bool app = a.k_new != nullptr;
   switch (D) {
-    case 64: return launch_decode_t<64>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
-    case 128: return launch_decode_t<128>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
-    case 256: return launch_decode_t<256>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
-    case 512: return launch_decode_t<512>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 64:
+      return app ? launch_decode_t<64, true>(a, k_cache, v_cache, max_seq_len, stream, num_sms)
+                 : launch_decode_t<64, false>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 128:
+      return app ? launch_decode_t<128, true>(a, k_cache, v_cache, max_seq_len, stream, num_sms)
+                 : launch_decode_t<128, false>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 256:
+      return app ? launch_decode_t<256, true>(a, k_cache, v_cache, max_seq_len, stream, num_sms)
+                 : launch_decode_t<256, false>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
+    case 512:
+      return app ? launch_decode_t<512, true>(a, k_cache, v_cache, max_seq_len, stream, num_sms)
+                 : launch_decode_t<512, false>(a, k_cache, v_cache, max_seq_len, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -204,8 +204,9 @@ struct DecodePlan {
 // hosts this body on part of its warps), so the body synchronises on a
 // named barrier of its own threads instead of the whole block.  `cta` is
 // this CTA's index among the a.cta_count CTAs that run the body; smem is the
-// 1024-aligned base of the dynamic shared memory.
-template <int D, int NW, int NSTAGE, bool SUBSET>
+// 1024-aligned base of the dynamic shared memory.  APPEND: the fused append
+// of paged_attn_decode_append (a.k_new set); compiled out otherwise.
+template <int D, int NW, int NSTAGE, bool SUBSET, bool APPEND = false>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
   static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
@@ -531,7 +532,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     int npage = -1;  // page of key L-1 (-1: nothing to write)
     auto prefetch_new = [&](const Item& p) {
       npage = -1;
-      if (a.k_new == nullptr || !p.more || p.n <= 0 || p.L <= 0) return;
+      if (!APPEND || !p.more || p.n <= 0 || p.L <= 0) return;
       const int last = (p.L - 1) / kTile;
       if (last < p.first_tile || last >= p.first_tile + p.n) return;
       npage = __ldg(a.block_table + (int64_t)p.b * a.max_blocks + (p.L - 1) / a.P);
@@ -544,7 +545,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       }
     };
     auto write_new = [&](const Item& p) {
-      if (npage < 0) return;
+      if (!APPEND || npage < 0) return;
       if ((int64_t)npage >= a.num_pages) {
         if (lane == 0) raise_err(a.err, PKV_DEVERR_PAGE);
         return;
