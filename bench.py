@@ -57,10 +57,10 @@ _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcg
 TRAFFIC = {
     "decode_qwen3": (320_379_392, _DEC_SRC, "a8e385bacff3eb17"),
     "decode_d512": (573_968_896, _DEC_SRC, "a8e385bacff3eb17"),
-    "varlen_mixed": (92_538_880, _VAR_SRC, "673a7df588a8d73b"),
-    "varlen_d512": (43_752_448, _VAR_SRC, "673a7df588a8d73b"),
+    "varlen_mixed": (92_761_600, _VAR_SRC, "673a7df588a8d73b"),
+    "varlen_d512": (43_810_304, _VAR_SRC, "673a7df588a8d73b"),
     "mixed_single": (1_250_429_440, _MIX_SRC, "71052bd1c5eb6ed1"),
-    "append_mixed": (23_233_536, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
+    "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
     "append_rope_mixed": (84_039_936, ("rope_append.cu",), "e68e8d036bcc4835"),
 }
 
