@@ -61,7 +61,7 @@ TRAFFIC = {
     "varlen_d512": (43_810_304, _VAR_SRC, "673a7df588a8d73b"),
     "mixed_single": (1_250_429_440, _MIX_SRC, "71052bd1c5eb6ed1"),
     "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
-    "append_rope_mixed": (84_039_936, ("rope_append.cu",), "e68e8d036bcc4835"),
+    "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4b03849b8c981063"),
 }
 
 

@@ -44,10 +44,10 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cs,
 // rows, the v rows) are loaded before any is finished.  Arithmetic on pairs
 // of floats uses the f32x2 forms.
 #ifndef PKV_ROPE_STEPS
-#define PKV_ROPE_STEPS 1
+#define PKV_ROPE_STEPS 2
 #endif
 #ifndef PKV_ROPE_MINBLOCKS
-#define PKV_ROPE_MINBLOCKS 3
+#define PKV_ROPE_MINBLOCKS 2
 #endif
 constexpr int kRopeSteps = PKV_ROPE_STEPS;
 constexpr int kRopeBlocksPerSm = PKV_ROPE_MINBLOCKS;

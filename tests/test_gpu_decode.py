@@ -245,6 +245,39 @@ def test_append_large_prefill_sized(pkv):
     assert np.array_equal(bf16_dev_to_bits(vd), hv)
 
 
+@pytest.mark.parametrize("T,H_kv,D,P", [
+    (1, 8, 128, 16),       # one token
+    (3, 1, 512, 16),       # a 1 KB row: fewer vectors than lanes
+    (40000, 8, 128, 16),   # more tokens than one wave of warps
+    (5000, 1, 256, 64),
+    (777, 2, 64, 32),
+    (300, 24, 512, 16),    # 24 KB rows: many passes per warp
+    (50, 64, 512, 16),     # 64 KB rows
+])
+def test_append_row_sizes_and_padding(pkv, T, H_kv, D, P):
+    """Whole pools bit-exact against the oracle across token counts and row
+    sizes (one or two vectors per lane per pass, many passes), with padding
+    rows mixed in."""
+    import torch
+    rng = np.random.default_rng(T + H_kv + D)
+    num_pages = -(-T // P) + 3
+    kc = wl.randn_bf16(rng, (num_pages, H_kv, P, D))
+    vc = wl.randn_bf16(rng, (num_pages, H_kv, P, D))
+    slots = rng.permutation(num_pages * P)[:T].astype(np.int64)
+    slots[::7] = -1
+    k_new = wl.randn_bf16(rng, (T, H_kv, D))
+    v_new = wl.randn_bf16(rng, (T, H_kv, D))
+    kd, vd = to_dev_bf16(kc), to_dev_bf16(vc)
+    err = _err(torch)
+    pkv.paged_kv_append(to_dev_bf16(k_new), to_dev_bf16(v_new), kd, vd, to_dev(slots),
+                        err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    hk, hv = oracle.kv_append(kc, vc, k_new, v_new, slots)
+    assert np.array_equal(bf16_dev_to_bits(kd), hk)
+    assert np.array_equal(bf16_dev_to_bits(vd), hv)
+
+
 def test_decode_workspace_reuse_stays_clean(pkv):
     """One workspace across many calls of different shapes: the arrival
     counters must return to zero after every call."""
