@@ -5,14 +5,14 @@
 
 namespace pkv {
 
-template <int D, int NW, int NSTAGE, bool APPEND>
+template <int D, int NW, int NSTAGE, bool APPEND, int HP>
 __global__ void __launch_bounds__((NW + 2) * 32, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  decode_cta<D, NW, NSTAGE, false, APPEND>(a, tmK, tmV, smem, blockIdx.x);
+  decode_cta<D, NW, NSTAGE, false, APPEND, HP>(a, tmK, tmV, smem, blockIdx.x);
 }
 
 // --------------------------------------------------------------- host side
@@ -49,19 +49,21 @@ static int decode_ctas_per_sm(int D) {
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Work items (and so partial slots) are at most one per segment plus 2 per
-// CTA: a segment is cut into chunks of >= W/(2N) tiles.
-static int64_t decode_max_pieces(int32_t batch, int32_t H_kv, int32_t D, int num_sms) {
-  return (int64_t)batch * H_kv + 2 * (int64_t)num_sms * decode_ctas_per_sm(D);
+// CTA: a segment is cut into chunks of >= W/(2N) tiles.  A slot holds the
+// item's HP * G query rows.
+static int64_t decode_max_rows(int32_t batch, int32_t H_kv, int32_t G, int32_t D, int num_sms) {
+  const int HP = decode_heads_per_item(D, H_kv, G);
+  const int64_t pieces = (int64_t)batch * (H_kv / HP) + 2 * (int64_t)num_sms * decode_ctas_per_sm(D);
+  return pieces * G * HP;
 }
 
 // Workspace: [seg_count: batch*H_kv int32][merge_jobs: batch*H_kv int32]
 //            [queue: 8 int32] ... [part_lse: pieces*G f32][part_o: pieces*G*D f32]
 // (partials aligned to the end of the caller's buffer)
 size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t D, int num_sms) {
-  const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
-  const int64_t G = H_q / H_kv;
-  return align256(((size_t)batch * H_kv * 2 + 8) * 4) + align256((size_t)pieces * G * 4) +
-         align256((size_t)pieces * G * D * 4);
+  const int64_t rows = decode_max_rows(batch, H_kv, H_q / H_kv, D, num_sms);
+  return align256(((size_t)batch * H_kv * 2 + 8) * 4) + align256((size_t)rows * 4) +
+         align256((size_t)rows * D * 4);
 }
 
 // Counters sit at the front and the partial results at the back of the
@@ -69,30 +71,31 @@ size_t decode_workspace_bytes(int32_t batch, int32_t H_q, int32_t H_kv, int32_t 
 // never see each other's partials in their counter slots.
 void decode_workspace_split(DecodeArgs& a, void* workspace, size_t workspace_bytes,
                             int32_t batch, int32_t H_kv, int32_t D, int num_sms) {
-  const int64_t pieces = decode_max_pieces(batch, H_kv, D, num_sms);
+  const int64_t rows = decode_max_rows(batch, H_kv, a.G, D, num_sms);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.seg_count = reinterpret_cast<int32_t*>(ws);
   a.merge_jobs = a.seg_count + (int64_t)batch * H_kv;
   a.queue = a.merge_jobs + (int64_t)batch * H_kv;
   uint8_t* end = ws + (workspace_bytes & ~size_t(255));
-  end -= align256((size_t)pieces * a.G * D * 4);
+  end -= align256((size_t)rows * D * 4);
   a.part_o = reinterpret_cast<float*>(end);
-  end -= align256((size_t)pieces * a.G * 4);
+  end -= align256((size_t)rows * 4);
   a.part_lse = reinterpret_cast<float*>(end);
 }
 
-template <int D, int NW, int NSTAGE, bool APPEND>
+template <int D, int NW, int NSTAGE, bool APPEND, int HP = 1>
 static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
-  using P_ = DecodePlan<D, NW, NSTAGE>;
-  auto kern = decode_split_kernel<D, NW, NSTAGE, APPEND>;
+  using P_ = DecodePlan<D, NW, NSTAGE, HP>;
+  auto kern = decode_split_kernel<D, NW, NSTAGE, APPEND, HP>;
   (void)max_seq_len;
-  // one TMA box per 16-key K or V tile (all D columns of one page and head)
+  // one TMA box per 16-key K or V tile (all D columns of one page and the
+  // item's HP heads)
   CUtensorMap tmK, tmV;
   const bool enc_ok =
-      encode_pool_map_groups(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv, kTile) &&
-      encode_pool_map_groups(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv, kTile);
+      encode_pool_map_groups(&tmK, k_cache, D, a.P, a.num_pages, a.H_kv, kTile, 0, HP) &&
+      encode_pool_map_groups(&tmV, v_cache, D, a.P, a.num_pages, a.H_kv, kTile, 0, HP);
   if (!enc_ok) return cudaErrorInvalidValue;
   const size_t smem = P_(a.G, a.batch).total;
   if (smem > 227 * 1024) return cudaErrorNotSupported;
@@ -137,15 +140,20 @@ static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void
 // The configured shape when the batch's shared-memory plan leaves room for
 // it, else smaller rings (then fewer consumer warps): large batches need
 // room for the per-sequence schedule arrays.
-template <int D, int NW, int NSTAGE>
+template <int D, int NW, int NSTAGE, int HP = 1>
 static bool decode_fits(const DecodeArgs& a) {
-  return DecodePlan<D, NW, NSTAGE>(a.G, a.batch).total <= 227 * 1024;
+  return DecodePlan<D, NW, NSTAGE, HP>(a.G, a.batch).total <= 227 * 1024;
 }
 
 template <int D, bool APPEND>
 static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
+  // One kv head per item here: with every SM streaming, the decode runs at
+  // HBM's rate either way, and items of one head balance the grid better
+  // (two-head items made the schedule cut the longest sequences of the
+  // qwen3 batch into merged chunks: 65.5 against 61.4 us).  The mixed-step
+  // kernel, whose decode runs on part of the SMs, takes two.
   if (decode_fits<D, C::NW, C::NSTAGE>(a))
     return launch_decode_s<D, C::NW, C::NSTAGE, APPEND>(a, k_cache, v_cache, max_seq_len,
                                                          stream, num_sms);

@@ -171,12 +171,13 @@ struct DecodeLayout {
 };
 
 // Shared-memory plan (byte offsets from the 1024-aligned base); depends on
-// the runtime GQA group and batch.
-template <int D, int NW, int NSTAGE>
+// the runtime GQA group and batch.  HP: kv heads per work item (a stage
+// holds the item's HP heads of one 16-key tile, K then V).
+template <int D, int NW, int NSTAGE, int HP = 1>
 struct DecodePlan {
   using Lay = DecodeLayout<D>;
-  static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+  static constexpr int kTileBytes = kTile * D * 2;      // one K (or V) tile of one head
+  static constexpr int kStageBytes = 2 * HP * kTileBytes;  // K + V
   static constexpr int kCombStride = D + 4;             // padded row (floats)
   // consumer states reach the epilogue through two combine buffers, or one
   // where the buffer is large (head_dim 512, or 8 consumer warps)
@@ -185,7 +186,7 @@ struct DecodePlan {
   __host__ __device__ DecodePlan(int G, int batch) {
     int o = NSTAGE * kStageBytes;
     rec = o;   o += kNRec * (int)sizeof(PieceRec);
-    qslot = (Lay::kQSmem ? kGP : G) * Lay::kQRowBytes;
+    qslot = (Lay::kQSmem ? kGP : G * HP) * Lay::kQRowBytes;
     qbuf = o;  o += kNRec * qslot;
     comb = o;  o += kNComb * NW * G * kCombStride * 4;
     ml = o;    o += kNComb * NW * G * 2 * 4;
@@ -206,12 +207,22 @@ struct DecodePlan {
 // this CTA's index among the a.cta_count CTAs that run the body; smem is the
 // 1024-aligned base of the dynamic shared memory.  APPEND: the fused append
 // of paged_attn_decode_append (a.k_new set); compiled out otherwise.
-template <int D, int NW, int NSTAGE, bool SUBSET, bool APPEND = false>
+// HP: kv heads per work item.  With HP = 2 an item is (sequence, pair of kv
+// heads, chunk): one TMA box carries both heads' 16-key slice of a page
+// (half the boxes per byte), the item's 2G query rows are handled as one
+// group ("virtual head" g of H_kv / 2), and consumer warp w takes head
+// w % 2 of the stages of its pair w / 2.  The host requires H_kv % HP == 0
+// and HP * G <= 8.
+template <int D, int NW, int NSTAGE, bool SUBSET, bool APPEND = false, int HP = 1>
 __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMap& tmK,
                                            const CUtensorMap& tmV, uint8_t* smem, int cta) {
-  static_assert(NSTAGE % NW == 0, "each stage must always feed the same warp");
+  static_assert(HP == 1 || HP == 2, "one or two kv heads per item");
+  static_assert(NW % HP == 0, "whole warp pairs");
+  constexpr int NWH = NW / HP;  // consumer warps per head
+  static_assert(NSTAGE % NWH == 0, "each stage must always feed the same warps");
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
-  using P_ = DecodePlan<D, NW, NSTAGE>;
+  static_assert(HP == 1 || !DecodeLayout<D>::kQSmem, "query rows in registers");
+  using P_ = DecodePlan<D, NW, NSTAGE, HP>;
   using Lay = DecodeLayout<D>;
   constexpr bool QS = Lay::kQSmem;
   constexpr int NCB = P_::kNComb;
@@ -220,7 +231,9 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   constexpr int CS = P_::kCombStride;
   constexpr int kIssueLanes = NSTAGE < 16 ? NSTAGE : 16;  // producer lanes testing stages
   static_assert(kIssueLanes < 32, "a run of free stages ends inside the warp");
-  const int G = a.G;
+  const int G = a.G;        // query heads per kv head
+  const int GV = G * HP;    // query rows per item
+  const int HV = a.H_kv / HP;  // items per (sequence, chunk)
   const P_ plan(G, a.batch);
 
   auto block_sync = [&]() {
@@ -260,7 +273,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     if (i < NSTAGE) {
       mbar_init(full + i, 1);
     } else if (i < 2 * NSTAGE) {
-      mbar_init(full + i, 1);  // empty[i - NSTAGE]
+      mbar_init(full + i, HP);  // empty[i - NSTAGE]: the stage's consumer warps
     } else if (i < 2 * NSTAGE + kNRec) {
       mbar_init(rec_full + (i - 2 * NSTAGE), 32);
     } else if (i < 2 * NSTAGE + 2 * kNRec) {
@@ -344,12 +357,14 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         tot += scan_tmp[w];
         tmax = max(tmax, s_misc[4 + w]);
       }
-      const int64_t W = tot * a.H_kv;
+      // units: an item's tile (HP heads of 16 keys, K and V: 64 * D * HP bytes)
+      const int64_t W = tot * HV;
       const int64_t half_share = (W + 2 * (int64_t)a.share_ctas - 1) / (2 * (int64_t)a.share_ctas);
       int64_t floor_tiles = kMinChunkTiles;
-      if ((int64_t)kMinChunkBytes / (64 * D) > floor_tiles) floor_tiles = kMinChunkBytes / (64 * D);
+      if ((int64_t)kMinChunkBytes / (64 * D * HP) > floor_tiles)
+        floor_tiles = kMinChunkBytes / (64 * D * HP);
       int64_t cut = half_share > floor_tiles ? half_share : floor_tiles;
-      if ((int64_t)tmax <= cut + kMergeCostBytes / (64 * D)) cut = tmax > 0 ? tmax : 1;
+      if ((int64_t)tmax <= cut + kMergeCostBytes / (64 * D * HP)) cut = tmax > 0 ? tmax : 1;
       s_misc[0] = (int)cut;  // S_max
       s_misc[1] = 0;  // sequences cut into more than one chunk
     }
@@ -363,7 +378,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     for (int b = tid; b < B; b += NT) {
       const int t = s_nat[b];
       const int nch = nch_of(t);
-      s_nat[b] = nch * a.H_kv;
+      s_nat[b] = nch * HV;
       s_sp[b] = t == 0 ? 0 : (t + nch - 1) / nch;
       chunked += nch > 1 ? 1 : 0;
     }
@@ -476,7 +491,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     // item is streamed, so no global-memory latency sits between items.
     constexpr int QV = D / 32;  // query vectors per lane for a group of <= 8 heads
     bool dead = false;
-    const int qvec = G * D / 8;  // 16-byte vectors of the group's query rows
+    const int qvec = GV * D / 8;  // 16-byte vectors of the item's query rows
     struct Item {
       bool more;
       int b, g, L, lo, first_tile, n, nch, slot0, chunk, pfx;
@@ -523,11 +538,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       it.pfx = pfx;
       return it;
     };
-    // fused append: the item whose tiles hold key L-1 writes the new K/V row
-    // of its (sequence, kv head) first.  Lane l holds 16-byte vector l of
-    // the K row then of the V row (kNV per lane).
+    // fused append: the item whose tiles hold key L-1 writes the new K/V
+    // rows of its (sequence, kv heads) first.  Lane l holds 16-byte vector l
+    // of the HP K rows then of the HP V rows (kNV per lane).
     constexpr int kRowVec = D / 8;                      // vectors of one row
-    constexpr int kNV = (2 * kRowVec + 31) / 32;        // per lane
+    constexpr int kNV = (2 * HP * kRowVec + 31) / 32;   // per lane
     uint4 nrow[kNV];
     int npage = -1;  // page of key L-1 (-1: nothing to write)
     auto prefetch_new = [&](const Item& p) {
@@ -536,12 +551,13 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       const int last = (p.L - 1) / kTile;
       if (last < p.first_tile || last >= p.first_tile + p.n) return;
       npage = __ldg(a.block_table + (int64_t)p.b * a.max_blocks + (p.L - 1) / a.P);
-      const int64_t row = (int64_t)p.b * a.H_kv + p.g;
+      const int64_t row = (int64_t)p.b * a.H_kv + HP * p.g;  // the item's first head
 #pragma unroll
       for (int i = 0; i < kNV; ++i) {
         const int v = lane + 32 * i;
-        if (v < kRowVec) nrow[i] = __ldg(a.k_new + row * kRowVec + v);
-        else if (v < 2 * kRowVec) nrow[i] = __ldg(a.v_new + row * kRowVec + (v - kRowVec));
+        if (v < HP * kRowVec) nrow[i] = __ldg(a.k_new + row * kRowVec + v);
+        else if (v < 2 * HP * kRowVec)
+          nrow[i] = __ldg(a.v_new + row * kRowVec + (v - HP * kRowVec));
       }
     };
     auto write_new = [&](const Item& p) {
@@ -550,12 +566,16 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         if (lane == 0) raise_err(a.err, PKV_DEVERR_PAGE);
         return;
       }
-      const int64_t dst = (((int64_t)npage * a.H_kv + p.g) * a.P + (p.L - 1) % a.P) * kRowVec;
+      // head h's row sits P * kRowVec vectors after head h - 1's
+      const int64_t dst =
+          (((int64_t)npage * a.H_kv + HP * p.g) * a.P + (p.L - 1) % a.P) * kRowVec;
 #pragma unroll
       for (int i = 0; i < kNV; ++i) {
         const int v = lane + 32 * i;
-        if (v < kRowVec) a.k_pool[dst + v] = nrow[i];
-        else if (v < 2 * kRowVec) a.v_pool[dst + (v - kRowVec)] = nrow[i];
+        const int w = v < HP * kRowVec ? v : v - HP * kRowVec;  // vector in the K or V rows
+        const int64_t off = dst + (int64_t)(w / kRowVec) * a.P * kRowVec + (w % kRowVec);
+        if (v < HP * kRowVec) a.k_pool[off] = nrow[i];
+        else if (v < 2 * HP * kRowVec) a.v_pool[off] = nrow[i];
       }
       // the rows must be seen by the TMA (async proxy) copies of this item
       asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -571,7 +591,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         pages = __ldg(a.block_table + (int64_t)p.b * a.max_blocks +
                       ((p.first_tile + lane) * kTile) / a.P);
       const uint4* qsrc =
-          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.b * a.H_q + p.g * G) * D);
+          reinterpret_cast<const uint4*>(a.q + ((int64_t)p.b * a.H_q + p.g * GV) * D);
 #pragma unroll
       for (int i = 0; i < QV; ++i) {
         const int v = lane + 32 * i;
@@ -674,10 +694,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
               uint8_t* st = smem + s * P_::kStageBytes;
               mbar_arrive_expect_tx(full + s, P_::kStageBytes);
               const int row = key0 % a.P;
-              const int z = pg * a.H_kv + cur.g;
-              // one box per tile: 16 keys x all D columns of one page and head
+              const int z = pg * a.H_kv + HP * cur.g;
+              // one box per tile: 16 keys x all D columns of one page and
+              // the item's HP heads
               tma_load_5d(st, &tmK, full + s, 0, 0, 0, row / 8, z);
-              tma_load_5d(st + P_::kTileBytes, &tmV, full + s, 0, 0, 0, row / 8, z);
+              tma_load_5d(st + HP * P_::kTileBytes, &tmV, full + s, 0, 0, 0, row / 8, z);
             } else {
               raise_err(a.err, PKV_DEVERR_PAGE);
               mbar_arrive(full + s);
@@ -715,6 +736,8 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
     // ============================== consumer warps ==========================
     const int quad = lane >> 2;  // 0..7: key row (QK) / head (Q frag)
     const int qlan = lane & 3;   // 0..3: head pair (2*qlan, 2*qlan+1)
+    const int hd = warp % HP;    // the item's kv head this warp takes
+    const int team = warp / HP;  // this warp's place among the head's warps
     bool dead = false;
     int it_base = 0;
     for (int k = 0;; ++k) {
@@ -726,7 +749,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       uint32_t qb[QS ? 1 : KS][2];
       if (!QS) {
         const bool hv = rec.n >= 0 && quad < G;
-        const uint8_t* qrow = qbuf + slot * plan.qslot + (hv ? quad : 0) * D * 2;
+        const uint8_t* qrow = qbuf + slot * plan.qslot + (hv ? hd * G + quad : 0) * D * 2;
 #pragma unroll
         for (int ks = 0; ks < (QS ? 1 : KS); ++ks) {
           qb[ks][0] = hv ? *reinterpret_cast<const uint32_t*>(qrow + (ks * 16 + 2 * qlan) * 2)
@@ -750,17 +773,19 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
       const int n = rec.n;
-      // this warp takes the item's tiles kk = r, r+NW, ...; r depends only on
-      // where the item starts in the stage ring, and the epilogue combines
-      // the warps in r order, so the result does not depend on the CTA
-      const int r0 = ((warp - it_base) % NW + NW) % NW;
-      for (int kk = r0; kk < n; kk += NW) {
+      // this warp takes the item's tiles kk = r, r+NWH, ...; r depends only
+      // on where the item starts in the stage ring, and the epilogue
+      // combines the warps in r order, so the result does not depend on the
+      // CTA
+      const int r0 = ((team - it_base) % NWH + NWH) % NWH;
+      for (int kk = r0; kk < n; kk += NWH) {
         const int it = it_base + kk;
         const int s = it % NSTAGE;
         const bool landed = mbar_wait(full + s, (it / NSTAGE) & 1, a.err, dead);
         const bool ok = landed && stage_ok[s] != 0;
-        const uint32_t stK = smem_u32(smem + s * P_::kStageBytes);
-        const uint32_t stV = stK + P_::kTileBytes;
+        // head hd's K tile, then (after the HP K tiles) its V tile
+        const uint32_t stK = smem_u32(smem + s * P_::kStageBytes) + hd * P_::kTileBytes;
+        const uint32_t stV = stK + HP * P_::kTileBytes;
         const int key0 = (rec.first_tile + kk) * kTile;
 
         // ---- S^T = K Q^T: 16 keys x 8 heads, two accumulation chains ----
@@ -851,8 +876,8 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       }
       const int cb = k % NCB;
       if (k >= NCB) mbar_wait(comb_empty + cb, ((k / NCB) - 1) & 1, a.err, dead);
-      float* co = comb_o + ((cb * NW + r0) * G) * CS;
-      float* cml = comb_ml + ((cb * NW + r0) * G) * 2;
+      float* co = comb_o + ((cb * NW + hd * NWH + r0) * G) * CS;
+      float* cml = comb_ml + ((cb * NW + hd * NWH + r0) * G) * 2;
       const int hA = 2 * qlan, hB = hA + 1;
 #pragma unroll
       for (int md = 0; md < KS; ++md) {
@@ -895,25 +920,28 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       // inline, with the prefix partial's weight from its log-sum-exp
       const bool join_pfx = rec.nch == 1 && rec.pfx == 1;
       const bool whole = rec.nch == 1;
-      const int64_t pre_row0 = (int64_t)b * a.H_q + g * G;
+      const int64_t pre_row0 = (int64_t)b * a.H_q + g * GV;
       float* w_item = epi_w + NW * kGP;  // [kGP] weights of the joined outputs
       float* w_pfx = w_item + kGP;           // [kGP]
       const float* co = comb_o + (cb * NW * G) * CS;
       const float* cml = comb_ml + (cb * NW * G) * 2;
       const int64_t pslot = (int64_t)rec.slot0 + rec.chunk;
-      // per head: weight of each consumer warp's state, 1/l, log2-sum-exp
-      float* wsc = epi_w;  // [NW][G] scratch
-      if (lane < G) {
+      // per query row h of the item (kv head h / G, its row h % G, held by
+      // warps (h / G) * NWH + r): weight of each warp's state, 1/l,
+      // log2-sum-exp
+      float* wsc = epi_w;  // [NWH][GV] scratch
+      auto cidx = [&](int r, int h) { return ((h / G) * NWH + r) * G + (h % G); };
+      if (lane < GV) {
         const int h = lane;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, cml[(w * G + h) * 2]);
+        for (int r = 0; r < NWH; ++r) M = fmaxf(M, cml[cidx(r, h) * 2]);
         float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = M == -INFINITY ? 0.f : exp2f(cml[(w * G + h) * 2] - M);
-          wsc[w * G + h] = sc;
-          lsum += sc * cml[(w * G + h) * 2 + 1];
+        for (int r = 0; r < NWH; ++r) {
+          const float sc = M == -INFINITY ? 0.f : exp2f(cml[cidx(r, h) * 2] - M);
+          wsc[r * GV + h] = sc;
+          lsum += sc * cml[cidx(r, h) * 2 + 1];
         }
         merge_m[h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
         merge_inv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -931,12 +959,12 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       __syncwarp();
       // 4 slices per lane per pass; the prefix partial's loads (cascade)
       // are issued before any is used
-      for (int j0 = lane; j0 < G * (D / 4); j0 += 128) {
+      for (int j0 = lane; j0 < GV * (D / 4); j0 += 128) {
         float4 pv[4];
         if (join_pfx) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int j = j0 + 32 * u < G * (D / 4) ? j0 + 32 * u : 0;
+            const int j = j0 + 32 * u < GV * (D / 4) ? j0 + 32 * u : 0;
             const int h = j / (D / 4), d4 = j - h * (D / 4);
             pv[u] = __ldcg(reinterpret_cast<const float4*>(a.pre_o + (pre_row0 + h) * D) + d4);
           }
@@ -944,13 +972,13 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = j0 + 32 * u;
-          if (j >= G * (D / 4)) break;
+          if (j >= GV * (D / 4)) break;
           const int h = j / (D / 4), d4 = j - h * (D / 4);
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            const float sc = wsc[w * G + h];
-            const float4 v = *reinterpret_cast<const float4*>(co + (w * G + h) * CS + d4 * 4);
+          for (int r = 0; r < NWH; ++r) {
+            const float sc = wsc[r * GV + h];
+            const float4 v = *reinterpret_cast<const float4*>(co + cidx(r, h) * CS + d4 * 4);
             acc.x += sc * v.x;
             acc.y += sc * v.y;
             acc.z += sc * v.z;
@@ -974,11 +1002,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
             uint2 pk;
             pk.x = *reinterpret_cast<uint32_t*>(&lo2);
             pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * G + h) * D + d4 * 4) =
+            *reinterpret_cast<uint2*>(a.out + ((int64_t)b * a.H_q + g * GV + h) * D + d4 * 4) =
                 pk;
           } else {
-            *reinterpret_cast<float4*>(a.part_o + (pslot * G + h) * D + d4 * 4) = acc;
-            if (d4 == 0) a.part_lse[pslot * G + h] = merge_m[h];
+            *reinterpret_cast<float4*>(a.part_o + (pslot * GV + h) * D + d4 * 4) = acc;
+            if (d4 == 0) a.part_lse[pslot * GV + h] = merge_m[h];
           }
         }
       }
@@ -988,7 +1016,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
         // arrival counter: the CTA that delivers the last chunk of this
         // segment posts it to the merge queue (nobody waits here; the
         // counter is reset for the next call)
-        const int64_t seg = (int64_t)b * a.H_kv + g;
+        const int64_t seg = (int64_t)b * HV + g;
         __threadfence();
         __syncwarp();
         if (lane == 0) {
@@ -1015,11 +1043,11 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
   // every copy it issued.
   // segments with more than one chunk: each is posted exactly once (none:
   // the CTA ends here, touching no merge counter)
-  const int n_jobs = s_misc[1] * a.H_kv;
+  const int n_jobs = s_misc[1] * HV;
   if (n_jobs > 0) {
     block_sync();
     volatile int* s_job = s_misc + 2;  // [2]: queue index, segment
-    float* wts = reinterpret_cast<float*>(smem);  // [np * G] weights, then [2][G]
+    float* wts = reinterpret_cast<float*>(smem);  // [np * GV] weights, then [2][GV]
     bool mdead = false;
     while (true) {
       if (tid == 0) s_job[0] = atomicAdd(a.queue + 2, 1);
@@ -1046,8 +1074,8 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       block_sync();
       const int seg = s_job[1];
       if (seg < 0) break;
-      const int b = seg / a.H_kv, g = seg - b * a.H_kv;
-      const int nch = (s_nat[b + 1] - s_nat[b]) / a.H_kv;
+      const int b = seg / HV, g = seg - b * HV;
+      const int nch = (s_nat[b + 1] - s_nat[b]) / HV;
       const int64_t slot0 = (int64_t)s_nat[b] + (int64_t)g * nch;
       int L, klo, t_lo, t_hi, pfx;
       if (s_len) {
@@ -1058,31 +1086,31 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       }
       // the segment's chunks, plus the prefix partial as chunk nch (cascade)
       const int np = nch + pfx;
-      const int64_t row0 = (int64_t)b * a.H_q + g * G;
+      const int64_t row0 = (int64_t)b * a.H_q + g * GV;
       auto l_src = [&](int c, int h) -> const float* {
-        return c < nch ? a.part_lse + (slot0 + c) * G + h : a.pre_lse + row0 + h;
+        return c < nch ? a.part_lse + (slot0 + c) * GV + h : a.pre_lse + row0 + h;
       };
       auto o_src = [&](int c, int h) -> const float* {
-        return c < nch ? a.part_o + ((slot0 + c) * G + h) * D : a.pre_o + (row0 + h) * D;
+        return c < nch ? a.part_o + ((slot0 + c) * GV + h) * D : a.pre_o + (row0 + h) * D;
       };
-      const int nl = np * G;
-      float* wm = wts + nl;  // [G] max, [G] 1 / sum
-      for (int i = tid; i < nl; i += NT) wts[i] = __ldcg(l_src(i / G, i % G));
+      const int nl = np * GV;
+      float* wm = wts + nl;  // [GV] max, [GV] 1 / sum
+      for (int i = tid; i < nl; i += NT) wts[i] = __ldcg(l_src(i / GV, i % GV));
       block_sync();
-      if (tid < G) {  // per head: max and 1 / sum of the weights
+      if (tid < GV) {  // per head: max and 1 / sum of the weights
         const int h = tid;
         float M = -INFINITY, sum = 0.f;
-        for (int c = 0; c < np; ++c) M = fmaxf(M, wts[c * G + h]);
+        for (int c = 0; c < np; ++c) M = fmaxf(M, wts[c * GV + h]);
         if (M != -INFINITY)
-          for (int c = 0; c < np; ++c) sum += exp2f(wts[c * G + h] - M);
+          for (int c = 0; c < np; ++c) sum += exp2f(wts[c * GV + h] - M);
         wm[h] = M;
-        wm[G + h] = sum > 0.f ? 1.f / sum : 0.f;
+        wm[GV + h] = sum > 0.f ? 1.f / sum : 0.f;
       }
       block_sync();
       for (int i = tid; i < nl; i += NT) {
-        const int h = i % G;
+        const int h = i % GV;
         const float M = wm[h];
-        wts[i] = M == -INFINITY ? 0.f : exp2f(wts[i] - M) * wm[G + h];
+        wts[i] = M == -INFINITY ? 0.f : exp2f(wts[i] - M) * wm[GV + h];
       }
       block_sync();
       // weighted sum of the chunks' outputs, 4 dims (a slice) per load; each
@@ -1092,13 +1120,13 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       auto wsum = [&](auto s_c, auto mc_c) {
         constexpr int kS = decltype(s_c)::value, kMC = decltype(mc_c)::value;
         constexpr int Q4 = D / 4;
-        for (int j0 = tid; j0 < G * Q4; j0 += NT * kS) {
+        for (int j0 = tid; j0 < GV * Q4; j0 += NT * kS) {
           float4 acc[kS];
           int hh[kS], dd[kS];
 #pragma unroll
           for (int u = 0; u < kS; ++u) {
             acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int j = j0 + NT * u < G * Q4 ? j0 + NT * u : 0;
+            const int j = j0 + NT * u < GV * Q4 ? j0 + NT * u : 0;
             hh[u] = j / Q4;
             dd[u] = j - hh[u] * Q4;
           }
@@ -1115,7 +1143,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
             for (int u = 0; u < kS; ++u)
 #pragma unroll
               for (int cc = 0; cc < kMC; ++cc) {
-                const float w = c0 + cc < np ? wts[(c0 + cc) * G + hh[u]] : 0.f;
+                const float w = c0 + cc < np ? wts[(c0 + cc) * GV + hh[u]] : 0.f;
                 acc[u].x += w * v[u][cc].x;
                 acc[u].y += w * v[u][cc].y;
                 acc[u].z += w * v[u][cc].z;
@@ -1124,7 +1152,7 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           }
 #pragma unroll
           for (int u = 0; u < kS; ++u) {
-            if (j0 + NT * u >= G * Q4) continue;
+            if (j0 + NT * u >= GV * Q4) continue;
             __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
             __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
             uint2 pk;

@@ -43,7 +43,7 @@ static_assert(kMixThreads == 384, "three warpgroups");
 constexpr int kMixDecNW = PKV_MIX_DEC_NW;  // decode consumer warps (+ producer + epilogue)
 static_assert((kMixDecNW + 2) * 32 <= kMixThreads, "decode warps fit the block");
 
-template <int NSTAGE_DEC>
+template <int NSTAGE_DEC, int HP>
 __global__ void __launch_bounds__(kMixThreads, 1)
     mixed_step_kernel(const MixedArgs m, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmKv,
@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kMixThreads, 1)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
   if (m.has_dec && warp < kMixDecNW + 2)
-    decode_cta<kMixD, kMixDecNW, NSTAGE_DEC, true>(m.dec, tmKd, tmVd, smem, blockIdx.x);
+    decode_cta<kMixD, kMixDecNW, NSTAGE_DEC, true, false, HP>(m.dec, tmKd, tmVd, smem,
+                                                              blockIdx.x);
 }
 
 // CTAs that start with decode when the caller leaves the split open: the
@@ -75,7 +76,10 @@ static int mixed_decode_ctas(int num_sms, int64_t dec_batch, int64_t dec_max_seq
   double pairs_per_q = (double)max_seqlen_k - 0.5 * (double)max_seqlen_q;
   if (pairs_per_q < 1.0) pairs_per_q = 1.0;
   const double var_flops = (double)total_q * pairs_per_q * 4.0 * D * H_q;
-  const double hbm = 6.5e12, per_sm_bw = 55e9, per_sm_flops = 4.4e12;
+  // per-SM decode rate measured with 72 decode CTAs: ~73 GB/s with items of
+  // two kv heads, ~60 GB/s with one
+  const double per_sm_bw = decode_heads_per_item(D, H_kv, H_q / H_kv) == 2 ? 73e9 : 55e9;
+  const double hbm = 6.5e12, per_sm_flops = 4.4e12;
   for (int nd = 1; nd < num_sms; ++nd) {
     double bw = nd * per_sm_bw;
     if (bw > hbm) bw = hbm;
@@ -86,14 +90,16 @@ static int mixed_decode_ctas(int num_sms, int64_t dec_batch, int64_t dec_max_seq
   return num_sms - 1;
 }
 
-template <int NSTAGE_DEC>
+template <int NSTAGE_DEC, int HP>
 static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const void* k_cache,
                                   const void* v_cache, size_t smem, cudaStream_t stream,
                                   int num_sms) {
-  auto kern = mixed_step_kernel<NSTAGE_DEC>;
+  auto kern = mixed_step_kernel<NSTAGE_DEC, HP>;
   CUtensorMap tmKd, tmVd;
-  if (!encode_pool_map_groups(&tmKd, k_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile) ||
-      !encode_pool_map_groups(&tmVd, v_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile))
+  if (!encode_pool_map_groups(&tmKd, k_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile,
+                              0, HP) ||
+      !encode_pool_map_groups(&tmVd, v_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile,
+                              0, HP))
     return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
@@ -186,17 +192,29 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   // ---- shared memory: the larger of the two plans
   using VS = VarlenSmem<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS>;
   const size_t var_smem = m.has_var ? VS::bytes(v.batch, v.pairs_max) : 0;
-  const size_t dec24 = DecodePlan<kMixD, kMixDecNW, 24>(a.G, a.batch).total;
-  const size_t dec16 = DecodePlan<kMixD, kMixDecNW, 16>(a.G, a.batch).total;
   constexpr size_t kMax = 227 * 1024;
   if (var_smem > kMax) return cudaErrorNotSupported;
+  if (decode_heads_per_item(L.D, L.H_kv, a.G) == 2) {
+    // two kv heads per decode item: 12 stages of 16 KB, or 8
+    const size_t dec12 = DecodePlan<kMixD, kMixDecNW, 12, 2>(a.G, a.batch).total;
+    const size_t dec8 = DecodePlan<kMixD, kMixDecNW, 8, 2>(a.G, a.batch).total;
+    if (!m.has_dec || dec12 <= kMax) {
+      const size_t smem = var_smem > dec12 ? var_smem : dec12;
+      return launch_mixed_t<12, 2>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+    }
+    if (dec8 > kMax) return cudaErrorNotSupported;
+    const size_t smem = var_smem > dec8 ? var_smem : dec8;
+    return launch_mixed_t<8, 2>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+  }
+  const size_t dec24 = DecodePlan<kMixD, kMixDecNW, 24>(a.G, a.batch).total;
+  const size_t dec16 = DecodePlan<kMixD, kMixDecNW, 16>(a.G, a.batch).total;
   if (!m.has_dec || dec24 <= kMax) {
     const size_t smem = var_smem > dec24 ? var_smem : dec24;
-    return launch_mixed_t<24>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+    return launch_mixed_t<24, 1>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
   }
   if (dec16 > kMax) return cudaErrorNotSupported;
   const size_t smem = var_smem > dec16 ? var_smem : dec16;
-  return launch_mixed_t<16>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
+  return launch_mixed_t<16, 1>(m, vmaps, L.k_cache, L.v_cache, smem, stream, num_sms);
 }
 
 }  // namespace pkv

@@ -38,15 +38,19 @@ inline EncodeTiledFn encode_fn() {
 // boxes of a tile.
 // box_cols: the columns one box covers (a multiple of 64, default all D):
 // a box then lands as [row group][box_cols/64 chunks][8 rows][128 bytes].
+// heads: consecutive kv heads of the page in one box (the outermost box
+// dimension): the box lands as [head][row group][chunk][8 rows][128 bytes].
 inline bool encode_pool_map_groups(CUtensorMap* m, const void* base, int D, int P,
-                                   int64_t num_pages, int H_kv, int rows, int box_cols = 0) {
+                                   int64_t num_pages, int H_kv, int rows, int box_cols = 0,
+                                   int heads = 1) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   if (box_cols <= 0) box_cols = D;
   cuuint64_t dims[5] = {64, 8, (cuuint64_t)(D / 64), (cuuint64_t)(P / 8),
                         (cuuint64_t)(num_pages * H_kv)};
   cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)8 * D * 2, (cuuint64_t)P * D * 2};
-  cuuint32_t box[5] = {64, 8, (cuuint32_t)(box_cols / 64), (cuuint32_t)(rows / 8), 1};
+  cuuint32_t box[5] = {64, 8, (cuuint32_t)(box_cols / 64), (cuuint32_t)(rows / 8),
+                       (cuuint32_t)heads};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -117,11 +117,13 @@ def test_mixed_step_twice_on_one_workspace(pkv, mixed_case):
     assert np.array_equal(bf16_dev_to_bits(op1), bf16_dev_to_bits(op2))
 
 
-def test_mixed_step_small(pkv):
-    """A small mixed step (2 prefill chunks, 8 decode rows, 4/2/128 heads)
-    with the split at 3 decode-first CTAs."""
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (8, 1), (12, 3), (4, 4)])
+def test_mixed_step_small(pkv, H_q, H_kv):
+    """A small mixed step (2 prefill chunks, 8 decode rows) with the split at
+    3 decode-first CTAs: decode items of two kv heads (8/2, 4/4) and of one
+    (a group of 8; an odd kv-head count)."""
     import torch
-    step = wl.mixed_step(n_chunks=2, n_dec=8, H_q=8, H_kv=2, num_pages=2048)
+    step = wl.mixed_step(n_chunks=2, n_dec=8, H_q=H_q, H_kv=H_kv, num_pages=2048)
     vals = wl.fill_values(step, 11)
     kc, vc = to_dev_bf16(vals.k_cache), to_dev_bf16(vals.v_cache)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")

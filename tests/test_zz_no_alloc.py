@@ -54,16 +54,19 @@ def _case(seed, B, long_len, H_q=32, H_kv=8, D=128, P=16):
     return q, kc, vc, bt, lens
 
 
-def _longest_segment_is_split(lens, H_kv, P, n_sms, D):
-    """The decode kernel cuts a (sequence, kv head) segment into chunks when
-    it has more 16-key tiles than half of one CTA's share of the batch's
-    tiles (one persistent CTA per SM) and more than 16, and the longest
-    segment exceeds that cut by more than a merge's cost (480 KB of K+V,
-    64*D bytes per tile)."""
+def _longest_segment_is_split(lens, H_q, H_kv, P, n_sms, D):
+    """The decode kernel cuts a segment (a sequence and its HP kv heads: two
+    at head_dim 128 with an even kv-head count and a GQA group of at most 4,
+    else one) into chunks when it has more 16-key tiles than half of one
+    CTA's share of the batch's item tiles (one persistent CTA per SM) and
+    more than 16, and the longest segment exceeds that cut by more than a
+    merge's cost (480 KB of K+V, 64*D*HP bytes per item tile)."""
+    G = H_q // H_kv
+    hp = 2 if (D == 128 and H_kv % 2 == 0 and G <= 4) else 1
     tiles = -(-lens.astype(np.int64) // 16)
-    half_share = -(-int(tiles.sum()) * H_kv // (2 * n_sms))
+    half_share = -(-int(tiles.sum()) * (H_kv // hp) // (2 * n_sms))
     cut = max(16, half_share)
-    return int(tiles.max()) > cut + (480 * 1024) // (64 * D)
+    return int(tiles.max()) > cut + (480 * 1024) // (64 * D * hp)
 
 
 def _args(out, q, kc, vc, bt, lens, scale):
@@ -81,7 +84,8 @@ def test_static_scratch_decode_matches_oracle_and_workspace_decode_twice(lib):
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     for call, (seed, B, long_len) in enumerate([(101, 64, 20000), (202, 23, 9000)]):
         q, kc, vc, bt, lens = _case(seed, B, long_len)
-        assert _longest_segment_is_split(lens, kc.shape[1], kc.shape[2], n_sms, q.shape[2])
+        assert _longest_segment_is_split(lens, q.shape[1], kc.shape[1], kc.shape[2], n_sms,
+                                         q.shape[2])
         qd, kd, vd = to_dev_bf16(q), to_dev_bf16(kc), to_dev_bf16(vc)
         btd, ld = to_dev(bt), to_dev(lens)
         scale = 1.0 / np.sqrt(q.shape[2])
