@@ -930,18 +930,23 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
       // warps (h / G) * NWH + r): weight of each warp's state, 1/l,
       // log2-sum-exp
       float* wsc = epi_w;  // [NWH][GV] scratch
-      auto cidx = [&](int r, int h) { return ((h / G) * NWH + r) * G + (h % G); };
+      // state of row h from its head's r-th warp: hbase(h) + r * G
+      auto hbase = [&](int h) -> int {
+        if (HP == 1) return h;
+        return (h / G) * NWH * G + (h % G);
+      };
       if (lane < GV) {
         const int h = lane;
+        const int hb = hbase(h);
         float M = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < NWH; ++r) M = fmaxf(M, cml[cidx(r, h) * 2]);
+        for (int r = 0; r < NWH; ++r) M = fmaxf(M, cml[(hb + r * G) * 2]);
         float lsum = 0.f;
 #pragma unroll
         for (int r = 0; r < NWH; ++r) {
-          const float sc = M == -INFINITY ? 0.f : exp2f(cml[cidx(r, h) * 2] - M);
+          const float sc = M == -INFINITY ? 0.f : exp2f(cml[(hb + r * G) * 2] - M);
           wsc[r * GV + h] = sc;
-          lsum += sc * cml[cidx(r, h) * 2 + 1];
+          lsum += sc * cml[(hb + r * G) * 2 + 1];
         }
         merge_m[h] = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
         merge_inv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -974,11 +979,12 @@ __device__ __forceinline__ void decode_cta(const DecodeArgs& a, const CUtensorMa
           const int j = j0 + 32 * u;
           if (j >= GV * (D / 4)) break;
           const int h = j / (D / 4), d4 = j - h * (D / 4);
+          const float* cor = co + hbase(h) * CS + d4 * 4;
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int r = 0; r < NWH; ++r) {
             const float sc = wsc[r * GV + h];
-            const float4 v = *reinterpret_cast<const float4*>(co + cidx(r, h) * CS + d4 * 4);
+            const float4 v = *reinterpret_cast<const float4*>(cor + r * G * CS);
             acc.x += sc * v.x;
             acc.y += sc * v.y;
             acc.z += sc * v.z;
