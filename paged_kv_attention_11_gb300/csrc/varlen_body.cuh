@@ -706,7 +706,9 @@ __device__ __forceinline__ void varlen_cta(const VarlenArgs& a, const CUtensorMa
             // the first half of the S row is dead, to keep registers free
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {  // O *= alpha (warp-collective)
               const uint64_t al2 = f2(alpha, alpha);
-#pragma unroll
+              // rare (the running max grew by more than 2^8): kept rolled,
+              // so that the tile loop's code stays small
+#pragma unroll 1
               for (int c = 0; c < DV / 32; ++c) {
                 uint32_t o[32];
                 tc::ld_32x32b_x32(o_addr + c * 32, o);
