@@ -57,9 +57,9 @@ _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcg
 TRAFFIC = {
     "decode_qwen3": (320_301_824, _DEC_SRC, "94e78b36e07b1b4e"),
     "decode_d512": (573_872_640, _DEC_SRC, "94e78b36e07b1b4e"),
-    "varlen_mixed": (92_761_600, _VAR_SRC, "673a7df588a8d73b"),
-    "varlen_d512": (43_810_304, _VAR_SRC, "673a7df588a8d73b"),
-    "mixed_single": (1_249_686_016, _MIX_SRC, "f7eb1e3d38a81b49"),
+    "varlen_mixed": (91_294_464, _VAR_SRC, "36237ec41593b2d7"),
+    "varlen_d512": (44_015_616, _VAR_SRC, "36237ec41593b2d7"),
+    "mixed_single": (1_221_445_888, _MIX_SRC, "08bda397fa47bc44"),
     "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
     "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4b03849b8c981063"),
 }
