@@ -134,3 +134,22 @@ def test_mixed_step_small(pkv, H_q, H_kv):
     wd, wp = _want(step, vals, hk, hv)
     assert_close_attn(bf16_dev_to_f64(od), wd, "small mixed decode")
     assert_close_attn(bf16_dev_to_f64(op), wp, "small mixed prefill")
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(12, 4), (6, 2), (24, 8)])
+def test_mixed_decode_only_group_of_three(pkv, H_q, H_kv):
+    """Decode rows alone through the one-launch path with a GQA group of 3
+    (query rows of two kv heads per item: 6); the longest rows (up to 4096
+    keys against a share of ~20-40 tiles per CTA) are cut and merged."""
+    import torch
+    step = wl.mixed_step(n_chunks=2, n_dec=24, H_q=H_q, H_kv=H_kv, num_pages=8192)
+    vals = wl.fill_values(step, 13)
+    kc, vc = to_dev_bf16(vals.k_cache), to_dev_bf16(vals.v_cache)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_kv_append(to_dev_bf16(vals.k_new), to_dev_bf16(vals.v_new), kc, vc,
+                        to_dev(step.all_slots), err_flag=err)
+    hk, hv = oracle.kv_append(vals.k_cache, vals.v_cache, vals.k_new, vals.v_new, step.all_slots)
+    od, _ = _run(pkv, step, vals, kc, vc, pre=False)
+    wd = oracle.paged_decode(vals.q_dec[0], hk, hv, step.dec_block_table, step.dec_seq_lens,
+                             step.scale)
+    assert_close_attn(bf16_dev_to_f64(od), wd, f"mixed decode-only {H_q}/{H_kv}")
