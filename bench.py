@@ -714,6 +714,7 @@ def run_mixed(args, device, stream, flush, rank):
                                 "traffic": traffic_bytes("append_mixed"),
                                 "note": "the phase between two graph events: the launch is inside"},
             "single_launch": fused,
+            "single_launch_append": fused_app,
             "with_rope": with_rope}
 
 

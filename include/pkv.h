@@ -301,6 +301,39 @@ pkv_status paged_attn_mixed(void* dec_out, const void* dec_q,
                             int32_t* err_flag, void* stream);
 
 /*
+ * paged_attn_mixed_append - paged_attn_mixed with the step's append fused
+ * in: the same result as paged_kv_append(k_new, v_new, slot_mapping)
+ * followed by paged_attn_mixed, in one launch (the engine's in-kernel
+ * k_cache[addr] = k_val write: scripts/benchmarks commit log, "Files").
+ *
+ *   k_new, v_new    [num_new_tokens, num_kv_heads, head_dim] bf16 (read),
+ *                   16-byte aligned: the step's new rows (decode rows' and
+ *                   prefill chunks' tokens alike)
+ *   slot_mapping    [num_new_tokens] int64 (device): page * page_size + row;
+ *                   negative: skip; past the pool: skipped, PKV_DEVERR_SLOT
+ *   k_cache, v_cache  the pools, written at the slots, then read
+ *   workspace       required whenever num_new_tokens > 0 (the launch's grid
+ *                   barrier keeps two counters in it), at least
+ *                   paged_attn_decode_workspace_size(dec_batch, ...) bytes
+ *   every other argument as paged_attn_mixed.
+ *
+ * Every CTA of the launch appends a slice of the rows, then all CTAs meet
+ * at a grid barrier (one CTA per SM, all resident; a wait that does not
+ * end within 2 s raises PKV_DEVERR_TIMEOUT) before any of them reads a
+ * pool.  Slots must be distinct, as for paged_kv_append.
+ */
+pkv_status paged_attn_mixed_append(
+    void* dec_out, const void* dec_q, const int32_t* dec_block_table,
+    int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens, int32_t dec_batch,
+    int32_t dec_max_seq_len, void* pre_out, const void* pre_q, const int32_t* cu_seq_lens_q,
+    const int32_t* cu_seq_lens_k, const int32_t* pre_block_table, int32_t pre_max_blocks_per_seq,
+    int32_t pre_batch, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, int32_t num_new_tokens,
+    void* k_cache, void* v_cache, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t page_size, int64_t num_pages, float scale, int32_t window, int32_t decode_ctas,
+    void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
  * paged_attn_decode_static - paged_attn_decode for callers that cannot
  * allocate device memory.  (Not an operation of the pages: it exists for
  * callers of this library that may not call cudaMalloc on the attention

@@ -8,7 +8,8 @@ Three calls, same names as the C ABI (include/pkv.h):
 
 plus ``paged_attn_decode_append`` (the decode step with its append in the
 same launch), ``paged_attn_mixed`` (a step's decode rows and prefill chunks
-in one launch), ``paged_attn_decode_shared_prefix`` (decode that reads a prefix
+in one launch), ``paged_attn_mixed_append`` (the same with the step's append
+fused in), ``paged_attn_decode_shared_prefix`` (decode that reads a prefix
 shared by a group of sequences once per group), ``paged_kv_append_rope`` (the
 append with q/k RMSNorm and the rotary embedding fused in) and
 ``rope_table`` (its cos/sin table).
@@ -34,6 +35,7 @@ from ._binding import (  # noqa: F401
     paged_attn_decode_shared_prefix,
     paged_attn_decode_static,
     paged_attn_mixed,
+    paged_attn_mixed_append,
     paged_attn_varlen,
     paged_kv_append,
     paged_kv_append_rope,

@@ -42,6 +42,10 @@ _SIGS = {
                          _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i32,
                          _c_i32, _c_i32, _c_i32, _c_i64, _c_f, _c_i32, _c_i32, _c_p,
                          ctypes.c_size_t, _c_p, _c_p],
+    "paged_attn_mixed_append": [_c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_p,
+                                _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p,
+                                _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64,
+                                _c_f, _c_i32, _c_i32, _c_p, ctypes.c_size_t, _c_p, _c_p],
     "pkv_rope_table": [_c_p, _c_i32, _c_i32, ctypes.c_double, _c_p],
     "paged_kv_append_rope": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p,
                              _c_f, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_p, _c_p],
@@ -299,6 +303,45 @@ def paged_attn_mixed(dec_out: torch.Tensor, dec_q: torch.Tensor, dec_block_table
         _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), _ptr(pre_block_table),
         pre_block_table.shape[1], cu_seq_lens_q.shape[0] - 1, int(max_seqlen_q),
         int(max_seqlen_k), total_q, _ptr(k_cache), _ptr(v_cache), H_q, H_kv, D, P, num_pages,
+        float(scale), int(window), int(decode_ctas), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(stream)))
+
+
+def paged_attn_mixed_append(dec_out: torch.Tensor, dec_q: torch.Tensor,
+                            dec_block_table: torch.Tensor, dec_seq_lens: torch.Tensor,
+                            dec_max_seq_len: int, pre_out: torch.Tensor, pre_q: torch.Tensor,
+                            cu_seq_lens_q: torch.Tensor, cu_seq_lens_k: torch.Tensor,
+                            pre_block_table: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                            k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float,
+                            window: int = 0, decode_ctas: int = 0,
+                            workspace: Optional[torch.Tensor] = None,
+                            err_flag: Optional[torch.Tensor] = None, stream=None):
+    """paged_attn_mixed with the step's append (k_new/v_new [T, H_kv, D],
+    slot_mapping [T] int64) in the same launch."""
+    for n, t in (("dec_out", dec_out), ("dec_q", dec_q), ("pre_out", pre_out),
+                 ("pre_q", pre_q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                 ("v_cache", v_cache)):
+        _bf16(t, n)
+    for n, t in (("dec_block_table", dec_block_table), ("dec_seq_lens", dec_seq_lens),
+                 ("cu_seq_lens_q", cu_seq_lens_q), ("cu_seq_lens_k", cu_seq_lens_k),
+                 ("pre_block_table", pre_block_table)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{n} must be int32")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    B, H_q, D = dec_q.shape
+    total_q = pre_q.shape[0]
+    num_pages, H_kv, P, _ = k_cache.shape
+    if workspace is None:
+        workspace = decode_workspace(dec_q.device, _stream(stream), max(B, 1), H_q, H_kv, D)
+    _check("paged_attn_mixed_append", lib().paged_attn_mixed_append(
+        _ptr(dec_out), _ptr(dec_q), _ptr(dec_block_table), dec_block_table.shape[1],
+        _ptr(dec_seq_lens), B, int(dec_max_seq_len), _ptr(pre_out), _ptr(pre_q),
+        _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), _ptr(pre_block_table),
+        pre_block_table.shape[1], cu_seq_lens_q.shape[0] - 1, int(max_seqlen_q),
+        int(max_seqlen_k), total_q, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+        k_new.shape[0], _ptr(k_cache), _ptr(v_cache), H_q, H_kv, D, P, num_pages,
         float(scale), int(window), int(decode_ctas), _ptr(workspace), workspace.numel(),
         _ptr(err_flag), _stream(stream)))
 

@@ -277,7 +277,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, const void* k_cache, cons
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
-pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec_block_table,
+static pkv_status mixed_impl(void* dec_out, const void* dec_q, const int32_t* dec_block_table,
                             int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens,
                             int32_t dec_batch, int32_t dec_max_seq_len, void* pre_out,
                             const void* pre_q, const int32_t* cu_seq_lens_q,
@@ -288,7 +288,8 @@ pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec
                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                             int64_t num_pages, float scale, int32_t window, int32_t decode_ctas,
                             void* workspace, size_t workspace_bytes, int32_t* err_flag,
-                            void* stream) {
+                            void* stream, const void* k_new, const void* v_new,
+                            const int64_t* slot_mapping, int32_t num_new) {
   if (dec_batch < 0 || pre_batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
     return PKV_ERR_INVALID;
   if (!(scale >= 0.f)) return PKV_ERR_INVALID;  // NaN or negative
@@ -311,12 +312,20 @@ pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec
   }
   if (head_dim != 128 || (128 % page_size != 0 && page_size % 128 != 0))
     return PKV_ERR_UNSUPPORTED;
-  if (dec_batch == 0 && !has_var) return PKV_OK;
+  if (num_new < 0) return PKV_ERR_INVALID;
+  if (num_new > 0) {
+    // the new rows and their slots; the grid barrier's counters live in the
+    // workspace, which every appending call needs
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
+      return PKV_ERR_INVALID;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PKV_ERR_INVALID;
+  }
+  if (dec_batch == 0 && !has_var && num_new == 0) return PKV_OK;
   if (dec_batch > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return PKV_ERR_INVALID;
   int sms = 0;
   if (int e = num_sms_current(&sms)) return cuda_fail((cudaError_t)e);
-  if (dec_batch > 0 &&
+  if ((dec_batch > 0 || num_new > 0) &&
       workspace_bytes <
           pkv::decode_workspace_bytes(dec_batch, num_q_heads, num_kv_heads, head_dim, sms))
     return PKV_ERR_INVALID;
@@ -363,9 +372,52 @@ pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec
   L.workspace = workspace;
   L.workspace_bytes = workspace_bytes;
   L.err = err_flag;
+  L.k_new = k_new;
+  L.v_new = v_new;
+  L.slot_mapping = slot_mapping;
+  L.num_new = num_new;
   cudaError_t e = pkv::launch_mixed(L, maps, static_cast<cudaStream_t>(stream), sms);
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+pkv_status paged_attn_mixed(void* dec_out, const void* dec_q, const int32_t* dec_block_table,
+                            int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens,
+                            int32_t dec_batch, int32_t dec_max_seq_len, void* pre_out,
+                            const void* pre_q, const int32_t* cu_seq_lens_q,
+                            const int32_t* cu_seq_lens_k, const int32_t* pre_block_table,
+                            int32_t pre_max_blocks_per_seq, int32_t pre_batch,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+                            const void* k_cache, const void* v_cache, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                            int64_t num_pages, float scale, int32_t window, int32_t decode_ctas,
+                            void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                            void* stream) {
+  return mixed_impl(dec_out, dec_q, dec_block_table, dec_max_blocks_per_seq, dec_seq_lens,
+                    dec_batch, dec_max_seq_len, pre_out, pre_q, cu_seq_lens_q, cu_seq_lens_k,
+                    pre_block_table, pre_max_blocks_per_seq, pre_batch, max_seqlen_q,
+                    max_seqlen_k, total_q, k_cache, v_cache, num_q_heads, num_kv_heads,
+                    head_dim, page_size, num_pages, scale, window, decode_ctas, workspace,
+                    workspace_bytes, err_flag, stream, nullptr, nullptr, nullptr, 0);
+}
+
+pkv_status paged_attn_mixed_append(
+    void* dec_out, const void* dec_q, const int32_t* dec_block_table,
+    int32_t dec_max_blocks_per_seq, const int32_t* dec_seq_lens, int32_t dec_batch,
+    int32_t dec_max_seq_len, void* pre_out, const void* pre_q, const int32_t* cu_seq_lens_q,
+    const int32_t* cu_seq_lens_k, const int32_t* pre_block_table, int32_t pre_max_blocks_per_seq,
+    int32_t pre_batch, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t total_q,
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, int32_t num_new_tokens,
+    void* k_cache, void* v_cache, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t page_size, int64_t num_pages, float scale, int32_t window, int32_t decode_ctas,
+    void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return mixed_impl(dec_out, dec_q, dec_block_table, dec_max_blocks_per_seq, dec_seq_lens,
+                    dec_batch, dec_max_seq_len, pre_out, pre_q, cu_seq_lens_q, cu_seq_lens_k,
+                    pre_block_table, pre_max_blocks_per_seq, pre_batch, max_seqlen_q,
+                    max_seqlen_k, total_q, k_cache, v_cache, num_q_heads, num_kv_heads,
+                    head_dim, page_size, num_pages, scale, window, decode_ctas, workspace,
+                    workspace_bytes, err_flag, stream, k_new, v_new, slot_mapping,
+                    num_new_tokens);
 }
 
 pkv_status pkv_rope_table(float* cos_sin, int32_t max_position, int32_t head_dim,

@@ -138,6 +138,12 @@ struct MixedLaunch {
   void* workspace;
   size_t workspace_bytes;
   int32_t* err;
+  // the fused append (paged_attn_mixed_append): num_new tokens' K/V rows
+  // ([num_new, H_kv, D]) to the pools at slot_mapping; num_new = 0: none
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  int32_t num_new;
 };
 
 // keys per KV tile of the varlen kernel for a head_dim (page_size must

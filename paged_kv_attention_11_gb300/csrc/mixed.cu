@@ -19,6 +19,11 @@
 // and the zero rows of empty sequences work as in paged_attn_decode.  No
 // warp moves registers (setmaxnreg): both bodies run in the launch's 168 per
 // thread.
+//
+// paged_attn_mixed_append also writes the step's new K/V rows first: every
+// CTA appends a slice of them (a warp per token, as paged_kv_append), then
+// all CTAs meet at a grid barrier (every CTA is resident: one per SM; the
+// wait is bounded) before any work reads the pools.
 #include "decode_body.cuh"
 #include "tmap.h"
 #include "varlen_body.cuh"
@@ -28,6 +33,17 @@ namespace pkv {
 struct MixedArgs {
   DecodeArgs dec;
   VarlenArgs var;
+  // the fused append (num_new > 0): rows of num_new tokens, vpt 16-byte
+  // vectors each, to the pools at slot_mapping; bar: two grid-barrier
+  // counters in the workspace (zero between calls)
+  const uint4* k_new;
+  const uint4* v_new;
+  uint4* k_pool;
+  uint4* v_pool;
+  const int64_t* slot_mapping;
+  int64_t num_slots;
+  int32_t num_new, vpt, vpr;
+  int32_t* bar;
   int32_t has_dec, has_var;
   int32_t var_first;  // first CTA that starts with the prefill
 };
@@ -43,6 +59,74 @@ static_assert(kMixThreads == 384, "three warpgroups");
 constexpr int kMixDecNW = PKV_MIX_DEC_NW;  // decode consumer warps (+ producer + epilogue)
 static_assert((kMixDecNW + 2) * 32 <= kMixThreads, "decode warps fit the block");
 
+// The step's new rows, a warp per token (4 vectors of K and of V per lane per
+// pass), then the grid barrier.
+__device__ __forceinline__ void mixed_append_rows(const MixedArgs& m) {
+  pdl_wait();  // the rows may come from the previous kernel
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int nw = gridDim.x * wpb;
+  const int P = m.dec.P, H_kv = m.dec.H_kv;
+  const int hstride = P * m.vpr;
+  for (int tok = blockIdx.x * wpb + (threadIdx.x >> 5); tok < m.num_new; tok += nw) {
+    const int64_t slot = __ldg(m.slot_mapping + tok);
+    const int64_t src0 = (int64_t)tok * m.vpt;
+    for (int v0 = 0; v0 < m.vpt; v0 += 128) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + lane + 32 * j;
+        if (v < m.vpt) {
+          kv[j] = __ldg(m.k_new + src0 + v);
+          vv[j] = __ldg(m.v_new + src0 + v);
+        }
+      }
+      if (slot < 0) continue;  // padding row
+      if (slot >= m.num_slots) {
+        if (lane == 0 && v0 == 0) raise_err(m.dec.err, PKV_DEVERR_SLOT);
+        continue;
+      }
+      const int64_t page = slot / P;
+      const int row = (int)(slot - page * P);
+      uint4* kd = m.k_pool + (page * H_kv * P + row) * m.vpr;
+      uint4* vd = m.v_pool + (kd - m.k_pool);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + lane + 32 * j;
+        if (v < m.vpt) {
+          const int h = v / m.vpr;
+          const int off = h * hstride + (v - h * m.vpr);
+          kd[off] = kv[j];
+          vd[off] = vv[j];
+        }
+      }
+    }
+  }
+  // the rows are read by TMA (the async proxy) in every CTA
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(m.bar, 1);
+    const unsigned long long t0 = globaltimer();
+    while (ld_volatile_i32(m.bar) < (int)gridDim.x) {
+      __nanosleep(32);
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        raise_err(m.dec.err, PKV_DEVERR_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+    // the last CTA past the wait resets both counters for the next call
+    if (atomicAdd(m.bar + 1, 1) == (int)gridDim.x - 1) {
+      m.bar[0] = 0;
+      m.bar[1] = 0;
+    }
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 template <int NSTAGE_DEC, int HP>
 __global__ void __launch_bounds__(kMixThreads, 1)
     mixed_step_kernel(const MixedArgs m, const __grid_constant__ CUtensorMap tmQ,
@@ -55,6 +139,7 @@ __global__ void __launch_bounds__(kMixThreads, 1)
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int nd = m.var_first;
+  if (m.num_new > 0) mixed_append_rows(m);
   if (m.has_var && (int)blockIdx.x >= nd)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
@@ -153,6 +238,17 @@ cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStre
   a.pre_lse = nullptr;
   a.err = L.err;
   decode_workspace_split(a, L.workspace, L.workspace_bytes, L.dec_batch, L.H_kv, L.D, num_sms);
+  // ---- the fused append (paged_attn_mixed_append)
+  m.num_new = L.num_new > 0 ? L.num_new : 0;
+  m.k_new = static_cast<const uint4*>(L.k_new);
+  m.v_new = static_cast<const uint4*>(L.v_new);
+  m.k_pool = static_cast<uint4*>(const_cast<void*>(L.k_cache));
+  m.v_pool = static_cast<uint4*>(const_cast<void*>(L.v_cache));
+  m.slot_mapping = L.slot_mapping;
+  m.num_slots = L.num_pages * L.P;
+  m.vpr = L.D / 8;
+  m.vpt = L.H_kv * m.vpr;
+  m.bar = a.queue + 5;  // queue[5..6]: free slots of the decode workspace's counters
   // ---- prefill arguments (as launch_varlen)
   VarlenArgs& v = m.var;
   const int QP = 128 / a.G;

@@ -208,3 +208,21 @@ def test_decode_append_validates_on_host(lib):
     assert call(scale=float("nan")) == 1
     assert call(D=96) == 2                 # head_dim outside the decode shapes
     assert call(B=0, kn=None, vn=None) == 0  # empty batch: no-op
+
+
+def test_mixed_append_validates_on_host(lib):
+    L = _bind(lib)
+    P = 0x1000  # fake, never dereferenced: validation fails first
+
+    def call(kn=P, vn=P, sm=P, T=16, ws=P, D=128, H_q=32, B=8):
+        return L.paged_attn_mixed_append(
+            P, P, P, 4, P, B, 64, P, P, P, P, P, 4, 2, 64, 128, 100,
+            kn, vn, sm, T, P, P, H_q, 8, D, 16, 64, 0.1, 0, 0, ws, 1 << 24, None, None)
+    assert call(kn=None) == 1              # missing new K rows
+    assert call(vn=P + 8) == 1             # misaligned new V rows
+    assert call(sm=None) == 1              # missing slot mapping
+    assert call(T=-1) == 1                 # negative token count
+    assert call(ws=None) == 1              # appending needs the workspace (grid barrier)
+    assert call(ws=P + 64) == 1            # workspace not 256-byte aligned
+    assert call(H_q=30) == 1               # H_q not a multiple of H_kv
+    assert call(D=64) == 2                 # head_dim other than 128
