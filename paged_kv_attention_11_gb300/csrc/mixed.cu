@@ -59,45 +59,62 @@ static_assert(kMixThreads == 384, "three warpgroups");
 constexpr int kMixDecNW = PKV_MIX_DEC_NW;  // decode consumer warps (+ producer + epilogue)
 static_assert((kMixDecNW + 2) * 32 <= kMixThreads, "decode warps fit the block");
 
-// The step's new rows, a warp per token (4 vectors of K and of V per lane per
-// pass), then the grid barrier.
+// The step's new rows: a warp takes kMixTokPerPass tokens at once (4
+// vectors of K and of V per lane per token), so that a prefill-sized step's
+// reads are all in flight together on the launch's 12 warps per SM; then
+// the grid barrier.
+constexpr int kMixTokPerPass = 4;
 __device__ __forceinline__ void mixed_append_rows(const MixedArgs& m) {
   pdl_wait();  // the rows may come from the previous kernel
+  constexpr int TP = kMixTokPerPass;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int nw = gridDim.x * wpb;
   const int P = m.dec.P, H_kv = m.dec.H_kv;
   const int hstride = P * m.vpr;
-  for (int tok = blockIdx.x * wpb + (threadIdx.x >> 5); tok < m.num_new; tok += nw) {
-    const int64_t slot = __ldg(m.slot_mapping + tok);
-    const int64_t src0 = (int64_t)tok * m.vpt;
-    for (int v0 = 0; v0 < m.vpt; v0 += 128) {
-      uint4 kv[4], vv[4];
+  // warp w takes tokens w + (k * TP + i) * nw, i < TP, in pass k
+  for (int tok0 = blockIdx.x * wpb + (threadIdx.x >> 5); tok0 < m.num_new; tok0 += nw * TP) {
+    int64_t slot[TP];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int v = v0 + lane + 32 * j;
-        if (v < m.vpt) {
-          kv[j] = __ldg(m.k_new + src0 + v);
-          vv[j] = __ldg(m.v_new + src0 + v);
+    for (int i = 0; i < TP; ++i) {
+      const int tok = tok0 + i * nw;
+      slot[i] = tok < m.num_new ? __ldg(m.slot_mapping + tok) : -1;
+    }
+    for (int v0 = 0; v0 < m.vpt; v0 += 128) {
+      uint4 kv[TP][4], vv[TP][4];
+#pragma unroll
+      for (int i = 0; i < TP; ++i) {
+        const int tok = tok0 + i * nw;
+        const int64_t src0 = (int64_t)tok * m.vpt;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int v = v0 + lane + 32 * j;
+          if (tok < m.num_new && v < m.vpt) {
+            kv[i][j] = __ldg(m.k_new + src0 + v);
+            vv[i][j] = __ldg(m.v_new + src0 + v);
+          }
         }
       }
-      if (slot < 0) continue;  // padding row
-      if (slot >= m.num_slots) {
-        if (lane == 0 && v0 == 0) raise_err(m.dec.err, PKV_DEVERR_SLOT);
-        continue;
-      }
-      const int64_t page = slot / P;
-      const int row = (int)(slot - page * P);
-      uint4* kd = m.k_pool + (page * H_kv * P + row) * m.vpr;
-      uint4* vd = m.v_pool + (kd - m.k_pool);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int v = v0 + lane + 32 * j;
-        if (v < m.vpt) {
-          const int h = v / m.vpr;
-          const int off = h * hstride + (v - h * m.vpr);
-          kd[off] = kv[j];
-          vd[off] = vv[j];
+      for (int i = 0; i < TP; ++i) {
+        if (slot[i] < 0) continue;  // padding row, or no token
+        if (slot[i] >= m.num_slots) {
+          if (lane == 0 && v0 == 0) raise_err(m.dec.err, PKV_DEVERR_SLOT);
+          continue;
+        }
+        const int64_t page = slot[i] / P;
+        const int row = (int)(slot[i] - page * P);
+        uint4* kd = m.k_pool + (page * H_kv * P + row) * m.vpr;
+        uint4* vd = m.v_pool + (kd - m.k_pool);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int v = v0 + lane + 32 * j;
+          if (v < m.vpt) {
+            const int h = v / m.vpr;
+            const int off = h * hstride + (v - h * m.vpr);
+            kd[off] = kv[i][j];
+            vd[off] = vv[i][j];
+          }
         }
       }
     }
