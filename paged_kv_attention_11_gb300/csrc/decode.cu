@@ -149,6 +149,18 @@ template <int D, bool APPEND>
 static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void* v_cache,
                                    int max_seq_len, cudaStream_t stream, int num_sms) {
   using C = DecodeCfg<D>;
+  if constexpr (D == 256) {
+    // A small call (at most ~1 MB of K/V per SM: a few windows or short
+    // rows) runs at the per-SM streaming rate, not HBM's: 2 consumer warps
+    // and 10 stages of 16 KB (160 KB in flight) beat 4 warps and 8 stages
+    // there (sliding-window decode, 32 rows of a 512-key window: 20.5 vs
+    // 22.5 us).  Larger calls keep 4 consumer warps.
+    const int64_t keys = (a.window > 0 && a.window < max_seq_len) ? a.window : max_seq_len;
+    const int64_t bytes = (int64_t)a.batch * a.H_kv * keys * D * 4;
+    if (bytes <= ((int64_t)num_sms << 20) && decode_fits<D, 2, 10>(a))
+      return launch_decode_s<D, 2, 10, APPEND>(a, k_cache, v_cache, max_seq_len, stream,
+                                                num_sms);
+  }
   // One kv head per item here: with every SM streaming, the decode runs at
   // HBM's rate either way, and items of one head balance the grid better
   // (two-head items made the schedule cut the longest sequences of the

@@ -114,6 +114,19 @@ def test_decode_shapes(pkv, D, H, P):
     assert np.all(got[lens.index(0)] == 0)
 
 
+def test_decode_head_dim_256_large_call(pkv):
+    """head_dim 256 above the small-call size (more than ~1 MB of K/V per
+    SM): the launch with 4 consumer warps and 8 stages."""
+    rng = np.random.default_rng(256)
+    lens = list(rng.integers(1, 2048, size=24))
+    lens[0] = 2048
+    q, kc, vc, bt, L = _random_case(rng, len(lens), 8, 4, 256, 16, lens)
+    out, err = _decode(pkv, q, kc, vc, bt, L, 1 / 16, 0)
+    assert err == 0
+    want = oracle.paged_decode(q, kc, vc, bt, L, 1 / 16)
+    assert_close_attn(bf16_dev_to_f64(out), want, "d256 large")
+
+
 @pytest.mark.parametrize("window", [1, 2, 16, 17, 100, 512])
 def test_decode_window(pkv, window):
     rng = np.random.default_rng(window)
