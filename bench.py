@@ -55,11 +55,11 @@ _VAR_SRC = ("varlen.cu", "varlen_body.cuh", "tcgen05.cuh", "exp2_math.cuh", "com
 _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcgen05.cuh",
             "exp2_math.cuh", "common.cuh")
 TRAFFIC = {
-    "decode_qwen3": (320_301_824, _DEC_SRC, "94e78b36e07b1b4e"),
-    "decode_d512": (573_872_640, _DEC_SRC, "94e78b36e07b1b4e"),
+    "decode_qwen3": (320_480_512, _DEC_SRC, "3cc1187e033ba155"),
+    "decode_d512": (573_889_280, _DEC_SRC, "3cc1187e033ba155"),
     "varlen_mixed": (91_294_464, _VAR_SRC, "36237ec41593b2d7"),
     "varlen_d512": (44_015_616, _VAR_SRC, "36237ec41593b2d7"),
-    "mixed_single": (1_221_445_888, _MIX_SRC, "08bda397fa47bc44"),
+    "mixed_single": (1_218_637_568, _MIX_SRC, "fbcd298fac532031"),
     "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
     "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4b03849b8c981063"),
 }
