@@ -123,7 +123,11 @@ static cudaError_t launch_decode_s(DecodeArgs a, const void* k_cache, const void
   // persistent grid: every resident CTA takes items until the queue is empty
   const int64_t n = (int64_t)num_sms * per_sm;
   a.cta_count = (int32_t)n;
-  a.share_ctas = (int32_t)n;
+  // the cut rule's share: with two-head items on every SM, a segment is cut
+  // above half of a CTA's share of keys x heads (items of one head would be
+  // cut there too); the mixed-step kernel, whose decode starts on part of
+  // the SMs, keeps the finer cut of half a share of items
+  a.share_ctas = (int32_t)(HP == 2 ? (n + 1) / 2 : n);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n);
   cfg.blockDim = dim3((NW + 2) * 32);
@@ -161,11 +165,20 @@ static cudaError_t launch_decode_t(DecodeArgs a, const void* k_cache, const void
       return launch_decode_s<D, 2, 10, APPEND>(a, k_cache, v_cache, max_seq_len, stream,
                                                 num_sms);
   }
-  // One kv head per item here: with every SM streaming, the decode runs at
-  // HBM's rate either way, and items of one head balance the grid better
-  // (two-head items made the schedule cut the longest sequences of the
-  // qwen3 batch into merged chunks: 65.5 against 61.4 us).  The mixed-step
-  // kernel, whose decode runs on part of the SMs, takes two.
+  if constexpr (D == 128) {
+    // two kv heads per item (one 8 KB box per tile: half the boxes per
+    // byte): 12 stages of 16 KB, or 8.  On the qwen3 batch 59.4 against
+    // 61.4 us for one-head items (the cut rule counts keys, so two-head
+    // items are cut no more often)
+    if (decode_heads_per_item(D, a.H_kv, a.G) == 2) {
+      if (decode_fits<D, 4, 12, 2>(a))
+        return launch_decode_s<D, 4, 12, APPEND, 2>(a, k_cache, v_cache, max_seq_len, stream,
+                                                     num_sms);
+      if (decode_fits<D, 4, 8, 2>(a))
+        return launch_decode_s<D, 4, 8, APPEND, 2>(a, k_cache, v_cache, max_seq_len, stream,
+                                                    num_sms);
+    }
+  }
   if (decode_fits<D, C::NW, C::NSTAGE>(a))
     return launch_decode_s<D, C::NW, C::NSTAGE, APPEND>(a, k_cache, v_cache, max_seq_len,
                                                          stream, num_sms);

@@ -56,11 +56,10 @@ cudaError_t launch_rope_table(float* cos_sin, int32_t max_pos, int32_t D, double
 cudaError_t launch_kv_append_rope(const RopeAppendArgs& a, int32_t D, cudaStream_t stream,
                                   int num_sms);
 
-// kv heads per decode work item of the mixed-step kernel: two for head_dim
-// 128 with an even number of kv heads and a GQA group of at most 4 (one TMA
-// box then carries both heads' slice of a page: half the boxes per byte,
-// +20-27 % per-SM decode rate when the decode runs on part of the SMs),
-// else one.  The decode workspace is sized for the larger of the two.
+// kv heads per decode work item: two for head_dim 128 with an even number
+// of kv heads and a GQA group of at most 4 (one TMA box then carries both
+// heads' slice of a page: half the boxes per byte, +20-27 % per-SM decode
+// rate), else one.
 #ifndef PKV_DEC_HP2
 #define PKV_DEC_HP2 1
 #endif

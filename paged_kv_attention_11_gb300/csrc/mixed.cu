@@ -144,7 +144,9 @@ __device__ __forceinline__ void mixed_append_rows(const MixedArgs& m) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <int NSTAGE_DEC, int HP>
+// APPEND: paged_attn_mixed_append's build (the plain launch carries none of
+// the append's code)
+template <int NSTAGE_DEC, int HP, bool APPEND>
 __global__ void __launch_bounds__(kMixThreads, 1)
     mixed_step_kernel(const MixedArgs m, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmKv,
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kMixThreads, 1)
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int nd = m.var_first;
-  if (m.num_new > 0) mixed_append_rows(m);
+  if (APPEND) mixed_append_rows(m);
   if (m.has_var && (int)blockIdx.x >= nd)
     varlen_cta<kMixD, kMixNQ, kMixBN, kMixNS, kMixNKS, kMixNVS, true>(
         m.var, tmQ, tmKv, tmVv, smem, (int)blockIdx.x - nd, (int)gridDim.x - nd);
@@ -192,11 +194,11 @@ static int mixed_decode_ctas(int num_sms, int64_t dec_batch, int64_t dec_max_seq
   return num_sms - 1;
 }
 
-template <int NSTAGE_DEC, int HP>
-static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const void* k_cache,
+template <int NSTAGE_DEC, int HP, bool APPEND>
+static cudaError_t launch_mixed_k(MixedArgs& m, const VarlenMaps& vmaps, const void* k_cache,
                                   const void* v_cache, size_t smem, cudaStream_t stream,
                                   int num_sms) {
-  auto kern = mixed_step_kernel<NSTAGE_DEC, HP>;
+  auto kern = mixed_step_kernel<NSTAGE_DEC, HP, APPEND>;
   CUtensorMap tmKd, tmVd;
   if (!encode_pool_map_groups(&tmKd, k_cache, kMixD, m.dec.P, m.dec.num_pages, m.dec.H_kv, kTile,
                               0, HP) ||
@@ -224,6 +226,17 @@ static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const v
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, m, vmaps.q, vmaps.k, vmaps.v, tmKd, tmVd);
+}
+
+template <int NSTAGE_DEC, int HP>
+static cudaError_t launch_mixed_t(MixedArgs& m, const VarlenMaps& vmaps, const void* k_cache,
+                                  const void* v_cache, size_t smem, cudaStream_t stream,
+                                  int num_sms) {
+  if (m.num_new > 0)
+    return launch_mixed_k<NSTAGE_DEC, HP, true>(m, vmaps, k_cache, v_cache, smem, stream,
+                                                num_sms);
+  return launch_mixed_k<NSTAGE_DEC, HP, false>(m, vmaps, k_cache, v_cache, smem, stream,
+                                               num_sms);
 }
 
 cudaError_t launch_mixed(const MixedLaunch& L, const VarlenMaps& vmaps, cudaStream_t stream,

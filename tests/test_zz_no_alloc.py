@@ -58,13 +58,14 @@ def _longest_segment_is_split(lens, H_q, H_kv, P, n_sms, D):
     """The decode kernel cuts a segment (a sequence and its HP kv heads: two
     at head_dim 128 with an even kv-head count and a GQA group of at most 4,
     else one) into chunks when it has more 16-key tiles than half of one
-    CTA's share of the batch's item tiles (one persistent CTA per SM) and
-    more than 16, and the longest segment exceeds that cut by more than a
-    merge's cost (480 KB of K+V, 64*D*HP bytes per item tile)."""
+    CTA's share of the batch's head-tiles (16 keys of one kv head; one
+    persistent CTA per SM) and more than 16, and the longest segment
+    exceeds that cut by more than a merge's cost (480 KB of K+V, 64*D*HP
+    bytes per tile of the segment)."""
     G = H_q // H_kv
     hp = 2 if (D == 128 and H_kv % 2 == 0 and G <= 4) else 1
     tiles = -(-lens.astype(np.int64) // 16)
-    half_share = -(-int(tiles.sum()) * (H_kv // hp) // (2 * n_sms))
+    half_share = -(-int(tiles.sum()) * H_kv // (2 * n_sms))
     cut = max(16, half_share)
     return int(tiles.max()) > cut + (480 * 1024) // (64 * D * hp)
 
