@@ -43,11 +43,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # is reported only while the sources still have that hash; once the kernel
 # changes the field is null until a new capture replaces the entry.  The
 # summaries under profiles/ give the command and the other counters.
-#   decode_qwen3: decode_split_kernel<128,4,24,0,1> on the qwen3_decode step
+#   decode_qwen3: decode_split_kernel<128,4,12,0,2> on the qwen3_decode step
 #   decode_d512:  decode_split_kernel<512,2,4,0,1> on the head_dim 512 step
 #   varlen_mixed: varlen_fwd_kernel<128,2,128,1,3,2,128> on the mixed step
 #   varlen_d512:  varlen_fwd_kernel<512,1,32,2,2,2,256> on the head_dim 512 step
-#   mixed_single: mixed_step_kernel<12, 2> on the mixed step
+#   mixed_single: mixed_step_kernel<12,2,0> on the mixed step
 #   append_mixed: kv_append_kernel<2> on the mixed step (5645 rows)
 #   append_rope_mixed: kv_append_rope_kernel<128> on the mixed step, both norms
 _DEC_SRC = ("decode.cu", "decode_body.cuh", "tile16.cuh", "common.cuh")
@@ -55,11 +55,11 @@ _VAR_SRC = ("varlen.cu", "varlen_body.cuh", "tcgen05.cuh", "exp2_math.cuh", "com
 _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcgen05.cuh",
             "exp2_math.cuh", "common.cuh")
 TRAFFIC = {
-    "decode_qwen3": (320_480_512, _DEC_SRC, "3cc1187e033ba155"),
-    "decode_d512": (573_889_280, _DEC_SRC, "3cc1187e033ba155"),
+    "decode_qwen3": (320_193_536, _DEC_SRC, "47fb06d2bceb4501"),
+    "decode_d512": (573_851_648, _DEC_SRC, "47fb06d2bceb4501"),
     "varlen_mixed": (91_294_464, _VAR_SRC, "36237ec41593b2d7"),
     "varlen_d512": (44_015_616, _VAR_SRC, "36237ec41593b2d7"),
-    "mixed_single": (1_218_637_568, _MIX_SRC, "fbcd298fac532031"),
+    "mixed_single": (1_218_739_456, _MIX_SRC, "892345637f9c0f1b"),
     "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
     "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4b03849b8c981063"),
 }
