@@ -8,28 +8,36 @@
 // Design (GB300):
 //  * Work item = a (sequence, kv head) "segment" of 16-key tiles, or a chunk
 //    of one: a segment longer than half of a CTA's fair share of the batch
-//    is cut into equal chunks.  One persistent CTA per SM takes items from
-//    a device-side queue (an atomic counter in the workspace) in
-//    longest-first order, so the SMs finish together whatever the length
-//    mix, and only the few long segments need a merge.
+//    is cut into equal chunks (unless the longest segment is within a
+//    merge's cost of that length).  With HP = 2 (head_dim 128, an even
+//    kv-head count, GQA group <= 4) a segment covers two kv heads of the
+//    sequence: one TMA box per tile spans both heads' slice of a page.  One
+//    persistent CTA per SM takes items from a device-side queue (an atomic
+//    counter in the workspace) in longest-first order, so the SMs finish
+//    together whatever the length mix, and only the few long segments need
+//    a merge.
 //  * Producer warp: grabs the next item, writes a record (sequence, head,
-//    tiles, ...) and the G query rows into a 4-deep record ring in shared
-//    memory, then streams the item's K and V tiles: page ids from the
-//    block table (32 per coalesced load), TMA boxes per 16-key tile
-//    (128-byte swizzle) into a deep NSTAGE ring.
-//  * NW consumer warps: take the tiles of each item round-robin.  Per tile
-//    a warp computes S^T = K Q^T (16 keys x 8 heads, GQA group padded to
-//    8) with mma.sync, does the online softmax (exp2, warp shuffles),
-//    transposes P in registers with movmatrix and accumulates
+//    tiles, ...) and the item's query rows into a 4-deep record ring in
+//    shared memory, then streams the item's K and V tiles: page ids from
+//    the block table (32 per coalesced load), one TMA box per 16-key K or V
+//    tile (5-D page view, 128-byte swizzle) into a deep NSTAGE ring, each
+//    tile as soon as its stage is free.  The fused append (APPEND) writes
+//    the sequence's newest K/V row before the copies of the tile that
+//    holds it.
+//  * NW consumer warps: take the tiles of each item round-robin (with two
+//    heads per item, each warp of a pair takes one head of the pair's
+//    tiles).  Per tile a warp computes S^T = K Q^T (16 keys x 8 heads, GQA
+//    group padded to 8) with mma.sync, does the online softmax (exp2, warp
+//    shuffles), transposes P in registers with movmatrix and accumulates
 //    O^T = V^T P^T with mma.sync.  At the end of an item it hands its
 //    (m, l, O) state to the epilogue warp through a double buffer and goes
 //    straight on: no CTA-wide barrier in the stream.
 //  * Epilogue warp: combines the consumer states of an item (log-sum-exp
 //    weights); a whole segment is written as the bf16 output, a chunk as a
-//    partial (o, lse) in the workspace.  The last CTA to deliver a chunk of
-//    a segment -- found with a per-segment arrival counter -- merges the
-//    chunks and writes the output, then resets the counter.  The last CTA
-//    to find the queue empty resets the queue.  No CTA waits for another.
+//    partial (o, lse) in the workspace.  The CTA that delivers the last
+//    chunk of a segment (per-segment arrival counter) posts it to a merge
+//    queue; CTAs that have run out of items merge the posted segments with
+//    all their warps.  The last CTA to find the queue empty resets it.
 //  * K/V bytes are read from HBM exactly once.  Launched with programmatic
 //    dependent launch: the prologue overlaps the previous kernel in the
 //    stream; griddepcontrol.wait precedes every read of the inputs.

@@ -10,7 +10,9 @@
 // latency chain; run back to back, each leaves the other's resource idle.
 // Here one grid of one CTA per SM splits the step:
 //   * CTAs [0, nd) start with decode (the split-KV body, decode_cta, on
-//     warps 0-5; the dynamic longest-first queue in the workspace.  8
+//     warps 0-5; the dynamic longest-first queue in the workspace; items of
+//     two kv heads where the shape allows, whose 8 KB boxes raise the
+//     per-SM streaming rate that bounds a decode on part of the SMs.  8
 //     consumer warps on warps 0-9 measured no faster);
 //   * CTAs [nd, N) run the prefill chunks (the tcgen05 body, varlen_cta,
 //     with the static snake schedule over those N - nd CTAs), then join the
