@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -39,10 +40,11 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
 # from an ncu capture on a GB300, with the SHA-256 prefix of the kernel's
-# source files (concatenated, in the order listed) at capture time.  A value
-# is reported only while the sources still have that hash; once the kernel
-# changes the field is null until a new capture replaces the entry.  The
-# summaries under profiles/ give the command and the other counters.
+# source files (concatenated, in the order listed, comments and blank lines
+# removed: see source_digest) at capture time.  A value is reported only
+# while the sources still have that hash; once the kernel's code changes the
+# field is null until a new capture replaces the entry.  The summaries under
+# profiles/ give the command and the other counters.
 #   decode_qwen3: decode_split_kernel<128,4,12,0,2> on the qwen3_decode step
 #   decode_d512:  decode_split_kernel<512,2,4,0,1> on the head_dim 512 step
 #   varlen_mixed: varlen_fwd_kernel<128,2,128,1,3,2,128> on the mixed step
@@ -55,29 +57,47 @@ _VAR_SRC = ("varlen.cu", "varlen_body.cuh", "tcgen05.cuh", "exp2_math.cuh", "com
 _MIX_SRC = ("mixed.cu", "decode_body.cuh", "varlen_body.cuh", "tile16.cuh", "tcgen05.cuh",
             "exp2_math.cuh", "common.cuh")
 TRAFFIC = {
-    "decode_qwen3": (320_193_536, _DEC_SRC, "47fb06d2bceb4501"),
-    "decode_d512": (573_851_648, _DEC_SRC, "47fb06d2bceb4501"),
-    "varlen_mixed": (91_294_464, _VAR_SRC, "36237ec41593b2d7"),
-    "varlen_d512": (44_015_616, _VAR_SRC, "36237ec41593b2d7"),
-    "mixed_single": (1_218_739_456, _MIX_SRC, "892345637f9c0f1b"),
-    "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "72ace70d0176fb74"),
-    "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4b03849b8c981063"),
+    "decode_qwen3": (320_193_536, _DEC_SRC, "3dd9f216abb9b4be"),
+    "decode_d512": (573_851_648, _DEC_SRC, "3dd9f216abb9b4be"),
+    "varlen_mixed": (91_294_464, _VAR_SRC, "abd6d5929394aa53"),
+    "varlen_d512": (44_015_616, _VAR_SRC, "abd6d5929394aa53"),
+    "mixed_single": (1_218_739_456, _MIX_SRC, "4227504b9f00f717"),
+    "append_mixed": (23_259_648, ("append.cu", "common.cuh"), "afb5104dd69f82c8"),
+    "append_rope_mixed": (83_629_312, ("rope_append.cu",), "4dad9297abe899eb"),
 }
 
 
 def traffic_bytes(key: str):
     """The captured traffic of TRAFFIC[key], or None when a kernel source
     file has changed since the capture."""
-    import hashlib
     nbytes, files, sha = TRAFFIC[key]
-    m = hashlib.sha256()
+    texts = []
     try:
         for f in files:
-            with open(os.path.join(ROOT, "paged_kv_attention_11_gb300", "csrc", f), "rb") as fh:
-                m.update(fh.read())
+            with open(os.path.join(ROOT, "paged_kv_attention_11_gb300", "csrc", f)) as fh:
+                texts.append(fh.read())
     except OSError:
         return None
-    return nbytes if m.hexdigest()[:16] == sha else None
+    return nbytes if source_digest(texts) == sha else None
+
+
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/',
+                          re.DOTALL)
+
+
+def source_digest(texts) -> str:
+    """SHA-256 prefix (16 hex digits) of C/CUDA sources with their comments,
+    trailing blanks and empty lines removed, so that an edit of a comment
+    does not mark a capture as stale while any change of code does.  String
+    and character literals are kept as written."""
+    import hashlib
+    m = hashlib.sha256()
+    for text in texts:
+        code = _CODE_TOKENS.sub(lambda t: t.group(0) if t.group(0)[0] in "\"'" else " ", text)
+        lines = [ln.rstrip() for ln in code.splitlines()]
+        m.update("\n".join(ln for ln in lines if ln).encode())
+        m.update(b"\0")
+    return m.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------ helpers

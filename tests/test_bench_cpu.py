@@ -109,3 +109,17 @@ def test_traffic_entries_name_existing_sources():
             assert os.path.isfile(os.path.join(bench.ROOT, "paged_kv_attention_11_gb300", "csrc", f)), f
         assert len(sha) == 16 and nbytes > 0
         assert bench.traffic_bytes(key) in (nbytes, None)
+
+
+def test_source_digest_ignores_comments_not_code():
+    # a comment edit keeps a capture's traffic entry; a code edit (even one
+    # inside a string literal, or a changed operator) retires it
+    base = 'int f(int x) {  // twice x\n  /* doubled */ return 2 * x;\n}\nconst char* s = "a//b";\n'
+    d = bench.source_digest([base])
+    assert bench.source_digest([base.replace("twice x", "x times two")]) == d
+    assert bench.source_digest([base.replace("/* doubled */", "/* a\nlonger\nnote */")]) == d
+    assert bench.source_digest(["// header\n\n" + base + "\n\n"]) == d
+    assert bench.source_digest([base.replace("2 * x", "3 * x")]) != d
+    assert bench.source_digest([base.replace('"a//b"', '"a//c"')]) != d
+    # file boundaries count: the same text split differently is another digest
+    assert bench.source_digest([base, base]) != bench.source_digest([base + base])
