@@ -342,8 +342,8 @@ pkv_status paged_attn_mixed_append(
  *
  * Same arguments, semantics and results as paged_attn_decode, minus the
  * workspace: the scratch lives in one fixed 8 MiB (8388608-byte) array of
- * device memory inside the library, held by every GPU that loads the
- * library until the process exits.  A batch whose
+ * device memory inside the library, which a device holds from the time the
+ * array is placed there (below) until the process exits.  A batch whose
  * paged_attn_decode_workspace_size() exceeds 8 MiB is rejected with
  * PKV_ERR_UNSUPPORTED (message in pkv_last_cuda_error()).
  *
