@@ -368,6 +368,24 @@ def test_lse_matches_log_sum_exp():
     assert abs(lse[0, 0] - math.log(sum(math.exp(x) for x in s))) < 1e-13
 
 
+def test_key_blocks_merged_by_lse_equal_whole_attention():
+    # The split-KV decode and the shared-prefix (cascade) decode both rest on
+    # this identity of softmax attention: attending over disjoint key blocks
+    # and weighting each block's normalised output by exp(lse_i - lse), with
+    # lse = log(sum_i exp(lse_i)), gives the attention over all keys.
+    rng = np.random.default_rng(18)
+    L, H_kv, G, D = 37, 2, 3, 8
+    K, V = f64(rand_bits(rng, (L, H_kv, D))), f64(rand_bits(rng, (L, H_kv, D)))
+    q = f64(rand_bits(rng, (1, H_kv * G, D)))
+    whole = oracle.attend_rows(q, K, V, np.array([L - 1]), 0.35)
+    parts = [oracle.attend_rows(q, K[a:b], V[a:b], np.array([L]), 0.35, causal=False,
+                                return_lse=True) for a, b in ((0, 16), (16, 17), (17, L))]
+    lses = np.stack([lse for _, lse in parts])            # [blocks, 1, H_q]
+    total = np.log(np.exp(lses).sum(axis=0))
+    merged = sum(np.exp(lse - total)[..., None] * o for o, lse in parts)
+    np.testing.assert_allclose(merged, whole, rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------
 # append
 # ---------------------------------------------------------------------------
