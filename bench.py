@@ -532,8 +532,18 @@ def run_ours(args):
     dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers ---------------
-    e2e = None if args.only else run_e2e(ds, step, stream, flush, args, dbytes + abytes,
-                                         fused=fused_best)
+    e2e = None
+    if not args.only:
+        # copies on the copy engines (torch's copy_), then on the SMs
+        # (pkv_copy); the line reports the SM path, the other beside it
+        ce = run_e2e(ds, step, stream, flush, args, dbytes + abytes, fused=fused_best,
+                     sm_copy=False)
+        try:
+            e2e = run_e2e(ds, step, stream, flush, args, dbytes + abytes, fused=fused_best)
+            e2e["copy_engine"] = {"value": ce["value"], "ms_per_step": ce["ms_per_step"]}
+        except Exception as ex:  # pkv_copy refused these buffers: keep the copy engines
+            e2e = ce
+            e2e["sm_copy"] = {"unavailable": f"{type(ex).__name__}: {ex}"[:200]}
 
     # ---- secondary: mixed continuous-batching step (tokens/s) -------------
     mixed = None if args.only == "decode" else run_mixed(args, device, stream, flush, rank)
@@ -590,14 +600,17 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes, fused=True):
+def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes, fused=True,
+            sm_copy=True):
     """Same step through the public API, inputs from pinned host memory.
 
     The step's inputs (q, the new K/V rows, block table, lengths; the slot
     mapping too on the two-call path) sit in one pinned host buffer and go
     to the device in one copy, as an engine batches its step metadata; the
     output comes back in one copy.  ``fused``: paged_attn_decode_append
-    (one launch), else paged_kv_append then paged_attn_decode."""
+    (one launch), else paged_kv_append then paged_attn_decode.
+    ``sm_copy``: both copies by the library's pkv_copy (the SMs), else by
+    torch's copy_ (the copy engines)."""
     import torch
     parts = {"q": ds.q_dec, "k_new": ds.k_new, "v_new": ds.v_new, "bt": ds.dec_bt,
              "lens": ds.dec_lens}
@@ -624,7 +637,10 @@ def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes, fused=Tr
 
     def full(s):
         with torch.cuda.stream(s):
-            dev_buf.copy_(host_buf, non_blocking=True)
+            if sm_copy:
+                pkv.pkv_copy(dev_buf, host_buf, stream=s)
+            else:
+                dev_buf.copy_(host_buf, non_blocking=True)
             if fused:
                 pkv.paged_attn_decode_append(ds.out_dec, dev["q"], dev["k_new"], dev["v_new"],
                                              ds.k_cache, ds.v_cache, dev["bt"], dev["lens"],
@@ -636,15 +652,20 @@ def run_e2e(ds: DeviceStep, step: wl.Step, stream, flush, args, nbytes, fused=Tr
                 pkv.paged_attn_decode(ds.out_dec, dev["q"], ds.k_cache, ds.v_cache, dev["bt"],
                                       dev["lens"], step.max_seq_len_dec(), step.scale,
                                       step.window, workspace=ds.ws, err_flag=ds.err, stream=s)
-            out_h.copy_(ds.out_dec, non_blocking=True)
+            if sm_copy:
+                pkv.pkv_copy(out_h, ds.out_dec, stream=s)
+            else:
+                out_h.copy_(ds.out_dec, non_blocking=True)
 
     per = time_steps([full], args.steps, args.warmup, stream, flush, graphs=False)
     ms = float(np.mean([p[0] for p in per]))
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
-            "path": ("one H2D copy, paged_attn_decode_append, one D2H copy" if fused else
-                     "one H2D copy, paged_kv_append + paged_attn_decode, one D2H copy")}
+            "path": (("one H2D copy, paged_attn_decode_append, one D2H copy" if fused else
+                      "one H2D copy, paged_kv_append + paged_attn_decode, one D2H copy")
+                     + (" (both copies by pkv_copy on the SMs)" if sm_copy else
+                        " (both copies by the copy engines)"))}
 
 
 def run_mixed(args, device, stream, flush, rank):

@@ -11,8 +11,9 @@ same launch), ``paged_attn_mixed`` (a step's decode rows and prefill chunks
 in one launch), ``paged_attn_mixed_append`` (the same with the step's append
 fused in), ``paged_attn_decode_shared_prefix`` (decode that reads a prefix
 shared by a group of sequences once per group), ``paged_kv_append_rope`` (the
-append with q/k RMSNorm and the rotary embedding fused in) and
-``rope_table`` (its cos/sin table).
+append with q/k RMSNorm and the rotary embedding fused in),
+``rope_table`` (its cos/sin table) and ``pkv_copy`` (a step's host transfers
+done by the SMs).
 
 This module only marshals arguments (device pointers, sizes, the current
 CUDA stream) into the library; every step of the computation runs in the
@@ -39,6 +40,7 @@ from ._binding import (  # noqa: F401
     paged_attn_varlen,
     paged_kv_append,
     paged_kv_append_rope,
+    pkv_copy,
     rope_table,
     shared_prefix_workspace_size,
 )

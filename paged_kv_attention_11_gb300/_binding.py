@@ -49,6 +49,7 @@ _SIGS = {
     "pkv_rope_table": [_c_p, _c_i32, _c_i32, ctypes.c_double, _c_p],
     "paged_kv_append_rope": [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p,
                              _c_f, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i64, _c_p, _c_p],
+    "pkv_copy": [_c_p, _c_p, ctypes.c_size_t, _c_p],
     "pkv_status_string": [_c_i32],
     "pkv_last_cuda_error": [],
 }
@@ -365,6 +366,19 @@ def paged_attn_decode_static(out: torch.Tensor, q: torch.Tensor, k_cache: torch.
         block_table.shape[1], _ptr(seq_lens), B, H_q, H_kv, D, P, num_pages, int(max_seq_len),
         float(scale), int(window), _ptr(err_flag), _stream(stream)))
     return out
+
+
+def pkv_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy src into dst (same byte size, both contiguous) with the SMs:
+    device memory of the current device or pinned host memory on either
+    side, 16-byte aligned, a multiple of 16 bytes."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("pkv_copy: dst and src must be contiguous")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise ValueError("pkv_copy: dst and src differ in size")
+    _check("pkv_copy", lib().pkv_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)))
+    return dst
 
 
 def rope_table(cos_sin: torch.Tensor, theta: float, stream=None) -> torch.Tensor:

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libpkv.so")
 SOURCES = ["api.cu", "append.cu", "decode.cu", "varlen.cu", "decode_static.cu", "rope_append.cu",
-           "prefix.cu", "mixed.cu"]
+           "prefix.cu", "mixed.cu", "copy.cu"]
 HEADERS = ["common.cuh", "decode_body.cuh", "exp2_math.cuh", "kernels.h", "tcgen05.cuh",
            "tile16.cuh", "tmap.h", "varlen_body.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -86,6 +86,38 @@ const char* pkv_status_string(int32_t s) {
 
 const char* pkv_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
+pkv_status pkv_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src || bytes % 16 != 0 || !aligned16(dst) || !aligned16(src))
+    return PKV_ERR_INVALID;
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+  if (d < s + bytes && s < d + bytes) return PKV_ERR_INVALID;  // overlapping ranges
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // both ends must be memory this device reaches at the same address:
+  // its own device memory, or host memory pinned through CUDA (mapped at
+  // the same address under unified addressing)
+  for (const void* p : {static_cast<const void*>(dst), src}) {
+    cudaPointerAttributes at;
+    e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const bool ok = (at.type == cudaMemoryTypeDevice && at.device == dev) ||
+                    (at.type == cudaMemoryTypeManaged) ||
+                    (at.type == cudaMemoryTypeHost && at.devicePointer == p);
+    if (!ok) {
+      g_last_cuda_error =
+          "pkv_copy: each pointer must be device memory of the current device or pinned host "
+          "memory mapped at the same address";
+      return PKV_ERR_UNSUPPORTED;
+    }
+  }
+  int sms = 0;
+  if (int err = num_sms_current(&sms)) return cuda_fail((cudaError_t)err);
+  e = pkv::launch_copy16(dst, src, (int64_t)(bytes / 16), static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 pkv_status paged_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                            const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                            int32_t head_dim, int32_t page_size, int64_t num_pages,

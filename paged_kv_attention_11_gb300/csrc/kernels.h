@@ -31,6 +31,10 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
                              int32_t D, int32_t P, int64_t num_pages, int32_t* err,
                              cudaStream_t stream, int num_sms);
 
+// n16 16-byte words from src to dst by the SMs (copy.cu)
+cudaError_t launch_copy16(void* dst, const void* src, int64_t n16, cudaStream_t stream,
+                          int num_sms);
+
 // Arguments of the fused norm + rotary + append kernel (rope_append.cu).
 struct RopeAppendArgs {
   void* q;                      // [T, H_q, D] bf16, transformed in place; null: no q

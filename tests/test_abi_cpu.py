@@ -226,3 +226,15 @@ def test_mixed_append_validates_on_host(lib):
     assert call(ws=P + 64) == 1            # workspace not 256-byte aligned
     assert call(H_q=30) == 1               # H_q not a multiple of H_kv
     assert call(D=64) == 2                 # head_dim other than 128
+
+
+def test_copy_validates_on_host(lib):
+    # sizes, alignment and overlap are checked before any CUDA call
+    L = _bind(lib)
+    a, b = 1 << 20, 1 << 21
+    assert L.pkv_copy(b, a, 8, None) == 1          # not a multiple of 16
+    assert L.pkv_copy(b + 8, a, 16, None) == 1     # misaligned destination
+    assert L.pkv_copy(b, a + 4, 16, None) == 1     # misaligned source
+    assert L.pkv_copy(a + 16, a, 64, None) == 1    # overlapping ranges
+    assert L.pkv_copy(None, a, 16, None) == 1
+    assert L.pkv_copy(b, a, 0, None) == 0          # nothing to copy
